@@ -1,0 +1,263 @@
+"""CPU oracle of the MoE layer forward pass -- TEST INFRASTRUCTURE.
+
+A ctypes shim over ``moe_oracle.c`` (plain C, IEEE double). Only the test
+suite, the package smoke check and the benchmark's CPU-baseline leg may import
+this module; the product path never does, and nothing here imports the product
+package. ``moe_oracle.c`` names the page passage each step follows.
+
+bf16 tensors cross this boundary as their raw 16-bit patterns (numpy uint16).
+Torch CPU tensors are accepted and converted.
+
+``Oracle(path)`` wraps any build of the C source; the module-level functions use
+the default build next to this file. (The test suite also builds deliberately
+broken copies of the source to show that its pins catch planted mistakes.)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "moe_oracle.c")
+LIBRARY = os.path.join(HERE, "libmoe_oracle.so")
+CFLAGS = ["-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall", "-Wextra"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc build of an oracle source file (no -ffast-math: IEEE semantics)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, LIBRARY)
+    return LIBRARY
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _np(a, dtype):
+    """Contiguous numpy array of ``dtype``; bf16 torch tensors -> uint16 bits."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().cpu().contiguous()
+        if a.dtype == torch.bfloat16:
+            a = a.view(torch.int16).numpy().view(np.uint16)
+        else:
+            a = a.numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        if dtype == np.uint16:
+            raise TypeError("bf16 operands must be bf16 tensors or uint16 bit patterns")
+        a = np.ascontiguousarray(a.astype(dtype))
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@dataclass
+class OracleResult:
+    logits: np.ndarray     # [T, N] float64
+    topk_idx: np.ndarray   # [T, K] int32
+    topk_w: np.ndarray     # [T, K] float32
+    demand: np.ndarray     # [N] int32
+    P: np.ndarray          # [N] float64 (mean over tokens of the full softmax)
+    capacity: int
+    kept: np.ndarray       # [N] int32
+    offsets: np.ndarray    # [N+1] int32
+    slot_of: np.ndarray    # [T, K] int32
+    row_token: np.ndarray  # [T*K] int32
+    y_perm: Optional[np.ndarray]  # [R, d] uint16 (bf16 bits); rows of unwanted tokens are 0
+    z: Optional[np.ndarray]       # [T, d] uint16 or None
+    y: Optional[np.ndarray]       # [T, d] uint16; rows of unwanted tokens are 0
+    aux: float
+
+
+class Oracle:
+    def __init__(self, path: Optional[str] = None):
+        lib = ctypes.CDLL(path or build())
+        P = ctypes.c_void_p
+        i32, f64 = ctypes.c_int32, ctypes.c_double
+        lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_value.restype = f64
+        lib.oracle_bf16_round.argtypes = [f64]
+        lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_gelu.argtypes = [f64]
+        lib.oracle_gelu.restype = f64
+        lib.oracle_capacity.argtypes = [i32, i32, f64]
+        lib.oracle_capacity.restype = i32
+        lib.oracle_gate_logits.argtypes = [i32, i32, i32, P, P, P]
+        lib.oracle_route.argtypes = [i32, i32, i32, P, P, P, P, P, P]
+        lib.oracle_dispatch.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
+        lib.oracle_expert_rows.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
+        lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.oracle_shared_ffn.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
+        lib.oracle_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
+        lib.oracle_aux_loss.argtypes = [i32, i32, i32, f64, P, P]
+        lib.oracle_aux_loss.restype = f64
+        self.lib = lib
+
+    # ---- scalar helpers
+    def bf16_round(self, v: float) -> int:
+        return int(self.lib.oracle_bf16_round(float(v)))
+
+    def gelu(self, v: float) -> float:
+        return float(self.lib.oracle_gelu(float(v)))
+
+    def capacity(self, T: int, N: int, capacity_factor: float) -> int:
+        return int(self.lib.oracle_capacity(T, N, float(capacity_factor)))
+
+    # ---- stages
+    def gate_logits(self, x, Wg) -> np.ndarray:
+        x = _np(x, np.uint16)
+        Wg = _np(Wg, np.uint16)
+        T, d = x.shape
+        N = Wg.shape[0]
+        s = np.empty((T, N), dtype=np.float64)
+        self.lib.oracle_gate_logits(T, d, N, _p(x), _p(Wg), _p(s))
+        return s
+
+    def route(self, s, K: int, sel_bias=None):
+        s = _np(s, np.float64)
+        T, N = s.shape
+        sb = _np(sel_bias, np.float32)
+        idx = np.empty((T, K), dtype=np.int32)
+        w = np.empty((T, K), dtype=np.float32)
+        demand = np.empty((N,), dtype=np.int32)
+        P = np.empty((N,), dtype=np.float64)
+        self.lib.oracle_route(T, N, K, _p(s), _p(sb), _p(idx), _p(w), _p(demand), _p(P))
+        return idx, w, demand, P
+
+    def dispatch(self, idx, N: int, C: int):
+        idx = _np(idx, np.int32)
+        T, K = idx.shape
+        kept = np.empty((N,), dtype=np.int32)
+        offsets = np.empty((N + 1,), dtype=np.int32)
+        slot_of = np.empty((T, K), dtype=np.int32)
+        row_token = np.empty((T * K,), dtype=np.int32)
+        self.lib.oracle_dispatch(T, N, K, C, _p(idx), _p(kept), _p(offsets), _p(slot_of), _p(row_token))
+        return kept, offsets, slot_of, row_token
+
+    def expert_rows(self, x, rows, W1e, b1e, W2e, b2e) -> np.ndarray:
+        """One expert's FFN on x[rows[i]]."""
+        x = _np(x, np.uint16)
+        rows = _np(rows, np.int32)
+        W1e, W2e = _np(W1e, np.uint16), _np(W2e, np.uint16)
+        b1e, b2e = _np(b1e, np.float32), _np(b2e, np.float32)
+        d = x.shape[1]
+        f = W1e.shape[0]
+        out = np.empty((rows.shape[0], d), dtype=np.uint16)
+        self.lib.oracle_expert_rows(d, f, rows.shape[0], _p(rows), _p(x), _p(W1e), _p(b1e),
+                                    _p(W2e), _p(b2e), _p(out))
+        return out
+
+    def expert_ffn(self, x, offsets, row_token, W1, b1, W2, b2, want=None) -> np.ndarray:
+        x = _np(x, np.uint16)
+        offsets, row_token = _np(offsets, np.int32), _np(row_token, np.int32)
+        W1, W2 = _np(W1, np.uint16), _np(W2, np.uint16)
+        b1, b2 = _np(b1, np.float32), _np(b2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        N, f = W1.shape[0], W1.shape[1]
+        y_perm = np.zeros((max(int(offsets[N]), 0), d), dtype=np.uint16)
+        self.lib.oracle_expert_ffn(T, d, f, N, _p(offsets), _p(row_token), _p(x), _p(W1), _p(b1),
+                                   _p(W2), _p(b2), _p(want), _p(y_perm))
+        return y_perm
+
+    def shared_ffn(self, x, Ws1, bs1, Ws2, bs2, want=None) -> np.ndarray:
+        x = _np(x, np.uint16)
+        Ws1, Ws2 = _np(Ws1, np.uint16), _np(Ws2, np.uint16)
+        bs1, bs2 = _np(bs1, np.float32), _np(bs2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        f = Ws1.shape[0]
+        z = np.zeros((T, d), dtype=np.uint16)
+        self.lib.oracle_shared_ffn(T, d, f, _p(x), _p(Ws1), _p(bs1), _p(Ws2), _p(bs2), _p(want), _p(z))
+        return z
+
+    def combine(self, y_perm, slot_of, w, d: int, z=None, want=None) -> np.ndarray:
+        y_perm = _np(y_perm, np.uint16)
+        if y_perm.size == 0:
+            y_perm = np.zeros((1, d), dtype=np.uint16)  # never read: every slot is -1
+        slot_of = _np(slot_of, np.int32)
+        w = _np(w, np.float32)
+        z = _np(z, np.uint16)
+        want = _np(want, np.uint8)
+        T, K = slot_of.shape
+        y = np.zeros((T, d), dtype=np.uint16)
+        self.lib.oracle_combine(T, d, K, _p(y_perm), _p(slot_of), _p(w), _p(z), _p(want), _p(y))
+        return y
+
+    def aux_loss(self, demand, P, T: int, K: int, alpha: float) -> float:
+        demand = _np(demand, np.int32)
+        P = _np(P, np.float64)
+        return float(self.lib.oracle_aux_loss(T, demand.shape[0], K, float(alpha), _p(demand), _p(P)))
+
+    # ---- the whole layer
+    def forward(self, x, Wg, W1, b1, W2, b2, K: int, capacity_factor: float, aux_alpha: float,
+                sel_bias=None, Ws1=None, bs1=None, Ws2=None, bs2=None, want=None,
+                skip_ffn: bool = False) -> OracleResult:
+        """Full layer forward. Routing, dispatch and the aux loss always cover
+        every token; ``want`` (bool/uint8 [T], optional) limits the FFN and the
+        combine to a sample of tokens (the others' outputs are left 0)."""
+        x = _np(x, np.uint16)
+        T, d = x.shape
+        N = _np(Wg, np.uint16).shape[0]
+        s = self.gate_logits(x, Wg)
+        idx, w, demand, P = self.route(s, K, sel_bias)
+        C = self.capacity(T, N, capacity_factor)
+        kept, offsets, slot_of, row_token = self.dispatch(idx, N, C)
+        aux = self.aux_loss(demand, P, T, K, aux_alpha)
+        y_perm = z = y = None
+        if not skip_ffn:
+            want_u8 = None if want is None else np.ascontiguousarray(np.asarray(want).astype(np.uint8))
+            y_perm = self.expert_ffn(x, offsets, row_token, W1, b1, W2, b2, want_u8)
+            if Ws1 is not None:
+                z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
+            y = self.combine(y_perm, slot_of, w, d, z, want_u8)
+        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux)
+
+
+_default: Optional[Oracle] = None
+_lock = threading.Lock()
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle()
+    return _default
+
+
+def forward(*args, **kw) -> OracleResult:
+    return default().forward(*args, **kw)
+
+
+def forward_inputs(inp, want=None, skip_ffn: bool = False) -> OracleResult:
+    """Forward over an object with the fields of the seeded input generator
+    (x, Wg, W1, b1, W2, b2, sel_bias, Ws1, bs1, Ws2, bs2 and cfg)."""
+    c = inp.cfg
+    return default().forward(inp.x, inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, c.K, c.capacity_factor,
+                             c.aux_alpha, inp.sel_bias, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
+                             want=want, skip_ffn=skip_ffn)

@@ -1,0 +1,380 @@
+/*
+ * moe_oracle.c -- plain, slow, obviously-correct CPU oracle of the MoE layer
+ * forward pass (gate -> TopK -> softmax over the K kept logits -> dispatch
+ * under capacity -> expert FFN -> combine -> load-balancing loss).
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The product path never
+ * calls it. It shares no source, header, table or helper with the CUDA path.
+ *
+ * Arithmetic is IEEE double throughout. The only roundings to narrower types
+ * are the storage points the layer defines: routing weights are stored fp32,
+ * the expert hidden activation, the expert output, the shared-expert output and
+ * the layer output are stored bf16 (round to nearest, ties to even).
+ * Compile without -ffast-math.
+ *
+ * Sources (the MoE web pages this layer is defined by):
+ *  [Infra]  lmnt.cn/news/351908, an infrastructure-side walk-through of MoE:
+ *           sec. 2.1 (score = Softmax(TopK(W_g x)), TopK before softmax),
+ *           sec. 3.1 (dispatch = regroup token order into per-expert blocks),
+ *           sec. 3.2 (combine equation; same order as dispatch),
+ *           sec. 3.3 (capacity equation; overflow dropped to the residual),
+ *           sec. 5.1-5.2 (balance loss alpha*N*sum f_i P_i and its code).
+ *  [Yunthe] "MoE混合专家模型实战：专家路由与稀疏激活的推理成本优化方案"
+ *           (yunthe.com): output equation y = sum_{i in TopK} g_i(x) E_i(x),
+ *           the MoELayer listing (expert = Linear -> GELU -> Linear), and the
+ *           aux-loss-free per-expert selection bias b_i.
+ *  [Wiblog] "MoE 专家路由如何实现稀疏激活：从 Router 到专家并行的工程权衡"
+ *           (wiblog.cn): the always-on shared expert.
+ *
+ * Readings taken where the pages are silent (each is also a test):
+ *  - TopK order and ties: experts sorted by (u descending, expert id
+ *    ascending); output slot k holds the k-th of that order.
+ *  - The selection bias b (optional) is added to the logits only for the
+ *    selection; the softmax weights use the unbiased logits.
+ *  - Capacity is ceil(T/N * capacity_factor) evaluated in double exactly as
+ *    the [Infra] sec. 3.3 equation is written (no factor K); capacity_factor
+ *    <= 0 means dropless (capacity = T).
+ *  - Which assignments survive capacity: per expert, the first C tokens in
+ *    increasing token order (dispatch scans tokens in order).
+ *  - A dropped assignment contributes nothing; surviving weights are not
+ *    renormalised.
+ *  - f_i counts assignments before capacity, divided by T*K; P_i is the mean
+ *    over tokens of the softmax over all N unbiased logits.
+ *  - GELU is the erf form 0.5 v (1 + erf(v / sqrt 2)) (nn.GELU's default).
+ *  - The shared expert's output enters the combine with weight 1, first.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 */
+
+static double bf16_val(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 (8 significant bits, ties to even),
+ * directly from the double (no intermediate float rounding). */
+static uint16_t bf16_round(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    double a = fabs(v);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else {
+        int e;
+        frexp(a, &e);              /* a = m 2^e, m in [0.5, 1) */
+        int E = e - 1;             /* a = 1.xxx 2^E */
+        if (E < -126)
+            E = -126;              /* subnormal range: fixed ulp 2^-133 */
+        /* nearbyint rounds half to even under the default rounding mode */
+        r = ldexp(nearbyint(ldexp(a, 7 - E)), E - 7);
+        if (r >= 0x1p128)
+            r = INFINITY;
+    }
+    float fr = (float)(signbit(v) ? -r : r); /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &fr, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+double oracle_bf16_value(uint16_t b) { return bf16_val(b); }
+uint16_t oracle_bf16_round(double v) { return bf16_round(v); }
+
+/* ---------------------------------------------------------------- capacity */
+
+/* [Infra] sec. 3.3: capacity = ceil(T / N * capacity_factor). */
+int oracle_capacity(int T, int N, double capacity_factor)
+{
+    if (capacity_factor <= 0.0)
+        return T;
+    double c = ceil((double)T / (double)N * capacity_factor);
+    if (c > (double)T)
+        c = (double)T;
+    if (c < 0.0)
+        c = 0.0;
+    return (int)c;
+}
+
+/* ---------------------------------------------------------------- gate */
+
+/* [Infra] sec. 2.1: logits = W_g x, one linear map with no bias.
+ * s[t*N + e] = sum_j x[t, j] * Wg[e, j]. */
+void oracle_gate_logits(int T, int d, int N, const uint16_t *x, const uint16_t *Wg, double *s)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < N; ++e) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j)
+                acc += bf16_val(x[(size_t)t * d + j]) * bf16_val(Wg[(size_t)e * d + j]);
+            s[(size_t)t * N + e] = acc;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- route */
+
+typedef struct {
+    double u;
+    int e;
+} scored_expert;
+
+/* Sort order: larger u first; equal u -> smaller expert id first. */
+static int cmp_scored(const void *pa, const void *pb)
+{
+    const scored_expert *a = (const scored_expert *)pa, *b = (const scored_expert *)pb;
+    if (a->u > b->u)
+        return -1;
+    if (a->u < b->u)
+        return 1;
+    return (a->e > b->e) - (a->e < b->e);
+}
+
+/* [Infra] sec. 2.1 (TopK over the N logits first, then softmax over only the
+ * K kept logits) and sec. 5.2 (the balance-loss statistics).
+ *   s        [T, N]  unbiased gate logits
+ *   sel_bias [N]     optional selection-only bias ([Yunthe], b_i), may be NULL
+ * Outputs:
+ *   idx      [T, K]  selected experts in rank order
+ *   w        [T, K]  softmax of the K unbiased logits, stored fp32
+ *   demand   [N]     number of (t, k) with idx == e (before capacity)
+ *   P        [N]     mean over t of softmax over all N unbiased logits */
+void oracle_route(int T, int N, int K, const double *s, const float *sel_bias,
+                  int32_t *idx, float *w, int32_t *demand, double *P)
+{
+    scored_expert *buf = (scored_expert *)malloc(sizeof(scored_expert) * (size_t)N);
+    double *ex = (double *)malloc(sizeof(double) * (size_t)N);
+    for (int e = 0; e < N; ++e) {
+        demand[e] = 0;
+        P[e] = 0.0;
+    }
+    for (int t = 0; t < T; ++t) {
+        const double *st = s + (size_t)t * N;
+        for (int e = 0; e < N; ++e) {
+            buf[e].u = st[e] + (sel_bias ? (double)sel_bias[e] : 0.0);
+            buf[e].e = e;
+        }
+        qsort(buf, (size_t)N, sizeof(scored_expert), cmp_scored);
+
+        /* softmax over the K kept, unbiased logits */
+        double m = -INFINITY;
+        for (int k = 0; k < K; ++k)
+            if (st[buf[k].e] > m)
+                m = st[buf[k].e];
+        double z = 0.0;
+        for (int k = 0; k < K; ++k)
+            z += exp(st[buf[k].e] - m);
+        for (int k = 0; k < K; ++k) {
+            idx[(size_t)t * K + k] = buf[k].e;
+            w[(size_t)t * K + k] = (float)(exp(st[buf[k].e] - m) / z);
+            demand[buf[k].e] += 1;
+        }
+
+        /* softmax over all N unbiased logits, for P_i */
+        double mn = -INFINITY;
+        for (int e = 0; e < N; ++e)
+            if (st[e] > mn)
+                mn = st[e];
+        double zn = 0.0;
+        for (int e = 0; e < N; ++e) {
+            ex[e] = exp(st[e] - mn);
+            zn += ex[e];
+        }
+        for (int e = 0; e < N; ++e)
+            P[e] += ex[e] / zn;
+    }
+    for (int e = 0; e < N; ++e)
+        P[e] /= (double)T;
+    free(ex);
+    free(buf);
+}
+
+/* ---------------------------------------------------------------- dispatch */
+
+/* [Infra] sec. 3.1 and 3.3: regroup the (token, rank) assignments into one
+ * contiguous block per expert, tokens in increasing order inside a block, and
+ * keep only the first C of each expert.
+ * Outputs:
+ *   kept    [N]      min(demand[e], C)
+ *   offsets [N + 1]  exclusive prefix sum of kept (offsets[N] = rows kept, R)
+ *   slot_of [T, K]   global row of assignment (t, k) in the regrouped buffer,
+ *                    or -1 when it was dropped
+ *   row_token [T*K]  token of each kept row (entries >= R are set to -1) */
+void oracle_dispatch(int T, int N, int K, int C, const int32_t *idx,
+                     int32_t *kept, int32_t *offsets, int32_t *slot_of, int32_t *row_token)
+{
+    int32_t *seen = (int32_t *)calloc((size_t)N, sizeof(int32_t));
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k)
+            seen[idx[(size_t)t * K + k]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < N; ++e) {
+        kept[e] = seen[e] < C ? seen[e] : C;
+        offsets[e + 1] = offsets[e] + kept[e];
+        seen[e] = 0;
+    }
+    for (int r = 0; r < T * K; ++r)
+        row_token[r] = -1;
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int e = idx[(size_t)t * K + k];
+            int p = seen[e]++;
+            if (p < C) {
+                int row = offsets[e] + p;
+                slot_of[(size_t)t * K + k] = row;
+                row_token[row] = t;
+            } else {
+                slot_of[(size_t)t * K + k] = -1;
+            }
+        }
+    }
+    free(seen);
+}
+
+/* ---------------------------------------------------------------- expert FFN */
+
+static double gelu_erf(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+
+double oracle_gelu(double v) { return gelu_erf(v); }
+
+/* [Yunthe] MoELayer listing: expert = Linear(d_model -> d_ff) -> GELU ->
+ * Linear(d_ff -> d_model), nn.Linear layout [out, in].
+ *   h = bf16(GELU(x W1^T + b1)),   out = bf16(h W2^T + b2). */
+static void ffn_row(int d, int f, const uint16_t *xrow, const uint16_t *W1e, const float *b1e,
+                    const uint16_t *W2e, const float *b2e, double *xd, double *h, uint16_t *out)
+{
+    for (int i = 0; i < d; ++i)
+        xd[i] = bf16_val(xrow[i]);
+    for (int j = 0; j < f; ++j) {
+        const uint16_t *wr = W1e + (size_t)j * d;
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i)
+            acc += xd[i] * bf16_val(wr[i]);
+        acc += (double)b1e[j];
+        h[j] = bf16_val(bf16_round(gelu_erf(acc)));
+    }
+    for (int c = 0; c < d; ++c) {
+        const uint16_t *wr = W2e + (size_t)c * f;
+        double acc = 0.0;
+        for (int j = 0; j < f; ++j)
+            acc += h[j] * bf16_val(wr[j]);
+        acc += (double)b2e[c];
+        out[c] = bf16_round(acc);
+    }
+}
+
+/* One expert FFN on a list of rows: out[i] = E(x[rows[i]]). */
+void oracle_expert_rows(int d, int f, int nrows, const int32_t *rows, const uint16_t *x,
+                        const uint16_t *W1e, const float *b1e, const uint16_t *W2e,
+                        const float *b2e, uint16_t *out)
+{
+#pragma omp parallel
+    {
+        double *xd = (double *)malloc(sizeof(double) * (size_t)d);
+        double *h = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int i = 0; i < nrows; ++i)
+            ffn_row(d, f, x + (size_t)rows[i] * d, W1e, b1e, W2e, b2e, xd, h, out + (size_t)i * d);
+        free(h);
+        free(xd);
+    }
+}
+
+/* The regrouped expert computation: for every kept row r of the dispatch
+ * (expert e = the block r lies in, token t = row_token[r]),
+ *   y_perm[r] = E_e(x[t]).
+ * Rows whose token has want[t] == 0 are skipped (want may be NULL = all). */
+void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
+                       const uint16_t *x, const uint16_t *W1, const float *b1, const uint16_t *W2,
+                       const float *b2, const uint8_t *want, uint16_t *y_perm)
+{
+    int R = offsets[N];
+    int *row_expert = (int *)malloc(sizeof(int) * (size_t)(R > 0 ? R : 1));
+    for (int e = 0; e < N; ++e)
+        for (int r = offsets[e]; r < offsets[e + 1]; ++r)
+            row_expert[r] = e;
+    (void)T;
+#pragma omp parallel
+    {
+        double *xd = (double *)malloc(sizeof(double) * (size_t)d);
+        double *h = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < R; ++r) {
+            int t = row_token[r];
+            if (want && !want[t])
+                continue;
+            int e = row_expert[r];
+            ffn_row(d, f, x + (size_t)t * d, W1 + (size_t)e * f * d, b1 + (size_t)e * f,
+                    W2 + (size_t)e * d * f, b2 + (size_t)e * d, xd, h, y_perm + (size_t)r * d);
+        }
+        free(h);
+        free(xd);
+    }
+    free(row_expert);
+}
+
+/* [Wiblog] shared expert: the same FFN applied to every token (want may be NULL). */
+void oracle_shared_ffn(int T, int d, int f, const uint16_t *x, const uint16_t *Ws1, const float *bs1,
+                       const uint16_t *Ws2, const float *bs2, const uint8_t *want, uint16_t *z)
+{
+#pragma omp parallel
+    {
+        double *xd = (double *)malloc(sizeof(double) * (size_t)d);
+        double *h = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int t = 0; t < T; ++t) {
+            if (want && !want[t])
+                continue;
+            ffn_row(d, f, x + (size_t)t * d, Ws1, bs1, Ws2, bs2, xd, h, z + (size_t)t * d);
+        }
+        free(h);
+        free(xd);
+    }
+}
+
+/* ---------------------------------------------------------------- combine */
+
+/* [Infra] sec. 3.2: output[t] = sum_{e in selected(t)} weight[t, e] *
+ * expert_output_e, read back through the dispatch table in the same (rank)
+ * order the dispatch used. Dropped assignments (slot -1) add nothing. The
+ * shared expert's output, when given, enters first with weight 1. */
+void oracle_combine(int T, int d, int K, const uint16_t *y_perm, const int32_t *slot_of,
+                    const float *w, const uint16_t *z, const uint8_t *want, uint16_t *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        if (want && !want[t])
+            continue;
+        for (int c = 0; c < d; ++c) {
+            double acc = z ? bf16_val(z[(size_t)t * d + c]) : 0.0;
+            for (int k = 0; k < K; ++k) {
+                int r = slot_of[(size_t)t * K + k];
+                if (r < 0)
+                    continue;
+                acc += (double)w[(size_t)t * K + k] * bf16_val(y_perm[(size_t)r * d + c]);
+            }
+            y[(size_t)t * d + c] = bf16_round(acc);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- balance loss */
+
+/* [Infra] sec. 5.1-5.2: L = alpha * N * sum_i f_i P_i with
+ * f_i = demand_i / (T K) and P_i the mean softmax probability of expert i. */
+double oracle_aux_loss(int T, int N, int K, double alpha, const int32_t *demand, const double *P)
+{
+    double acc = 0.0;
+    for (int e = 0; e < N; ++e)
+        acc += ((double)demand[e] / ((double)T * (double)K)) * P[e];
+    return alpha * (double)N * acc;
+}

@@ -1,0 +1,393 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` takes an ``Oracle`` and raises AssertionError when the oracle
+disagrees with a closed form, an invariant, a library routine on a special
+case, brute force on a tiny input, or the worked example printed on the pages.
+``test_oracle.py`` runs them on the real oracle; ``test_oracle_mutations.py``
+runs them on deliberately broken copies of the oracle to show each planted
+mistake is caught.
+"""
+
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from oracle import bf16_to_f64
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------ helpers
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def grid_x(rng, T, d):
+    return bits(torch.from_numpy(rng.integers(-128, 129, (T, d)) / 64.0).to(torch.bfloat16))
+
+
+def grid_wg(rng, N, d, lo=-8, hi=8):
+    return bits(torch.from_numpy(rng.integers(lo, hi + 1, (N, d)) / 64.0).to(torch.bfloat16))
+
+
+def randn_bf16(rng, shape, std):
+    return bits(torch.from_numpy(rng.standard_normal(shape) * std).to(torch.float32).to(torch.bfloat16))
+
+
+def torch_expert(xb, W1e, b1e, W2e, b2e) -> np.ndarray:
+    """Dense FFN through torch's float64 library ops: Linear -> GELU (erf) ->
+    bf16 -> Linear -> bf16. Independent of the oracle's C code."""
+    x = torch.from_numpy(bf16_to_f64(xb))
+    W1 = torch.from_numpy(bf16_to_f64(W1e))
+    W2 = torch.from_numpy(bf16_to_f64(W2e))
+    b1 = torch.from_numpy(np.asarray(b1e, np.float64))
+    b2 = torch.from_numpy(np.asarray(b2e, np.float64))
+    h = F.gelu(F.linear(x, W1, b1)).to(torch.bfloat16).to(torch.float64)
+    return F.linear(h, W2, b2).numpy()
+
+
+def to_bf16_bits_f64(v: np.ndarray) -> np.ndarray:
+    return bits(torch.from_numpy(np.asarray(v, np.float64)).to(torch.bfloat16))
+
+
+def assert_bf16_close(got_bits, ref_bits, max_mismatch_frac=1e-3, what=""):
+    """bf16 results equal bit for bit, except a small fraction (double rounding
+    through float32 in torch's float64->bf16 cast) which must lie within one
+    bf16 ulp."""
+    got_bits = np.asarray(got_bits, np.uint16)
+    ref_bits = np.asarray(ref_bits, np.uint16)
+    assert got_bits.shape == ref_bits.shape, what
+    diff = got_bits != ref_bits
+    frac = diff.mean() if diff.size else 0.0
+    assert frac <= max_mismatch_frac, f"{what}: {frac:.4%} of bf16 values differ"
+    if diff.any():
+        g = bf16_to_f64(got_bits[diff])
+        r = bf16_to_f64(ref_bits[diff])
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-30))) - 7)
+        assert np.all(np.abs(g - r) <= ulp * 1.0001), f"{what}: a differing value is more than 1 ulp off"
+
+
+# ------------------------------------------------------------------ bf16 rounding
+
+def pin_bf16_round(orc):
+    """Double -> bf16 RNE matches torch's float32 -> bf16 cast on values that
+    float32 holds exactly, including exact halfway cases (ties to even)."""
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(4000).astype(np.float32) * np.exp2(rng.integers(-20, 20, 4000)).astype(np.float32)
+    # exact midpoints between neighbouring bf16 values: low 16 bits = 0x8000
+    mids = (rng.integers(0x3000, 0x5000, 200).astype(np.uint32) << 16 | 0x8000).view(np.float32)
+    v = np.concatenate([v, mids, np.float32([0.0, -0.0, 1.0, -3.5])])
+    ref = bits(torch.from_numpy(v).to(torch.bfloat16))
+    got = np.array([orc.bf16_round(float(a)) for a in v], dtype=np.uint16)
+    assert np.array_equal(got, ref), "bf16 rounding differs from torch's RNE cast"
+    assert orc.bf16_round(1 + 2 ** -8) == 0x3F80       # halfway -> even (1.0)
+    assert orc.bf16_round(1 + 3 * 2 ** -8) == 0x3F82   # halfway -> even (1 + 2^-6)
+
+
+# ------------------------------------------------------------------ GELU
+
+def pin_gelu(orc):
+    """erf-form GELU: torch's exact GELU in float64 and the limits."""
+    xs = np.linspace(-8, 8, 401)
+    ref = F.gelu(torch.from_numpy(xs), approximate="none").numpy()
+    got = np.array([orc.gelu(float(a)) for a in xs])
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-15)
+    assert orc.gelu(0.0) == 0.0
+    assert abs(orc.gelu(30.0) - 30.0) < 1e-12 and abs(orc.gelu(-30.0)) < 1e-12
+    assert abs(orc.gelu(1.0) - 0.5 * (1 + math.erf(1 / math.sqrt(2)))) < 1e-15
+
+
+# ------------------------------------------------------------------ capacity
+
+def pin_capacity(orc):
+    """capacity = ceil(T / N * capacity_factor); dropless (cf <= 0) = T."""
+    assert orc.capacity(256, 8, 1.25) == 40
+    assert orc.capacity(4096, 8, 1.25) == 640
+    assert orc.capacity(8192, 64, 1.0) == 128
+    assert orc.capacity(4096, 256, 0.0) == 4096
+    assert orc.capacity(10, 3, 1.0) == 4      # ceil(3.33)
+    assert orc.capacity(7, 2, 1.5) == 6       # ceil(5.25)
+    assert orc.capacity(16, 8, 2.0) == 4
+    assert orc.capacity(5, 8, 100.0) == 5     # never above T
+
+
+# ------------------------------------------------------------------ gate
+
+def pin_gate_exact(orc):
+    """On the 1/64 grid every logit is an integer multiple of 2^-12: check it
+    against int64 matrix arithmetic (exact)."""
+    rng = np.random.default_rng(2)
+    T, d, N = 37, 96, 5
+    x = grid_x(rng, T, d)
+    Wg = grid_wg(rng, N, d)
+    s = orc.gate_logits(x, Wg)
+    xi = np.rint(bf16_to_f64(x) * 64).astype(np.int64)
+    wi = np.rint(bf16_to_f64(Wg) * 64).astype(np.int64)
+    ref = (xi @ wi.T).astype(np.float64) / 4096.0
+    assert s.shape == (T, N)
+    assert np.array_equal(s, ref)
+
+
+# ------------------------------------------------------------------ route
+
+def _brute_topk(u_row, K):
+    """Lexicographically smallest id set among the K-subsets of maximal sum."""
+    best, best_set = None, None
+    for comb in itertools.combinations(range(len(u_row)), K):  # lexicographic order
+        sm = sum(u_row[i] for i in comb)
+        if best is None or sm > best:
+            best, best_set = sm, comb
+    return set(best_set)
+
+
+def pin_route_bruteforce(orc):
+    """Selection = the maximal-sum K-subset (smallest ids on ties), ranked by
+    value then id; weights = softmax of the K unbiased logits (scipy)."""
+    rng = np.random.default_rng(3)
+    for N, K, with_bias in [(6, 1, False), (6, 2, False), (6, 3, True), (5, 5, False), (7, 2, True)]:
+        T = 48
+        s = rng.integers(-3, 4, (T, N)).astype(np.float64)  # small range: ties are common
+        bias = (rng.integers(-2, 3, N) / 2.0).astype(np.float32) if with_bias else None
+        idx, w, demand, P = orc.route(s, K, bias)
+        u = s + (bias.astype(np.float64) if with_bias else 0.0)
+        for t in range(T):
+            assert set(idx[t].tolist()) == _brute_topk(u[t], K), (N, K, t)
+            assert len(set(idx[t].tolist())) == K
+            for k in range(K - 1):
+                a, b = idx[t, k], idx[t, k + 1]
+                assert u[t, a] > u[t, b] or (u[t, a] == u[t, b] and a < b)
+            ref = scipy.special.softmax(s[t, idx[t]])
+            assert np.allclose(w[t], ref, rtol=2e-7, atol=1e-12)
+        assert np.array_equal(demand, np.bincount(idx.ravel(), minlength=N))
+        assert np.allclose(P, scipy.special.softmax(s, axis=1).mean(0), rtol=1e-13, atol=1e-15)
+
+
+def pin_route_closed_forms(orc):
+    """K=2: w0 = sigmoid(s_a - s_b); K=1: w = 1; sum of weights = 1; all-equal
+    logits select experts 0..K-1; a selection bias moves the choice but not
+    the weights."""
+    rng = np.random.default_rng(4)
+    s = rng.standard_normal((64, 8)) * 3
+    idx, w, _, _ = orc.route(s, 2)
+    d = s[np.arange(64), idx[:, 0]] - s[np.arange(64), idx[:, 1]]
+    assert np.allclose(w[:, 0], scipy.special.expit(d), rtol=2e-7)
+    assert np.all(d >= 0)
+    assert np.all(np.abs(w.sum(1) - 1) < 2e-7)
+    idx1, w1, _, _ = orc.route(s, 1)
+    assert np.all(w1 == 1.0) and np.array_equal(idx1[:, 0], np.argmax(s, axis=1))
+    idxe, _, _, _ = orc.route(np.zeros((3, 8)), 4)
+    assert np.array_equal(idxe, np.tile(np.arange(4), (3, 1)))
+    sb = np.array([[1.0, 0.0, 0.5]])
+    idxb, wb, _, _ = orc.route(sb, 2, np.float32([0.0, 2.0, 0.0]))
+    assert idxb.tolist() == [[1, 0]]
+    assert np.allclose(wb[0], [scipy.special.expit(-1.0), scipy.special.expit(1.0)], rtol=2e-7)
+
+
+def pin_worked_example(orc):
+    """The pages' worked top-2 example (the selection; the weights follow the
+    formula -- see the fixture for why the printed 0.62 is not pinned)."""
+    with open(os.path.join(GOLDEN, "worked_example_top2.json")) as fh:
+        g = json.load(fh)
+    idx, w, _, _ = orc.route(np.array([g["logits"]]), g["K"])
+    assert idx[0].tolist() == g["expected_idx"]
+    assert [i + 1 for i in idx[0]] == g["page_selected_1based"]
+    assert np.allclose(w[0], g["expected_weights"], rtol=1e-7)
+
+
+# ------------------------------------------------------------------ dispatch
+
+def _brute_dispatch(idx, N, C):
+    """Stable sort of all (expert, token) pairs, keep the first C per expert."""
+    T, K = idx.shape
+    pairs = sorted(((int(idx[t, k]), t, k) for t in range(T) for k in range(K)),
+                   key=lambda p: (p[0], p[1]))
+    slot = -np.ones((T, K), np.int64)
+    rows = []
+    per = {}
+    for e, t, k in pairs:
+        if per.get(e, 0) < C:
+            per[e] = per.get(e, 0) + 1
+            slot[t, k] = len(rows)
+            rows.append(t)
+    kept = np.array([per.get(e, 0) for e in range(N)])
+    return slot, np.array(rows, dtype=np.int64), kept
+
+
+def pin_dispatch_bruteforce(orc):
+    rng = np.random.default_rng(5)
+    for T, N, K, C in [(40, 5, 2, 6), (40, 5, 2, 40), (33, 8, 3, 4), (20, 4, 1, 3), (16, 6, 6, 9)]:
+        s = rng.standard_normal((T, N))
+        idx, _, demand, _ = orc.route(s, K)
+        kept, offsets, slot_of, row_token = orc.dispatch(idx, N, C)
+        slot, rows, kept_ref = _brute_dispatch(idx, N, C)
+        assert np.array_equal(slot_of, slot)
+        R = len(rows)
+        assert offsets[N] == R and np.array_equal(row_token[:R], rows)
+        assert np.all(row_token[R:] == -1)
+        assert np.array_equal(kept, kept_ref) and np.array_equal(kept, np.minimum(demand, C))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(kept)]))
+        # round trip: kept slots form a bijection onto [0, R) and point back to their token
+        live = slot_of[slot_of >= 0]
+        assert np.array_equal(np.sort(live), np.arange(R))
+        tt = np.repeat(np.arange(T)[:, None], K, 1)
+        assert np.array_equal(row_token[slot_of[slot_of >= 0]], tt[slot_of >= 0])
+
+
+def pin_permutation_roundtrip(orc):
+    """Gathering x by row_token and scattering back through slot_of restores x."""
+    rng = np.random.default_rng(6)
+    T, d, N, K = 50, 16, 6, 2
+    x = grid_x(rng, T, d)
+    idx, _, _, _ = orc.route(rng.standard_normal((T, N)), K)
+    kept, offsets, slot_of, row_token = orc.dispatch(idx, N, T)
+    R = offsets[N]
+    assert R == T * K
+    x_perm = x[row_token[:R]]
+    for e in range(N):  # contiguous per-expert blocks, tokens increasing
+        blk = row_token[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(blk) > 0)
+        assert np.all((idx[blk] == e).any(axis=1))
+    for k in range(K):
+        assert np.array_equal(x_perm[slot_of[:, k]], x)
+
+
+# ------------------------------------------------------------------ FFN and combine
+
+def _small_layer(rng, T, d, f, N):
+    x = grid_x(rng, T, d)
+    Wg = grid_wg(rng, N, d)
+    W1 = randn_bf16(rng, (N, f, d), d ** -0.5)
+    b1 = (rng.standard_normal((N, f)) * 0.02).astype(np.float32)
+    W2 = randn_bf16(rng, (N, d, f), f ** -0.5)
+    b2 = (rng.standard_normal((N, d)) * 0.02).astype(np.float32)
+    return x, Wg, W1, b1, W2, b2
+
+
+def pin_dense_special_case(orc):
+    """N = 1, K = 1, dropless: the layer is one dense FFN (torch float64 ops)."""
+    rng = np.random.default_rng(7)
+    T, d, f = 24, 32, 48
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, 1)
+    r = orc.forward(x, Wg, W1, b1, W2, b2, K=1, capacity_factor=0.0, aux_alpha=0.01)
+    ref = to_bf16_bits_f64(torch_expert(x, W1[0], b1[0], W2[0], b2[0]))
+    assert np.all(r.topk_w == 1.0)
+    assert_bf16_close(r.y, ref, what="dense FFN")
+
+
+def pin_identical_experts(orc):
+    """All experts share weights and nothing is dropped: the weights sum to 1
+    within fp32 rounding, which cannot move a bf16 value, so y == E(x)."""
+    rng = np.random.default_rng(8)
+    T, d, f, N, K = 40, 32, 64, 4, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, 1)
+    W1n, b1n = np.repeat(W1, N, 0), np.repeat(b1, N, 0)
+    W2n, b2n = np.repeat(W2, N, 0), np.repeat(b2, N, 0)
+    Wg = grid_wg(rng, N, d)
+    r = orc.forward(x, Wg, W1n, b1n, W2n, b2n, K=K, capacity_factor=0.0, aux_alpha=0.01)
+    single = orc.expert_rows(x, np.arange(T, dtype=np.int32), W1[0], b1[0], W2[0], b2[0])
+    assert np.array_equal(r.y, single)
+    assert_bf16_close(single, to_bf16_bits_f64(torch_expert(x, W1[0], b1[0], W2[0], b2[0])),
+                      what="shared-weight expert")
+
+
+def pin_token_major(orc):
+    """Dropless, distinct experts: y[t] = bf16(sum_k w[t,k] E_{idx[t,k]}(x_t)),
+    evaluated token by token with torch, no permutation at all."""
+    rng = np.random.default_rng(9)
+    T, d, f, N, K = 30, 32, 48, 5, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    r = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=0.0, aux_alpha=0.01)
+    out = np.zeros((T, d))
+    for e in range(N):
+        o = bf16_to_f64(to_bf16_bits_f64(torch_expert(x, W1[e], b1[e], W2[e], b2[e])))
+        for k in range(K):
+            sel = r.topk_idx[:, k] == e
+            out[sel] += r.topk_w[sel, k].astype(np.float64)[:, None] * o[sel]
+    assert_bf16_close(r.y, to_bf16_bits_f64(out), max_mismatch_frac=3e-3, what="token-major")
+
+
+def pin_soft_router(orc):
+    """K = N ('soft router'): y = sum_e softmax(s)_e E_e(x)."""
+    rng = np.random.default_rng(10)
+    T, d, f, N = 20, 32, 32, 4
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    r = orc.forward(x, Wg, W1, b1, W2, b2, K=N, capacity_factor=0.0, aux_alpha=0.01)
+    s = r.logits
+    p = scipy.special.softmax(s, axis=1).astype(np.float32).astype(np.float64)
+    out = np.zeros((T, d))
+    for e in range(N):
+        out += p[:, e:e + 1] * bf16_to_f64(to_bf16_bits_f64(torch_expert(x, W1[e], b1[e], W2[e], b2[e])))
+    assert_bf16_close(r.y, to_bf16_bits_f64(out), max_mismatch_frac=3e-3, what="soft router")
+
+
+def pin_drops_and_shared(orc):
+    """Capacity drops leave only the kept assignments; with the routed experts
+    silenced (W2 = 0, b2 = 0) the output is exactly the shared expert's."""
+    rng = np.random.default_rng(11)
+    T, d, f, N, K = 32, 32, 48, 4, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    Ws1, bs1 = W1[0].copy(), b1[0].copy()
+    Ws2, bs2 = W2[1].copy(), b2[1].copy()
+    zero2, zb2 = np.zeros_like(W2), np.zeros_like(b2)
+    r = orc.forward(x, Wg, W1, b1, zero2, zb2, K=K, capacity_factor=1.0, aux_alpha=0.01,
+                    Ws1=Ws1, bs1=bs1, Ws2=Ws2, bs2=bs2)
+    z_ref = to_bf16_bits_f64(torch_expert(x, Ws1, bs1, Ws2, bs2))
+    assert_bf16_close(r.z, z_ref, what="shared expert")
+    assert np.array_equal(r.y, r.z)
+    # routed only, with drops: the dropped assignment contributes nothing
+    r2 = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=1.0, aux_alpha=0.01)
+    assert r2.capacity == 8 and (r2.slot_of < 0).any()
+    out = np.zeros((T, d))
+    for e in range(N):
+        o = bf16_to_f64(to_bf16_bits_f64(torch_expert(x, W1[e], b1[e], W2[e], b2[e])))
+        for k in range(K):
+            sel = (r2.topk_idx[:, k] == e) & (r2.slot_of[:, k] >= 0)
+            out[sel] += r2.topk_w[sel, k].astype(np.float64)[:, None] * o[sel]
+    assert_bf16_close(r2.y, to_bf16_bits_f64(out), max_mismatch_frac=3e-3, what="dropped")
+
+
+# ------------------------------------------------------------------ aux loss
+
+def pin_aux(orc):
+    """alpha * N * sum f P: equals alpha for uniform logits (any f) and for
+    uniform f (any P); lies in [0, alpha N]; f and P are distributions."""
+    rng = np.random.default_rng(12)
+    alpha = 0.01
+    for N, K in [(8, 2), (6, 1), (16, 4)]:
+        T = 64
+        idx, w, demand, P = orc.route(np.zeros((T, N)), K)
+        assert abs(orc.aux_loss(demand, P, T, K, alpha) - alpha) < 1e-15
+        # uniform f: token t prefers experts t, t+1, ..., t+K-1 (mod N), T = N
+        s = np.zeros((N, N))
+        for t in range(N):
+            for j in range(K):
+                s[t, (t + j) % N] = 10.0 - j
+        s += rng.standard_normal((N, N)) * 0.01
+        idx, w, demand, P = orc.route(s, K)
+        assert np.all(demand == K)
+        assert abs(orc.aux_loss(demand, P, N, K, alpha) - alpha) < 1e-14
+        s = rng.standard_normal((T, N)) * 4
+        idx, w, demand, P = orc.route(s, K)
+        a = orc.aux_loss(demand, P, T, K, alpha)
+        assert 0.0 <= a <= alpha * N
+        assert demand.sum() == T * K and abs(P.sum() - 1) < 1e-12
+    # all mass on one expert: f = P = 1 for it -> alpha * N
+    idx, w, demand, P = orc.route(np.tile([[50.0, 0, 0, 0]], (10, 1)), 1)
+    assert abs(orc.aux_loss(demand, P, 10, 1, alpha) - alpha * 4) < 1e-12
+
+
+ALL_PINS = [
+    pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
+    pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
+    pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts,
+    pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux,
+]

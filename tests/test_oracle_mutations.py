@@ -1,0 +1,60 @@
+"""Plant one plausible mistake at a time in a copy of the oracle's C source
+and check that the pins catch it. Nothing here touches a GPU."""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+# (name, [(exact text in moe_oracle.c, replacement)])
+MUTATIONS = [
+    ("tie_break_flipped", [("return (a->e > b->e) - (a->e < b->e);",
+                            "return (a->e < b->e) - (a->e > b->e);")]),
+    ("weights_from_biased_logits", [("if (st[buf[k].e] > m)\n                m = st[buf[k].e];",
+                                     "if (buf[k].u > m)\n                m = buf[k].u;"),
+                                    ("z += exp(st[buf[k].e] - m);", "z += exp(buf[k].u - m);"),
+                                    ("w[(size_t)t * K + k] = (float)(exp(st[buf[k].e] - m) / z);",
+                                     "w[(size_t)t * K + k] = (float)(exp(buf[k].u - m) / z);")]),
+    ("capacity_floor", [("double c = ceil(", "double c = floor(")]),
+    ("capacity_off_by_one", [("if (p < C) {", "if (p <= C) {")]),
+    ("gate_transposed", [("bf16_val(Wg[(size_t)e * d + j])", "bf16_val(Wg[(size_t)j * N + e])")]),
+    ("bias1_dropped", [("acc += (double)b1e[j];", "acc += 0.0;")]),
+    ("bias2_dropped", [("acc += (double)b2e[c];", "acc += 0.0;")]),
+    ("gelu_sign", [("0.5 * v * (1.0 + erf(v / sqrt(2.0)))", "0.5 * v * (1.0 - erf(v / sqrt(2.0)))")]),
+    ("hidden_not_rounded", [("h[j] = bf16_val(bf16_round(gelu_erf(acc)));", "h[j] = gelu_erf(acc);")]),
+    ("w2_transposed", [("acc += h[j] * bf16_val(wr[j]);", "acc += h[j] * bf16_val(W2e[(size_t)j * d + c]);")]),
+    ("combine_weight_index", [("acc += (double)w[(size_t)t * K + k] *",
+                               "acc += (double)w[(size_t)t * K + (K - 1 - k)] *")]),
+    ("shared_not_added", [("double acc = z ? bf16_val(z[(size_t)t * d + c]) : 0.0;", "double acc = 0.0;")]),
+    ("aux_f_over_T", [("((double)T * (double)K)", "((double)T)")]),
+    ("round_ties_away", [("nearbyint(ldexp(a, 7 - E))", "round(ldexp(a, 7 - E))")]),
+    ("prob_not_normalised", [("P[e] += ex[e] / zn;", "P[e] += ex[e];")]),
+    ("dispatch_rank_order_by_k", [("for (int t = 0; t < T; ++t) {\n        for (int k = 0; k < K; ++k) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;",
+                                   "for (int k = 0; k < K; ++k) {\n        for (int t = 0; t < T; ++t) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;")]),
+]
+
+
+def _mutant(tmp_path, name, edits):
+    with open(oracle.SOURCE) as fh:
+        src = fh.read()
+    for old, new in edits:
+        assert src.count(old) == 1, f"{name}: mutation anchor not unique/absent: {old!r}"
+        src = src.replace(old, new)
+    path = os.path.join(tmp_path, f"{name}.c")
+    with open(path, "w") as fh:
+        fh.write(src)
+    return oracle.Oracle(oracle.compile_source(path, os.path.join(tmp_path, f"lib{name}.so")))
+
+
+@pytest.mark.parametrize("name,edits", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(tmp_path, name, edits):
+    orc = _mutant(str(tmp_path), name, edits)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"

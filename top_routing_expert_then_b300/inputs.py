@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for the MoE layer forward pass.
+
+This module is shared by the CUDA path's callers and by the CPU oracle's
+tests. It holds none of the layer's arithmetic: it only names the workload
+shapes and draws random tensors for them. Everything here is plain torch RNG
+on a caller-chosen device with a seeded generator, so a (config, seed, device)
+triple always produces the same bytes.
+
+Value recipe (the workloads of the MoE pages: Mixtral-shaped and
+DeepSeek-V3-shaped layers, a tiny layer and a skewed fine-grained layer):
+
+* ``x``  = randint(-128, 128 inclusive) / 64, stored bf16 (exact): multiples
+  of 1/64 uniform in [-2, 2].
+* ``Wg`` = randint(-8, 8 inclusive) / 64, stored bf16 (exact): multiples of
+  1/64 in [-0.125, 0.125]. Layout ``[N, d_model]`` (nn.Linear ``[out, in]``).
+  With these grids every gate logit is a multiple of 2^-12 of magnitude
+  below 2^11, so any fp32 or fp64 summation order gives the same logit.
+* Expert weights ``W1 [N, d_ff, d_model]``, ``W2 [N, d_model, d_ff]`` drawn
+  N(0, 1/fan_in) and rounded to bf16 (torch's RNE cast); biases N(0, 0.02^2)
+  in fp32.
+* Skewed routing: expert e's gate row gets an additive Zipf(s=1.2) offset
+  ``round(4 * (e+1)^-1.2) / 64`` on every entry, which stays on the 1/64 grid
+  and makes the first few experts hot.
+* Aux-loss-free selection bias ``b_i`` ~ U(-0.05, 0.05) rounded to a multiple
+  of 2^-12 (so ``s + b`` stays exact in fp32), fp32.
+* Shared expert weights drawn like the routed ones.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Dict, Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class MoEConfig:
+    name: str
+    T: int
+    d_model: int
+    d_ff: int
+    N: int
+    K: int
+    capacity_factor: float  # <= 0 means dropless (capacity = T)
+    has_shared: bool = False
+    sel_bias: bool = False
+    zipf: bool = False
+    aux_alpha: float = 0.01
+    note: str = ""
+
+    def with_(self, **kw) -> "MoEConfig":
+        return replace(self, **kw)
+
+
+# The named workloads. capacity_factor <= 0 encodes "dropless" (capacity = T).
+CONFIGS: Dict[str, MoEConfig] = {
+    "tiny": MoEConfig("tiny", 256, 128, 256, 8, 2, 1.25,
+                      note="tiny layer, top-2 of 8, capacity factor 1.25"),
+    "mixtral_prefill": MoEConfig("mixtral_prefill", 4096, 4096, 14336, 8, 2, 0.0,
+                                 note="Mixtral-shaped prefill, dropless"),
+    "mixtral_prefill_cf125": MoEConfig("mixtral_prefill_cf125", 4096, 4096, 14336, 8, 2, 1.25,
+                                       note="Mixtral-shaped prefill, capacity factor 1.25"),
+    "mixtral_decode16": MoEConfig("mixtral_decode16", 16, 4096, 14336, 8, 2, 0.0,
+                                  note="Mixtral-shaped decode, 16 tokens, dropless"),
+    "mixtral_decode64": MoEConfig("mixtral_decode64", 64, 4096, 14336, 8, 2, 0.0,
+                                  note="Mixtral-shaped decode, 64 tokens, dropless"),
+    "skewed": MoEConfig("skewed", 8192, 2048, 1408, 64, 2, 1.0, zipf=True,
+                        note="fine-grained 64 experts, Zipf-skewed gate, capacity factor 1.0"),
+    "dsv3": MoEConfig("dsv3", 4096, 7168, 2048, 256, 8, 0.0, has_shared=True, sel_bias=True,
+                      note="DeepSeek-V3-shaped: 256 routed + 1 shared expert, top-8, selection bias"),
+}
+
+
+@dataclass
+class MoEInputs:
+    cfg: MoEConfig
+    x: torch.Tensor            # [T, d] bf16
+    Wg: torch.Tensor           # [N, d] bf16
+    W1: torch.Tensor           # [N, f, d] bf16
+    b1: torch.Tensor           # [N, f] fp32
+    W2: torch.Tensor           # [N, d, f] bf16
+    b2: torch.Tensor           # [N, d] fp32
+    sel_bias: Optional[torch.Tensor] = None  # [N] fp32
+    Ws1: Optional[torch.Tensor] = None       # [f, d] bf16
+    bs1: Optional[torch.Tensor] = None       # [f] fp32
+    Ws2: Optional[torch.Tensor] = None       # [d, f] bf16
+    bs2: Optional[torch.Tensor] = None       # [d] fp32
+    extra: Dict[str, torch.Tensor] = field(default_factory=dict)
+
+    def to(self, device) -> "MoEInputs":
+        def mv(t):
+            return None if t is None else t.to(device)
+        return MoEInputs(self.cfg, mv(self.x), mv(self.Wg), mv(self.W1), mv(self.b1),
+                         mv(self.W2), mv(self.b2), mv(self.sel_bias), mv(self.Ws1),
+                         mv(self.bs1), mv(self.Ws2), mv(self.bs2),
+                         {k: mv(v) for k, v in self.extra.items()})
+
+
+ZIPF_AMPLITUDE_64THS = 4
+ZIPF_S = 1.2
+
+
+def zipf_offsets_64ths(N: int) -> torch.Tensor:
+    """Per-expert integer offsets (in units of 1/64) for the skewed gate."""
+    e = torch.arange(1, N + 1, dtype=torch.float64)
+    return torch.round(ZIPF_AMPLITUDE_64THS * e.pow(-ZIPF_S)).to(torch.int64)
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _randn_bf16(shape, std: float, g, device, chunk_rows: int = 1024) -> torch.Tensor:
+    """N(0, std^2) rounded to bf16, drawn chunk by chunk to bound fp32 scratch."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(-1, shape[-1])
+    for r0 in range(0, flat.shape[0], chunk_rows):
+        r1 = min(flat.shape[0], r0 + chunk_rows)
+        tmp = torch.randn((r1 - r0, shape[-1]), generator=g, device=device, dtype=torch.float32)
+        flat[r0:r1] = (tmp * std).to(torch.bfloat16)
+    return out
+
+
+def make_inputs(cfg: MoEConfig | str, seed: int = 0, device="cpu") -> MoEInputs:
+    """Draw every input of one MoE layer forward for ``cfg`` on ``device``."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    device = torch.device(device)
+    g = _gen(device, seed)
+    T, d, f, N = cfg.T, cfg.d_model, cfg.d_ff, cfg.N
+
+    x = (torch.randint(-128, 129, (T, d), generator=g, device=device, dtype=torch.int32)
+         .to(torch.float32) / 64).to(torch.bfloat16)
+    wg_int = torch.randint(-8, 9, (N, d), generator=g, device=device, dtype=torch.int32)
+    if cfg.zipf:
+        wg_int = wg_int + zipf_offsets_64ths(N).to(device=device, dtype=torch.int32)[:, None]
+    Wg = (wg_int.to(torch.float32) / 64).to(torch.bfloat16)
+
+    W1 = _randn_bf16((N, f, d), d ** -0.5, g, device)
+    b1 = torch.randn((N, f), generator=g, device=device, dtype=torch.float32) * 0.02
+    W2 = _randn_bf16((N, d, f), f ** -0.5, g, device)
+    b2 = torch.randn((N, d), generator=g, device=device, dtype=torch.float32) * 0.02
+
+    sel_bias = None
+    if cfg.sel_bias:
+        u = torch.rand((N,), generator=g, device=device, dtype=torch.float64) * 0.1 - 0.05
+        sel_bias = (torch.round(u * 4096) / 4096).to(torch.float32)
+
+    Ws1 = bs1 = Ws2 = bs2 = None
+    if cfg.has_shared:
+        Ws1 = _randn_bf16((f, d), d ** -0.5, g, device)
+        bs1 = torch.randn((f,), generator=g, device=device, dtype=torch.float32) * 0.02
+        Ws2 = _randn_bf16((d, f), f ** -0.5, g, device)
+        bs2 = torch.randn((d,), generator=g, device=device, dtype=torch.float32) * 0.02
+
+    return MoEInputs(cfg, x, Wg, W1, b1, W2, b2, sel_bias, Ws1, bs1, Ws2, bs2)
+
+
+def make_x(cfg: MoEConfig, seed: int, device="cpu") -> torch.Tensor:
+    """A fresh batch of tokens on the 1/64 grid (used for multi-batch runs)."""
+    g = _gen(torch.device(device), seed)
+    return (torch.randint(-128, 129, (cfg.T, cfg.d_model), generator=g, device=device,
+                          dtype=torch.int32).to(torch.float32) / 64).to(torch.bfloat16)
