@@ -1,0 +1,150 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and compare it with the CPU oracle on the same seeded inputs."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import bf16_to_f64
+from top_routing_expert_then_b300 import lib
+from top_routing_expert_then_b300.inputs import MoEConfig, make_inputs
+
+# Tolerances for bf16 outputs with fp32 accumulation (vs the fp64 oracle):
+# relative L2 over the tensor and a per-element bound.
+REL_L2 = 5e-3
+ELEM_ABS = 3e-2
+AUX_RTOL = 1e-5
+W_ATOL = 2e-6       # routing weights (fp32 softmax vs fp64 softmax rounded to fp32)
+PROB_RTOL = 2e-5    # per-expert sums of full-softmax probabilities
+
+
+def bits_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_bf16_tol(got_bits, ref_bits, what=""):
+    g = bf16_to_f64(got_bits)
+    r = bf16_to_f64(ref_bits)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    if g.size == 0:
+        return
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - r)
+    bound = ELEM_ABS * (1.0 + np.abs(r))
+    worst = np.argmax(err - bound)
+    assert np.all(err <= bound), (f"{what}: element {np.unravel_index(worst, g.shape)} got {g.flat[worst]} "
+                                  f"ref {r.flat[worst]}")
+    rel = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e}"
+
+
+def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
+    """n token ids spread over [0, T): both ends plus seeded random picks."""
+    rng = np.random.default_rng(seed)
+    pick = {0, T - 1} | set(rng.choice(T, size=min(n, T), replace=False).tolist())
+    return np.array(sorted(pick)[:max(n, 2)], dtype=np.int64)
+
+
+def gpu_inputs(cfg: MoEConfig, seed: int = 0):
+    inp = make_inputs(cfg, seed, device="cuda")
+    torch.cuda.synchronize()
+    return inp
+
+
+def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages: bool = True):
+    """Full comparison of one configuration.
+
+    Routing, dispatch, kept counts, drops, prob sums and the aux loss are
+    compared on every token. FFN outputs are compared on every row, or on the
+    rows of `sample` tokens when the oracle cannot do the whole batch in
+    seconds. With `stages`, each ABI stage is also run on oracle-produced
+    inputs, isolating it from the stages before it.
+    """
+    inp = gpu_inputs(cfg, seed)
+    cpu = inp.to("cpu")
+    T, K, N, d = cfg.T, cfg.K, cfg.N, cfg.d_model
+    want = None
+    if sample is not None and sample < T:
+        want = np.zeros(T, dtype=np.uint8)
+        want[sample_tokens(T, sample, seed)] = 1
+    ref = oracle.forward_inputs(cpu, want=want)
+    shape = lib.shape_of(cfg)
+    assert lib.capacity(shape) == ref.capacity
+
+    # ---- the whole layer through moe_forward
+    layer = lib.MoELayer.from_inputs(inp)
+    ro = layer.route_outputs()
+    y = layer.forward(inp.x, inp.sel_bias, route_out=ro)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+
+    assert np.array_equal(ro.topk_idx.cpu().numpy(), ref.topk_idx), "topk_idx"
+    assert np.allclose(ro.topk_w.cpu().numpy(), ref.topk_w, rtol=0, atol=W_ATOL), "topk_w"
+    assert np.array_equal(ro.demand.cpu().numpy(), ref.demand), "demand"
+    assert np.allclose(ro.prob_sum.cpu().numpy().astype(np.float64), ref.P * T, rtol=PROB_RTOL, atol=1e-6), "prob_sum"
+    assert np.array_equal(ro.kept.cpu().numpy(), ref.kept), "kept"
+    assert np.array_equal(ro.expert_offsets.cpu().numpy(), ref.offsets), "expert_offsets"
+    assert np.array_equal(ro.slot_of.cpu().numpy(), ref.slot_of), "slot_of"
+    aux = float(ro.aux.cpu()[0])
+    assert abs(aux - ref.aux) <= AUX_RTOL * abs(ref.aux), ("aux", aux, ref.aux)
+
+    yb = bits_np(y)
+    rows = slice(None) if want is None else want.astype(bool)
+    assert_bf16_tol(yb[rows], ref.y[rows], "forward y")
+
+    if not stages:
+        return ref
+    # ---- stage by stage, each fed with oracle-produced inputs
+    idx, w, demand, psum = lib.route(shape, inp.x, inp.Wg, inp.sel_bias)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), ref.topk_idx)
+    assert np.allclose(w.cpu().numpy(), ref.topk_w, rtol=0, atol=W_ATOL)
+    assert np.array_equal(demand.cpu().numpy(), ref.demand)
+
+    ref_idx = torch.from_numpy(ref.topk_idx).cuda()
+    kept, offsets, slot_of, row_token, x_perm = lib.dispatch(shape, ref_idx, inp.x)
+    torch.cuda.synchronize()
+    assert np.array_equal(kept.cpu().numpy(), ref.kept)
+    assert np.array_equal(offsets.cpu().numpy(), ref.offsets)
+    assert np.array_equal(slot_of.cpu().numpy(), ref.slot_of)
+    assert np.array_equal(row_token.cpu().numpy(), ref.row_token)
+    R = int(ref.offsets[N])
+    xb = bits_np(inp.x)
+    assert np.array_equal(bits_np(x_perm)[:R], xb[ref.row_token[:R]]), "x_perm = x[row_token]"
+
+    # FFN on the oracle's regrouped rows
+    xp = torch.zeros((T * K, d), dtype=torch.bfloat16, device="cuda")
+    if R:
+        xp[:R] = inp.x[torch.from_numpy(ref.row_token[:R].astype(np.int64)).cuda()]
+    y_perm, z = lib.expert_ffn(shape, xp, torch.from_numpy(ref.offsets).cuda(), inp.W1, inp.b1, inp.W2, inp.b2,
+                               inp.x, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2)
+    torch.cuda.synchronize()
+    ypb = bits_np(y_perm)[:R]
+    if want is None:
+        assert_bf16_tol(ypb, ref.y_perm, "y_perm")
+    else:
+        live = want[ref.row_token[:R]].astype(bool)
+        assert_bf16_tol(ypb[live], ref.y_perm[live], "y_perm (sampled)")
+    if cfg.has_shared:
+        assert_bf16_tol(bits_np(z)[rows], ref.z[rows], "z_shared")
+
+    # combine on the oracle's expert outputs and weights
+    if want is None:
+        yp_ref = torch.zeros((T * K, d), dtype=torch.bfloat16, device="cuda")
+        if R:
+            yp_ref[:R] = torch.from_numpy(ref.y_perm.view(np.int16)).cuda().view(torch.bfloat16)
+        z_ref = None
+        if cfg.has_shared:
+            z_ref = torch.from_numpy(ref.z.view(np.int16)).cuda().view(torch.bfloat16)
+        yc = lib.combine(shape, yp_ref, torch.from_numpy(ref.slot_of).cuda(), torch.from_numpy(ref.topk_w).cuda(),
+                         z_ref)
+        torch.cuda.synchronize()
+        assert_bf16_tol(bits_np(yc), ref.y, "combine")
+
+    a = lib.aux_loss(shape, torch.from_numpy(ref.demand).cuda(),
+                     torch.from_numpy((ref.P * T).astype(np.float32)).cuda())
+    assert abs(float(a.cpu()[0]) - ref.aux) <= AUX_RTOL * abs(ref.aux)
+    assert lib.device_error() == 0
+    return ref

@@ -1,0 +1,211 @@
+// dispatch.cuh -- capacity-limited, token-ordered dispatch and the combine
+// (lmnt.cn/news/351908 sec. 3.1: regroup token order into one contiguous block
+// per expert; sec. 3.2: combine through the same index table, same order;
+// sec. 3.3: capacity = ceil(T/N * capacity_factor), overflow dropped).
+//
+// Position of assignment (t, k) with expert e inside e's block:
+//   p = #{t' < t : e in topk_idx[t']}     (each token names an expert at most once)
+// computed as   base[chunk][e]              exclusive scan over 128-token chunks
+//             + popc(bits[w'][e]) for the chunk's earlier warps
+//             + popc(bits[w][e] & lanes below this one)
+// where bits[w][e] has bit l set iff token (chunk, w, l) chose e. Integer work
+// only: bit-exact and independent of scheduling.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace dispatch {
+
+constexpr int kChunk = 128;  // tokens per block (4 warps x 32 lanes)
+
+inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+
+// hist[chunk][e] = assignments to e among the chunk's tokens.
+__global__ void __launch_bounds__(kChunk)
+count_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int32_t *__restrict__ hist) {
+    extern __shared__ int cnt[];  // [N]
+    for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[(size_t)t * K + k];
+            if (e >= 0 && e < N)
+                atomicAdd(&cnt[e], 1);
+            else
+                flag_error(MOE_DEVERR_EXPERT_ID);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) hist[(size_t)blockIdx.x * N + e] = cnt[e];
+}
+
+// One block. base[c][e] = sum_{c' < c} hist[c'][e]; kept[e] = min(total, C);
+// offsets = exclusive prefix of kept (offsets[N] = kept rows R).
+__global__ void __launch_bounds__(1024)
+scan_kernel(const int32_t *__restrict__ hist, int chunks, int N, int C, int32_t *__restrict__ base,
+            int32_t *__restrict__ kept, int32_t *__restrict__ offsets) {
+    extern __shared__ int sh[];  // [N] kept, then scan buffer [N]
+    int *kv = sh;
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = 0;
+#pragma unroll 8
+        for (int c = 0; c < chunks; ++c) {
+            int h = hist[(size_t)c * N + e];
+            base[(size_t)c * N + e] = run;
+            run += h;
+        }
+        int kp = run < C ? run : C;
+        kept[e] = kp;
+        kv[e] = kp;
+    }
+    __syncthreads();
+    // inclusive Hillis-Steele scan over N <= 1024 entries, one per thread
+    const int e = threadIdx.x;
+    int v = (e < N) ? kv[e] : 0;
+    for (int o = 1; o < N; o <<= 1) {
+        int add = (e >= o && e < N) ? kv[e - o] : 0;
+        __syncthreads();
+        if (e < N) kv[e] = v = v + add;
+        __syncthreads();
+    }
+    if (e < N) offsets[e + 1] = v;
+    if (e == 0) offsets[0] = 0;
+}
+
+// slot_of[t, k] = offsets[e] + p if p < C else -1; row_token[slot] = t.
+__global__ void __launch_bounds__(kChunk)
+assign_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int C,
+              const int32_t *__restrict__ base, const int32_t *__restrict__ offsets,
+              int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token) {
+    extern __shared__ unsigned bits[];  // [4][N]
+    for (int i = threadIdx.x; i < 4 * N; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    const int w = warp_id(), lane = lane_id();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            int e = topk_idx[(size_t)t * K + k];
+            if (e >= 0 && e < N) atomicOr(&bits[w * N + e], 1u << lane);
+        }
+    }
+    __syncthreads();
+    if (t >= T) return;
+    const unsigned below = (1u << lane) - 1u;
+    for (int k = 0; k < K; ++k) {
+        int e = topk_idx[(size_t)t * K + k];
+        int slot = -1;
+        if (e >= 0 && e < N) {
+            int p = base[(size_t)blockIdx.x * N + e];
+            for (int w2 = 0; w2 < w; ++w2) p += __popc(bits[w2 * N + e]);
+            p += __popc(bits[w * N + e] & below);
+            if (p < C) {
+                slot = offsets[e] + p;
+                row_token[slot] = t;
+            }
+        }
+        slot_of[(size_t)t * K + k] = slot;
+    }
+}
+
+// x_perm[slot_of[t, k]] = x[t]: one block per token reads its row once and
+// writes it to each of its kept slots (16-byte vectors).
+__global__ void __launch_bounds__(256)
+permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_of, int T, int K,
+               int d, int rows, uint16_t *__restrict__ x_perm) {
+    const int t = blockIdx.x;
+    __shared__ int slots[8];
+    if (threadIdx.x < K) {
+        int s = slot_of[(size_t)t * K + threadIdx.x];
+        if (s >= rows) {
+            flag_error(MOE_DEVERR_ROW_INDEX);
+            s = -1;
+        }
+        slots[threadIdx.x] = s;
+    }
+    __syncthreads();
+    const int vec = d >> 3;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+    for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+        uint4 v = __ldg(src + c);
+        for (int k = 0; k < K; ++k) {
+            int s = slots[k];
+            if (s >= 0) reinterpret_cast<uint4 *>(x_perm + (size_t)s * d)[c] = v;
+        }
+    }
+}
+
+// y[t] = bf16(z[t] + sum_k w[t,k] * y_perm[slot_of[t,k]]), fp32, increasing k.
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ slot_of,
+               const float *__restrict__ topk_w, const uint16_t *__restrict__ z, int T, int K,
+               int d, int rows, uint16_t *__restrict__ y) {
+    const int t = blockIdx.x;
+    __shared__ int slots[8];
+    __shared__ float wts[8];
+    if (threadIdx.x < K) {
+        int s = slot_of[(size_t)t * K + threadIdx.x];
+        if (s >= rows) {
+            flag_error(MOE_DEVERR_ROW_INDEX);
+            s = -1;
+        }
+        slots[threadIdx.x] = s;
+        wts[threadIdx.x] = topk_w[(size_t)t * K + threadIdx.x];
+    }
+    __syncthreads();
+    const int vec = d >> 3;
+    for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+        float acc[8];
+        if (z != nullptr) {
+            uint4 v = __ldg(reinterpret_cast<const uint4 *>(z + (size_t)t * d) + c);
+            unpack_bf16x2(v.x, acc[0], acc[1]);
+            unpack_bf16x2(v.y, acc[2], acc[3]);
+            unpack_bf16x2(v.z, acc[4], acc[5]);
+            unpack_bf16x2(v.w, acc[6], acc[7]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        }
+        for (int k = 0; k < K; ++k) {
+            int s = slots[k];
+            if (s < 0) continue;
+            float wk = wts[k];
+            uint4 v = __ldg(reinterpret_cast<const uint4 *>(y_perm + (size_t)s * d) + c);
+            float f[8];
+            unpack_bf16x2(v.x, f[0], f[1]);
+            unpack_bf16x2(v.y, f[2], f[3]);
+            unpack_bf16x2(v.z, f[4], f[5]);
+            unpack_bf16x2(v.w, f[6], f[7]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(wk, f[j], acc[j]);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(y + (size_t)t * d)[c] = o;
+    }
+}
+
+// aux = alpha * N * sum_e (demand[e] / (T K)) * (prob_sum[e] / T), in double,
+// fixed reduction order (lmnt.cn/news/351908 sec. 5.1-5.2).
+__global__ void aux_loss_kernel(const int32_t *__restrict__ demand, const float *__restrict__ prob_sum,
+                                int T, int N, int K, float alpha, float *__restrict__ aux) {
+    __shared__ double part[32];
+    double a = 0.0;
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+        a += ((double)demand[e] / ((double)T * (double)K)) * ((double)prob_sum[e] / (double)T);
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane_id() == 0) part[warp_id()] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += part[w];
+        aux[0] = (float)((double)alpha * (double)N * s);
+    }
+}
+
+}  // namespace dispatch
+}  // namespace moe

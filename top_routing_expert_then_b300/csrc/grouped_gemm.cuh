@@ -1,0 +1,487 @@
+// grouped_gemm.cuh -- the expert FFN as grouped GEMMs on the 5th-generation
+// tensor cores (tcgen05 + TMEM, operands staged by TMA).
+//
+//   out[r, n] = epilogue( sum_k A[r, k] * B[g(r) * n_out + n, k] + bias[g(r), n] )
+//
+// A is the regrouped token buffer (one contiguous block of rows per expert,
+// the dispatch's output), B the stacked expert weights in nn.Linear layout
+// ([out, in], reduction dimension contiguous), g(r) the expert owning row r.
+// The epilogue is GELU (first Linear) or identity (second Linear), then RNE to
+// bf16. (Expert FFN = Linear -> GELU -> Linear: yunthe.com MoELayer listing;
+// the page's remark that production code groups tokens per expert and runs
+// grouped GEMMs is the prior art this replaces.)
+//
+// Work unit: a 128 x 256 output tile of one expert. The ragged per-expert row
+// counts live only on the device: a tile list (row0, rows, expert) is built on
+// the device from the expert offsets, and every block of a persistent grid
+// walks the same list, so no host synchronisation is needed.
+//
+// Block = 6 warps, one block per SM:
+//   warp 0     TMA producer (one lane): A tile 128x64 and B tile 256x64 per
+//              stage, 128-byte swizzle, 4-stage ring in shared memory
+//   warp 1     TMEM allocator + MMA issuer (one lane): tcgen05.mma
+//              kind::f16, M=128 N=256 K=16, fp32 accumulators in TMEM, two
+//              accumulator buffers (2 x 256 columns) so the epilogue of one
+//              tile overlaps the main loop of the next
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, bias,
+//              GELU, bf16, 16-byte stores; rows past the expert's block and
+//              columns past n_out are computed but not stored
+//
+// Every wait is bounded (globaltimer). On a timeout the block sets
+// MOE_DEVERR_TIMEOUT, stops issuing work, drains its own copies and MMAs in
+// flight, frees its TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int ACC_COLS = BN;          // fp32 accumulator columns per buffer
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;   // 4 s
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 = 1),
+// B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+struct Params {
+    const int4 *mtiles;       // [max_mtiles] {row0, rows, group, 0}; nullptr = dense mode
+    const int *num_mtiles;    // device count of valid mtiles
+    int max_mtiles;           // capacity of the list (bounds check)
+    int dense_rows;           // dense mode: rows of A (one group)
+    int n_out;                // output columns (multiple of 64)
+    int k_dim;                // reduction length (multiple of 64)
+    int num_groups;           // experts in B / bias
+    int out_rows;             // rows of `out` (bounds check)
+    const float *bias;        // [num_groups, n_out]
+    uint16_t *out;            // [out_rows, n_out] bf16
+    int gelu;                 // 1: GELU epilogue
+    int raster;               // m-tiles per raster group
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (SBO), version 1 (bits 46-47), layout 2 = SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;              // LBO (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // SBO
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(IDESC), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- helpers
+
+struct Shared {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(Shared) <= BAR_BYTES, "barrier block too large");
+
+// Bounded wait: true when the phase with `parity` has completed; false on
+// abort (another role gave up) or after `limit_ns` (then sets the abort flag
+// and the device error bit).
+__device__ __noinline__ bool wait_bounded(Shared *sh, uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns, bool raise) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (raise && sh->abort_flag) return false;
+            uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                if (raise) {
+                    sh->abort_flag = 1;
+                    flag_error(MOE_DEVERR_TIMEOUT);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+struct Tile {
+    int row0, rows, group, n0;
+    bool ok;
+};
+
+__device__ __forceinline__ int num_m_tiles(const Params &p) {
+    if (p.mtiles == nullptr) return (p.dense_rows + BM - 1) / BM;
+    int n = *p.num_mtiles;
+    return n < 0 ? 0 : (n > p.max_mtiles ? p.max_mtiles : n);
+}
+
+// Work item w -> (m-tile, n-tile): raster groups of `raster` m-tiles; inside a
+// group the m index runs fastest, so the blocks in flight share B tiles.
+__device__ __forceinline__ Tile tile_of(const Params &p, int w, int num_m, int num_n) {
+    const int G = p.raster;
+    const int g = w / (G * num_n);
+    const int local = w - g * G * num_n;
+    const int gm_left = num_m - g * G;
+    const int gm = gm_left < G ? gm_left : G;
+    const int m = g * G + local % gm;
+    const int n = local / gm;
+    Tile t;
+    if (p.mtiles == nullptr) {
+        t.row0 = m * BM;
+        t.rows = min(BM, p.dense_rows - t.row0);
+        t.group = 0;
+    } else {
+        int4 v = p.mtiles[m];
+        t.row0 = v.x;
+        t.rows = v.y;
+        t.group = v.z;
+    }
+    t.n0 = n * BN;
+    t.ok = t.rows > 0 && t.rows <= BM && t.row0 >= 0 && t.row0 + t.rows <= p.out_rows &&
+           t.group >= 0 && t.group < p.num_groups;
+    return t;
+}
+
+__device__ __forceinline__ float gelu_erf(float v) {
+    return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
+}
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    Shared *sh = reinterpret_cast<Shared *>(smem + STAGES * STAGE_BYTES);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&sh->full[s]), 1);
+            mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sh->tfull[a]), 1);
+            mbar_init(smem_u32(&sh->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sh->tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_base;
+
+    const int num_m = num_m_tiles(p);
+    const int num_n = (p.n_out + BN - 1) / BN;
+    const int total = num_m * num_n;
+    const int kblocks = p.k_dim / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t stage = 0, phase = 0;
+            int issued_phase[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
+            bool stop = false;
+            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+                Tile t = tile_of(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                const int brow = t.group * p.n_out + t.n0;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&sh->full[stage]);
+                    uint8_t *a_s = smem + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d(smem_u32(a_s), &tmA, fb, kb * BK, t.row0);
+                    tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (stop) {
+                // let this block's copies in flight land before the block exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_phase[s] >= 0)
+                        wait_bounded(sh, smem_u32(&sh->full[s]), (uint32_t)issued_phase[s],
+                                     DRAIN_LIMIT_NS, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+                Tile t = tile_of(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                if (!wait_bounded(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
+                                 (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&sh->empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+                mma_commit(smem_u32(&sh->tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // every MMA issued by this block has completed once `drain` fires
+            mma_commit(smem_u32(&sh->drain));
+            wait_bounded(sh, smem_u32(&sh->drain), 0, DRAIN_LIMIT_NS, false);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2-5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            Tile t = tile_of(p, w, num_m, num_n);
+            if (!t.ok) {
+                if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
+                continue;
+            }
+            if (!wait_bounded(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
+            tc_fence_after();
+            const bool store = row < t.rows;
+            uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
+            const float *bias = p.bias + (size_t)t.group * p.n_out;
+            const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                const int col = t.n0 + c0;
+                if (col >= p.n_out) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld32(tbase + c0, r);
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(bias + col + j));
+                    float v0 = __uint_as_float(r[j + 0]) + b.x;
+                    float v1 = __uint_as_float(r[j + 1]) + b.y;
+                    float v2 = __uint_as_float(r[j + 2]) + b.z;
+                    float v3 = __uint_as_float(r[j + 3]) + b.w;
+                    if (p.gelu) {
+                        v0 = gelu_erf(v0);
+                        v1 = gelu_erf(v1);
+                        v2 = gelu_erf(v2);
+                        v3 = gelu_erf(v3);
+                    }
+                    packed[j / 2] = pack_bf16x2(v0, v1);
+                    packed[j / 2 + 1] = pack_bf16x2(v2, v3);
+                }
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                            packed[4 * j + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// The m-tile list of the routed experts, from the expert offsets:
+// expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / BM) tiles.
+// One block of 1024 threads; N <= 1024.
+__global__ void __launch_bounds__(1024)
+build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int max_tiles,
+                    int4 *__restrict__ mtiles, int *__restrict__ num_mtiles) {
+    __shared__ int sc[1024];
+    const int e = threadIdx.x;
+    int cnt = 0, r0 = 0, r1 = 0;
+    bool bad = false;
+    if (e < N) {
+        r0 = offsets[e];
+        r1 = offsets[e + 1];
+        if (r0 < 0 || r1 < r0 || r1 > total_rows) {
+            bad = true;
+        } else {
+            cnt = (r1 - r0 + BM - 1) / BM;
+        }
+    }
+    if (bad) flag_error(MOE_DEVERR_TILE_LIST);
+    sc[e] = cnt;
+    __syncthreads();
+    int v = cnt;
+    for (int o = 1; o < 1024; o <<= 1) {
+        int add = (e >= o) ? sc[e - o] : 0;
+        __syncthreads();
+        sc[e] = v = v + add;
+        __syncthreads();
+    }
+    const int start = v - cnt;
+    for (int i = 0; i < cnt; ++i) {
+        int m = start + i;
+        if (m < max_tiles) {
+            int rr = r0 + i * BM;
+            int rows = r1 - rr < BM ? r1 - rr : BM;
+            mtiles[m] = make_int4(rr, rows, e, 0);
+        }
+    }
+    if (e == 1023) *num_mtiles = v < max_tiles ? v : max_tiles;
+}
+
+}  // namespace gg
+}  // namespace moe

@@ -1,0 +1,601 @@
+// libmoe.cu -- the C ABI of include/moe.h: host-side validation, workspace
+// layout and kernel launches for the MoE layer forward pass on sm_103a.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "grouped_gemm.cuh"
+#include "route.cuh"
+
+namespace {
+
+using moe::gg::BM;
+
+std::atomic<uint64_t> g_launches{0};
+
+inline void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// Sequential carve of a workspace (or, with base == nullptr, only its size).
+struct Carve {
+    char *base;
+    size_t off = 0;
+    explicit Carve(void *b) : base(static_cast<char *>(b)) {}
+    template <typename T>
+    T *take(size_t count) {
+        off = align_up(off);
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+    size_t bytes() const { return align_up(off); }
+};
+
+// ------------------------------------------------------------------ shape checks
+
+moe_status check_shape(const moe_shape *s) {
+    if (s == nullptr) return MOE_ERR_INVALID_ARG;
+    if (s->T <= 0 || s->d_model <= 0 || s->d_ff <= 0 || s->N <= 0 || s->K <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s->K > s->N) return MOE_ERR_INVALID_ARG;
+    if (std::isnan(s->capacity_factor) || std::isnan(s->aux_alpha)) return MOE_ERR_INVALID_ARG;
+    if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_INVALID_ARG;
+    if (s->d_model % 64 != 0 || s->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->K > moe::route::kMaxK || s->N > 1024) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s->T * s->K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s->N * s->d_ff >= (int64_t(1) << 31) || (int64_t)s->N * s->d_model >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int capacity_of(const moe_shape *s) {
+    // lmnt.cn/news/351908 sec. 3.3: capacity = ceil(T / N * capacity_factor)
+    if (s->capacity_factor <= 0.f) return s->T;
+    double c = std::ceil((double)s->T / (double)s->N * (double)s->capacity_factor);
+    if (c > (double)s->T) c = (double)s->T;
+    if (c < 0.0) c = 0.0;
+    return (int)c;
+}
+
+int max_mtiles(const moe_shape *s) {
+    return (int)(((int64_t)s->T * s->K + BM - 1) / BM) + s->N;
+}
+
+// ------------------------------------------------------------------ workspace layouts
+
+struct RouteWs {
+    float *logits;
+    float *partial;
+};
+RouteWs carve_route(Carve &c, const moe_shape *s) {
+    RouteWs w;
+    w.logits = c.take<float>((size_t)s->T * s->N);
+    w.partial = c.take<float>((size_t)moe::route::topk_grid(s->T) * s->N);
+    return w;
+}
+
+struct DispatchWs {
+    int32_t *hist;
+    int32_t *base;
+};
+DispatchWs carve_dispatch(Carve &c, const moe_shape *s) {
+    DispatchWs w;
+    size_t n = (size_t)moe::dispatch::num_chunks(s->T) * s->N;
+    w.hist = c.take<int32_t>(n);
+    w.base = c.take<int32_t>(n);
+    return w;
+}
+
+struct FfnWs {
+    int4 *mtiles;
+    int *num_mtiles;
+    uint16_t *H;
+    uint16_t *Hs;
+};
+FfnWs carve_ffn(Carve &c, const moe_shape *s) {
+    FfnWs w;
+    w.mtiles = c.take<int4>((size_t)max_mtiles(s));
+    w.num_mtiles = c.take<int>(4);
+    w.H = c.take<uint16_t>((size_t)s->T * s->K * s->d_ff);
+    w.Hs = s->has_shared ? c.take<uint16_t>((size_t)s->T * s->d_ff) : nullptr;
+    return w;
+}
+
+struct ForwardWs {
+    RouteWs route;
+    DispatchWs disp;
+    FfnWs ffn;
+    int32_t *topk_idx, *demand, *kept, *offsets, *slot_of, *row_token;
+    float *topk_w, *prob_sum, *aux;
+    uint16_t *x_perm, *y_perm, *z;
+};
+ForwardWs carve_forward(Carve &c, const moe_shape *s) {
+    ForwardWs w;
+    const size_t TK = (size_t)s->T * s->K;
+    w.route = carve_route(c, s);
+    w.disp = carve_dispatch(c, s);
+    w.ffn = carve_ffn(c, s);
+    w.topk_idx = c.take<int32_t>(TK);
+    w.topk_w = c.take<float>(TK);
+    w.demand = c.take<int32_t>(s->N);
+    w.prob_sum = c.take<float>(s->N);
+    w.kept = c.take<int32_t>(s->N);
+    w.offsets = c.take<int32_t>((size_t)s->N + 1);
+    w.slot_of = c.take<int32_t>(TK);
+    w.row_token = c.take<int32_t>(TK);
+    w.aux = c.take<float>(4);
+    w.x_perm = c.take<uint16_t>(TK * s->d_model);
+    w.y_perm = c.take<uint16_t>(TK * s->d_model);
+    w.z = s->has_shared ? c.take<uint16_t>((size_t)s->T * s->d_model) : nullptr;
+    return w;
+}
+
+size_t ws_bytes(const moe_shape *s, int kind) {
+    Carve c(nullptr);
+    switch (kind) {
+        case MOE_WS_ROUTE: carve_route(c, s); break;
+        case MOE_WS_DISPATCH: carve_dispatch(c, s); break;
+        case MOE_WS_FFN: carve_ffn(c, s); break;
+        case MOE_WS_FORWARD: carve_forward(c, s); break;
+        default: return 0;
+    }
+    return c.bytes();
+}
+
+moe_status check_ws(const moe_shape *s, int kind, void *ws, size_t bytes) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+        return MOE_ERR_WORKSPACE;
+    if (bytes < ws_bytes(s, kind)) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ per-device state
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    std::once_flag once;
+    int num_sms = 0;
+    cudaError_t init_err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+constexpr int kSmallGateMaxN = 16;
+constexpr size_t kSmallGateMaxSmem = 200 * 1024;
+
+moe_status device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    DeviceState &st = g_dev[dev];
+    std::call_once(st.once, [&st, dev]() {
+        cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::route::gate_logits_smallN_kernel<8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallGateMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::route::gate_logits_smallN_kernel<16>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallGateMaxSmem);
+        st.init_err = e;
+    });
+    if (st.init_err != cudaSuccess) return MOE_ERR_CUDA;
+    *out = &st;
+    return MOE_OK;
+}
+
+moe_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, []() {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        cudaGetLastError();
+    });
+    return g_encode != nullptr;
+}
+
+// Row-major bf16 [rows, cols] tensor, box = box_rows x 64 columns, 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)moe::gg::BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ stage launchers (no validation)
+
+moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
+                     const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
+                     float *prob_sum, const RouteWs &w, cudaStream_t st) {
+    const int T = s->T, d = s->d_model, N = s->N, K = s->K;
+    (void)dev;
+    const size_t wg_bytes = (size_t)N * d * 2;
+    if (N <= kSmallGateMaxN && wg_bytes <= kSmallGateMaxSmem) {
+        const int warps = moe::route::kGateThreads / 32;
+        int grid = (T + warps - 1) / warps;
+        if (grid > 1184) grid = 1184;
+        if (N <= 8)
+            moe::route::gate_logits_smallN_kernel<8>
+                <<<grid, moe::route::kGateThreads, wg_bytes, st>>>(x, Wg, T, d, N, w.logits);
+        else
+            moe::route::gate_logits_smallN_kernel<16>
+                <<<grid, moe::route::kGateThreads, wg_bytes, st>>>(x, Wg, T, d, N, w.logits);
+    } else {
+        dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
+        moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N, w.logits);
+    }
+    count_launch();
+    if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
+    const int grid = moe::route::topk_grid(T);
+    const size_t smem = (size_t)moe::route::kTopkWarps * N * sizeof(float) + (size_t)N * sizeof(int);
+    const int lpl = (N + 31) / 32;
+    const int thr = moe::route::kTopkWarps * 32;
+#define MOE_TOPK(L)                                                                                     \
+    moe::route::topk_softmax_kernel<L><<<grid, thr, smem, st>>>(w.logits, sel_bias, T, N, K, topk_idx, \
+                                                                topk_w, demand, w.partial)
+    if (lpl <= 1) MOE_TOPK(1);
+    else if (lpl <= 2) MOE_TOPK(2);
+    else if (lpl <= 4) MOE_TOPK(4);
+    else if (lpl <= 8) MOE_TOPK(8);
+    else if (lpl <= 16) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
+    count_launch();
+    moe::route::prob_finalize_kernel<<<(N + 127) / 128, 128, 0, st>>>(w.partial, grid, N, prob_sum);
+    count_launch();
+    return launch_status();
+}
+
+moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint16_t *x, int32_t *kept,
+                        int32_t *offsets, int32_t *slot_of, int32_t *row_token, uint16_t *x_perm,
+                        const DispatchWs &w, cudaStream_t st) {
+    const int T = s->T, N = s->N, K = s->K, d = s->d_model;
+    const int C = capacity_of(s);
+    const int chunks = moe::dispatch::num_chunks(T);
+    const int rows = T * K;
+    if (cudaMemsetAsync(row_token, 0xFF, sizeof(int32_t) * (size_t)rows, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, T, N, K,
+                                                                                         w.hist);
+    count_launch();
+    moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets);
+    count_launch();
+    moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
+        topk_idx, T, N, K, C, w.base, offsets, slot_of, row_token);
+    count_launch();
+    moe::dispatch::permute_kernel<<<T, 256, 0, st>>>(x, slot_of, T, K, d, rows, x_perm);
+    count_launch();
+    return launch_status();
+}
+
+moe_status launch_gemm(DeviceState *dev, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
+                       int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
+                       const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
+                       cudaStream_t st) {
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, moe::gg::BM)) return MOE_ERR_CUDA;
+    if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, moe::gg::BN)) return MOE_ERR_CUDA;
+    moe::gg::Params p;
+    p.mtiles = mtiles;
+    p.num_mtiles = num_mtiles;
+    p.max_mtiles = max_tiles;
+    p.dense_rows = dense_rows;
+    p.n_out = n_out;
+    p.k_dim = k_dim;
+    p.num_groups = groups;
+    p.out_rows = out_rows;
+    p.bias = bias;
+    p.out = out;
+    p.gelu = gelu ? 1 : 0;
+    p.raster = 8;
+    const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::BM - 1) / moe::gg::BM;
+    const int n_tiles = (n_out + moe::gg::BN - 1) / moe::gg::BN;
+    int64_t work = (int64_t)m_upper * n_tiles;
+    int grid = dev->num_sms;
+    if (work < grid) grid = (int)work;
+    if (grid < 1) grid = 1;
+    moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, p);
+    count_launch();
+    return MOE_OK;
+}
+
+moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm, const int32_t *offsets,
+                   const moe_weights *wt, const uint16_t *x, uint16_t *y_perm, uint16_t *z,
+                   const FfnWs &w, cudaStream_t st, cudaEvent_t mid = nullptr) {
+    const int T = s->T, N = s->N, K = s->K, d = s->d_model, f = s->d_ff;
+    const int rows = T * K;
+    const int mt = max_mtiles(s);
+    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, mt, w.mtiles, w.num_mtiles);
+    count_launch();
+    moe_status r;
+    // routed experts: H = GELU(x_perm W1^T + b1), y_perm = H W2^T + b2
+    r = launch_gemm(dev, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
+                    w.num_mtiles, mt, 0, true, st);
+    if (r != MOE_OK) return r;
+    if (s->has_shared) {
+        r = launch_gemm(dev, x, T, wt->Ws1, f, d, f, 1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T, true, st);
+        if (r != MOE_OK) return r;
+    }
+    if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
+    r = launch_gemm(dev, w.H, rows, wt->W2, (uint64_t)N * d, f, d, N, wt->b2, y_perm, rows, w.mtiles,
+                    w.num_mtiles, mt, 0, false, st);
+    if (r != MOE_OK) return r;
+    if (s->has_shared) {
+        r = launch_gemm(dev, w.Hs, T, wt->Ws2, d, f, d, 1, wt->bs2, z, T, nullptr, nullptr, 0, T, false, st);
+        if (r != MOE_OK) return r;
+    }
+    return launch_status();
+}
+
+moe_status run_combine(const moe_shape *s, const uint16_t *y_perm, const int32_t *slot_of,
+                       const float *topk_w, const uint16_t *z, uint16_t *y, cudaStream_t st) {
+    moe::dispatch::combine_kernel<<<s->T, 256, 0, st>>>(y_perm, slot_of, topk_w, z, s->T, s->K, s->d_model,
+                                                        s->T * s->K, y);
+    count_launch();
+    return launch_status();
+}
+
+moe_status run_aux(const moe_shape *s, const int32_t *demand, const float *prob_sum, float *aux,
+                   cudaStream_t st) {
+    moe::dispatch::aux_loss_kernel<<<1, 256, 0, st>>>(demand, prob_sum, s->T, s->N, s->K, s->aux_alpha, aux);
+    count_launch();
+    return launch_status();
+}
+
+bool weights_ok(const moe_shape *s, const moe_weights *w, bool need_gate) {
+    if (w == nullptr) return false;
+    if (need_gate && (w->Wg == nullptr || !aligned16(w->Wg))) return false;
+    const void *req[] = {w->W1, w->b1, w->W2, w->b2};
+    for (const void *p : req)
+        if (p == nullptr || !aligned16(p)) return false;
+    if (s->has_shared) {
+        const void *sh[] = {w->Ws1, w->bs1, w->Ws2, w->bs2};
+        for (const void *p : sh)
+            if (p == nullptr || !aligned16(p)) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+int32_t moe_capacity(const moe_shape *shape) {
+    if (check_shape(shape) != MOE_OK) return -1;
+    return capacity_of(shape);
+}
+
+size_t moe_workspace_bytes(const moe_shape *shape, int32_t kind) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return ws_bytes(shape, kind);
+}
+
+const char *moe_status_string(int32_t status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE: return "device-side error";
+        default: return "unknown status";
+    }
+}
+
+moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *Wg, const float *sel_bias,
+                     int32_t *topk_idx, float *topk_w, int32_t *demand, float *prob_sum, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x || !Wg || !topk_idx || !topk_w || !demand || !prob_sum) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(shape, MOE_WS_ROUTE, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    Carve c(workspace);
+    RouteWs w = carve_route(c, shape);
+    return run_route(shape, dev, x, Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, w, as_stream(stream));
+}
+
+moe_status moe_dispatch(const moe_shape *shape, const int32_t *topk_idx, const moe_bf16 *x, int32_t *kept,
+                        int32_t *expert_offsets, int32_t *slot_of, int32_t *row_token, moe_bf16 *x_perm,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!topk_idx || !x || !kept || !expert_offsets || !slot_of || !row_token || !x_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(shape, MOE_WS_DISPATCH, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    Carve c(workspace);
+    DispatchWs w = carve_dispatch(c, shape);
+    return run_dispatch(shape, topk_idx, x, kept, expert_offsets, slot_of, row_token, x_perm, w,
+                        as_stream(stream));
+}
+
+moe_status moe_expert_ffn(const moe_shape *shape, const moe_bf16 *x_perm, const int32_t *expert_offsets,
+                          const moe_weights *weights, const moe_bf16 *x, moe_bf16 *y_perm, moe_bf16 *z_shared,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x_perm || !expert_offsets || !y_perm || !weights_ok(shape, weights, false)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+    if (shape->has_shared && (!x || !z_shared || !aligned16(x) || !aligned16(z_shared)))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(shape, MOE_WS_FFN, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    Carve c(workspace);
+    FfnWs w = carve_ffn(c, shape);
+    return run_ffn(shape, dev, x_perm, expert_offsets, weights, x, y_perm, z_shared, w, as_stream(stream));
+}
+
+moe_status moe_combine(const moe_shape *shape, const moe_bf16 *y_perm, const int32_t *slot_of,
+                       const float *topk_w, const moe_bf16 *z_shared, moe_bf16 *y, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!y_perm || !slot_of || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_perm) || !aligned16(y) || (z_shared && !aligned16(z_shared))) return MOE_ERR_INVALID_ARG;
+    return run_combine(shape, y_perm, slot_of, topk_w, z_shared, y, as_stream(stream));
+}
+
+moe_status moe_aux_loss(const moe_shape *shape, const int32_t *demand, const float *prob_sum, float *aux,
+                        void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!demand || !prob_sum || !aux) return MOE_ERR_INVALID_ARG;
+    return run_aux(shape, demand, prob_sum, aux, as_stream(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
+                        const float *sel_bias, moe_bf16 *y, const moe_route_out *out, void *workspace,
+                        size_t workspace_bytes, void *const *events, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x || !y || !aligned16(x) || !aligned16(y) || !weights_ok(shape, weights, true)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(shape, MOE_WS_FORWARD, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    cudaStream_t st = as_stream(stream);
+    Carve c(workspace);
+    ForwardWs w = carve_forward(c, shape);
+    moe_route_out o;
+    std::memset(&o, 0, sizeof o);
+    if (out) o = *out;
+    int32_t *topk_idx = o.topk_idx ? o.topk_idx : w.topk_idx;
+    float *topk_w = o.topk_w ? o.topk_w : w.topk_w;
+    int32_t *demand = o.demand ? o.demand : w.demand;
+    float *prob_sum = o.prob_sum ? o.prob_sum : w.prob_sum;
+    int32_t *kept = o.kept ? o.kept : w.kept;
+    int32_t *offsets = o.expert_offsets ? o.expert_offsets : w.offsets;
+    int32_t *slot_of = o.slot_of ? o.slot_of : w.slot_of;
+    float *aux = o.aux ? o.aux : w.aux;
+
+    auto mark = [&](int i) -> bool {
+        return events == nullptr || events[i] == nullptr ||
+               cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+    };
+    if (!mark(0)) return MOE_ERR_CUDA;
+    if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, w.route, st)) !=
+        MOE_OK)
+        return r;
+    if (!mark(1)) return MOE_ERR_CUDA;
+    if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st)) != MOE_OK)
+        return r;
+    if (!mark(2)) return MOE_ERR_CUDA;
+    cudaEvent_t mid = events ? reinterpret_cast<cudaEvent_t>(events[3]) : nullptr;
+    if ((r = run_ffn(shape, dev, w.x_perm, offsets, weights, x, w.y_perm, w.z, w.ffn, st, mid)) != MOE_OK) return r;
+    if (!mark(4)) return MOE_ERR_CUDA;
+    if ((r = run_combine(shape, w.y_perm, slot_of, topk_w, w.z, y, st)) != MOE_OK) return r;
+    if ((r = run_aux(shape, demand, prob_sum, aux, st)) != MOE_OK) return r;
+    if (!mark(5)) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
+                       const float *sel_bias, moe_bf16 *y, const moe_route_out *out, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    return forward_impl(shape, weights, x, sel_bias, y, out, workspace, workspace_bytes, nullptr, stream);
+}
+
+moe_status moe_forward_marked(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
+                              const float *sel_bias, moe_bf16 *y, const moe_route_out *out, void *workspace,
+                              size_t workspace_bytes, void *const *events, void *stream) {
+    if (events == nullptr) return MOE_ERR_INVALID_ARG;
+    return forward_impl(shape, weights, x, sel_bias, y, out, workspace, workspace_bytes, events, stream);
+}
+
+moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x_host,
+                              moe_bf16 *x_dev, const float *sel_bias, moe_bf16 *y_dev, moe_bf16 *y_host,
+                              const moe_route_out *out, void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+    if (!x_dev || !y_dev || !aligned16(x_dev) || !aligned16(y_dev)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    const size_t bytes = (size_t)shape->T * shape->d_model * sizeof(moe_bf16);
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if ((r = moe_forward(shape, weights, x_dev, sel_bias, y_dev, out, workspace, workspace_bytes, stream)) != MOE_OK)
+        return r;
+    if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_get_device_error(int32_t clear, int32_t *code_out) {
+    if (code_out == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, moe::g_device_error, sizeof v) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    if (clear) {
+        unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(moe::g_device_error, &zero, sizeof zero) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    }
+    *code_out = (int32_t)v;
+    return MOE_OK;
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -19,8 +19,10 @@ DeepSeek-V3-shaped layers, a tiny layer and a skewed fine-grained layer):
   N(0, 1/fan_in) and rounded to bf16 (torch's RNE cast); biases N(0, 0.02^2)
   in fp32.
 * Skewed routing: expert e's gate row gets an additive Zipf(s=1.2) offset
-  ``round(4 * (e+1)^-1.2) / 64`` on every entry, which stays on the 1/64 grid
-  and makes the first few experts hot.
+  ``round(16 * (e+1)^-1.2) / 64`` on every entry. It stays on the 1/64 grid
+  (|W_g| <= 0.375, so logits stay exact multiples of 2^-12 below 2^12) and
+  makes experts 0 and 1 hot: about 9x and 3x the mean demand at
+  T=8192, N=64, K=2.
 * Aux-loss-free selection bias ``b_i`` ~ U(-0.05, 0.05) rounded to a multiple
   of 2^-12 (so ``s + b`` stays exact in fp32), fp32.
 * Shared expert weights drawn like the routed ones.
@@ -97,7 +99,7 @@ class MoEInputs:
                          {k: mv(v) for k, v in self.extra.items()})
 
 
-ZIPF_AMPLITUDE_64THS = 4
+ZIPF_AMPLITUDE_64THS = 16
 ZIPF_S = 1.2
 
 
