@@ -34,7 +34,7 @@
  *    MOE_ERR_INVALID_ARG: a NULL required pointer, a non-positive size,
  *    K > N, a misaligned pointer (bf16/fp32 tensors need 16-byte alignment).
  *    MOE_ERR_UNSUPPORTED: d_model or d_ff not a multiple of 64, K > 8,
- *    N > 1024, T * K >= 2^31. MOE_ERR_WORKSPACE: workspace NULL or smaller than
+ *    N > 1024, ceil(T * K / 128) + N > 65535. MOE_ERR_WORKSPACE: workspace NULL or smaller than
  *    required. MOE_ERR_CUDA: a CUDA launch error (the CUDA error is consumed).
  *  - Device-side consistency checks (an expert id outside [0, N), a row index
  *    outside its buffer, a pipeline wait that exceeds its time limit) never
@@ -205,11 +205,11 @@ MOE_API moe_status moe_forward(const moe_shape *shape, const moe_weights *weight
 
 /* moe_forward that also records timing marks on `stream`: events[i] is a
  * cudaEvent_t created by the caller (a NULL entry is skipped), recorded
- *   0 before routing, 1 after routing, 2 after dispatch,
+ *   0 before routing, 1 after routing (with the aux loss), 2 after dispatch,
  *   3 after the first grouped GEMM (tile list, x W1^T, shared expert's first
- *     Linear), 4 after the second grouped GEMM, 5 after combine and aux loss.
+ *     Linear), 4 after the second grouped GEMM, 5 after combine.
  * events must point to 6 entries. The kernels launched are those of
- * moe_forward. */
+ * moe_forward (which computes the aux loss inside its routing stage). */
 MOE_API moe_status moe_forward_marked(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
                                       const float *sel_bias, moe_bf16 *y, const moe_route_out *out,
                                       void *workspace, size_t workspace_bytes, void *const *events,

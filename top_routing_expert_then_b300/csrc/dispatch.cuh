@@ -109,76 +109,117 @@ assign_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int C,
     }
 }
 
-// x_perm[slot_of[t, k]] = x[t]: one block per token reads its row once and
-// writes it to each of its kept slots (16-byte vectors).
+// Tokens per block in the permute and combine kernels: a thread owns one
+// 16-byte column chunk of kRowTok consecutive tokens, so one block issues all
+// of its loads after a single round trip for the dispatch table.
+constexpr int kRowTok = 8;
+
+// x_perm[slot_of[t, k]] = x[t].
 __global__ void __launch_bounds__(256)
-permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_of, int T, int K,
-               int d, int rows, uint16_t *__restrict__ x_perm) {
-    const int t = blockIdx.x;
-    __shared__ int slots[8];
-    if (threadIdx.x < K) {
-        int s = slot_of[(size_t)t * K + threadIdx.x];
-        if (s >= rows) {
-            flag_error(MOE_DEVERR_ROW_INDEX);
-            s = -1;
+permute_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ slot_of, int T, int K, int d,
+               int rows, uint16_t *__restrict__ x_perm) {
+    const int t0 = blockIdx.x * kRowTok;
+    const int c = blockIdx.y * blockDim.x + threadIdx.x;
+    const int vec = d >> 3;
+    __shared__ int slots[kRowTok][8];
+    if (threadIdx.x < kRowTok * K) {
+        const int i = threadIdx.x / K, k = threadIdx.x % K;
+        int s = -1;
+        if (t0 + i < T) {
+            s = slot_of[(size_t)(t0 + i) * K + k];
+            if (s >= rows) {
+                flag_error(MOE_DEVERR_ROW_INDEX);
+                s = -1;
+            }
         }
-        slots[threadIdx.x] = s;
+        slots[i][k] = s;
     }
     __syncthreads();
-    const int vec = d >> 3;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
-    for (int c = threadIdx.x; c < vec; c += blockDim.x) {
-        uint4 v = __ldg(src + c);
-        for (int k = 0; k < K; ++k) {
-            int s = slots[k];
-            if (s >= 0) reinterpret_cast<uint4 *>(x_perm + (size_t)s * d)[c] = v;
+    if (c >= vec) return;
+    uint4 v[kRowTok];
+#pragma unroll
+    for (int i = 0; i < kRowTok; ++i)
+        if (t0 + i < T) v[i] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c);
+#pragma unroll
+    for (int i = 0; i < kRowTok; ++i) {
+        if (t0 + i >= T) break;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < K) {
+                const int s = slots[i][k];
+                if (s >= 0) reinterpret_cast<uint4 *>(x_perm + (size_t)s * d)[c] = v[i];
+            }
         }
     }
 }
 
 // y[t] = bf16(z[t] + sum_k w[t,k] * y_perm[slot_of[t,k]]), fp32, increasing k.
+// A thread owns one 16-byte column chunk of TOK = 8 / KMAX consecutive tokens
+// and issues all TOK * KMAX row loads before any arithmetic.
+template <int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t *__restrict__ y_perm, const int32_t *__restrict__ slot_of,
-               const float *__restrict__ topk_w, const uint16_t *__restrict__ z, int T, int K,
-               int d, int rows, uint16_t *__restrict__ y) {
-    const int t = blockIdx.x;
-    __shared__ int slots[8];
-    __shared__ float wts[8];
-    if (threadIdx.x < K) {
-        int s = slot_of[(size_t)t * K + threadIdx.x];
-        if (s >= rows) {
-            flag_error(MOE_DEVERR_ROW_INDEX);
-            s = -1;
+               const float *__restrict__ topk_w, const uint16_t *__restrict__ z, int T, int K, int d, int rows,
+               uint16_t *__restrict__ y) {
+    constexpr int TOK = 8 / KMAX;
+    const int t0 = blockIdx.x * TOK;
+    const int c = blockIdx.y * blockDim.x + threadIdx.x;
+    const int vec = d >> 3;
+    __shared__ int slots[TOK][KMAX];
+    __shared__ float wts[TOK][KMAX];
+    if (threadIdx.x < TOK * KMAX) {
+        const int i = threadIdx.x / KMAX, k = threadIdx.x % KMAX;
+        int s = -1;
+        float w = 0.f;
+        if (t0 + i < T && k < K) {
+            s = slot_of[(size_t)(t0 + i) * K + k];
+            w = topk_w[(size_t)(t0 + i) * K + k];
+            if (s >= rows) {
+                flag_error(MOE_DEVERR_ROW_INDEX);
+                s = -1;
+            }
         }
-        slots[threadIdx.x] = s;
-        wts[threadIdx.x] = topk_w[(size_t)t * K + threadIdx.x];
+        slots[i][k] = s;
+        wts[i][k] = w;
     }
     __syncthreads();
-    const int vec = d >> 3;
-    for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+    if (c >= vec) return;
+    uint4 v[TOK][KMAX];
+#pragma unroll
+    for (int i = 0; i < TOK; ++i)
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int sl = slots[i][k];
+            v[i][k] = sl >= 0 ? __ldg(reinterpret_cast<const uint4 *>(y_perm + (size_t)sl * d) + c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) {
+        const int t = t0 + i;
+        if (t >= T) break;
         float acc[8];
         if (z != nullptr) {
-            uint4 v = __ldg(reinterpret_cast<const uint4 *>(z + (size_t)t * d) + c);
-            unpack_bf16x2(v.x, acc[0], acc[1]);
-            unpack_bf16x2(v.y, acc[2], acc[3]);
-            unpack_bf16x2(v.z, acc[4], acc[5]);
-            unpack_bf16x2(v.w, acc[6], acc[7]);
+            uint4 zv = __ldg(reinterpret_cast<const uint4 *>(z + (size_t)t * d) + c);
+            unpack_bf16x2(zv.x, acc[0], acc[1]);
+            unpack_bf16x2(zv.y, acc[2], acc[3]);
+            unpack_bf16x2(zv.z, acc[4], acc[5]);
+            unpack_bf16x2(zv.w, acc[6], acc[7]);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = 0.f;
         }
-        for (int k = 0; k < K; ++k) {
-            int s = slots[k];
-            if (s < 0) continue;
-            float wk = wts[k];
-            uint4 v = __ldg(reinterpret_cast<const uint4 *>(y_perm + (size_t)s * d) + c);
-            float f[8];
-            unpack_bf16x2(v.x, f[0], f[1]);
-            unpack_bf16x2(v.y, f[2], f[3]);
-            unpack_bf16x2(v.z, f[4], f[5]);
-            unpack_bf16x2(v.w, f[6], f[7]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(wk, f[j], acc[j]);
+        for (int k = 0; k < KMAX; ++k) {
+            if (slots[i][k] >= 0) {
+                const float wk = wts[i][k];
+                float f[8];
+                unpack_bf16x2(v[i][k].x, f[0], f[1]);
+                unpack_bf16x2(v[i][k].y, f[2], f[3]);
+                unpack_bf16x2(v[i][k].z, f[4], f[5]);
+                unpack_bf16x2(v[i][k].w, f[6], f[7]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(wk, f[j], acc[j]);
+            }
         }
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);

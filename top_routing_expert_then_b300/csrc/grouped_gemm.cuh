@@ -73,7 +73,7 @@ struct Params {
     const float *bias;        // [num_groups, n_out]
     uint16_t *out;            // [out_rows, n_out] bf16
     int gelu;                 // 1: GELU epilogue
-    int raster;               // m-tiles per raster group
+    int raster;               // m-tiles per raster group (dense mode; the list mode stores groups)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -212,26 +212,44 @@ struct Tile {
     bool ok;
 };
 
+template <int TM>
 __device__ __forceinline__ int num_m_tiles(const Params &p) {
-    if (p.mtiles == nullptr) return (p.dense_rows + BM - 1) / BM;
+    if (p.mtiles == nullptr) return (p.dense_rows + TM - 1) / TM;
     int n = *p.num_mtiles;
     return n < 0 ? 0 : (n > p.max_mtiles ? p.max_mtiles : n);
 }
 
-// Work item w -> (m-tile, n-tile): raster groups of `raster` m-tiles; inside a
-// group the m index runs fastest, so the blocks in flight share B tiles.
+// Work item w -> (m-tile, n-tile). The m-tiles are cut into raster groups of
+// at most `raster` consecutive m-tiles of ONE expert; group j with first
+// m-tile m_j and g_j tiles owns the items [m_j * num_n, (m_j + g_j) * num_n),
+// m running fastest inside the group. So the blocks in flight at any time
+// work on a few experts' n-tiles at once and share their B (weight) tiles.
+// Each m-tile entry carries its group as (m_j << 16) | g_j in .w; the dense
+// mode (one group of rows) computes the same grouping arithmetically.
+template <int TM>
 __device__ __forceinline__ Tile tile_of(const Params &p, int w, int num_m, int num_n) {
-    const int G = p.raster;
-    const int g = w / (G * num_n);
-    const int local = w - g * G * num_n;
-    const int gm_left = num_m - g * G;
-    const int gm = gm_left < G ? gm_left : G;
-    const int m = g * G + local % gm;
-    const int n = local / gm;
-    Tile t;
+    const int q = w / num_n;  // an m-tile of the group that owns item w
+    int mj, gj;
     if (p.mtiles == nullptr) {
-        t.row0 = m * BM;
-        t.rows = min(BM, p.dense_rows - t.row0);
+        mj = (q / p.raster) * p.raster;
+        gj = min(p.raster, num_m - mj);
+    } else {
+        const int packed = p.mtiles[q].w;
+        mj = packed >> 16;
+        gj = packed & 0xFFFF;
+    }
+    Tile t;
+    t.ok = false;
+    if (gj <= 0 || mj < 0 || mj + gj > num_m) {
+        t.row0 = t.rows = t.group = t.n0 = 0;
+        return t;
+    }
+    const int local = w - mj * num_n;
+    const int m = mj + local % gj;
+    const int n = local / gj;
+    if (p.mtiles == nullptr) {
+        t.row0 = m * TM;
+        t.rows = min(TM, p.dense_rows - t.row0);
         t.group = 0;
     } else {
         int4 v = p.mtiles[m];
@@ -240,8 +258,8 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int w, int num_m, int n
         t.group = v.z;
     }
     t.n0 = n * BN;
-    t.ok = t.rows > 0 && t.rows <= BM && t.row0 >= 0 && t.row0 + t.rows <= p.out_rows &&
-           t.group >= 0 && t.group < p.num_groups;
+    t.ok = t.rows > 0 && t.rows <= TM && t.row0 >= 0 && t.row0 + t.rows <= p.out_rows &&
+           t.group >= 0 && t.group < p.num_groups && n < num_n;
     return t;
 }
 
@@ -291,7 +309,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
     const uint32_t tmem_base = sh->tmem_base;
 
-    const int num_m = num_m_tiles(p);
+    const int num_m = num_m_tiles<BM>(p);
     const int num_n = (p.n_out + BN - 1) / BN;
     const int total = num_m * num_n;
     const int kblocks = p.k_dim / BK;
@@ -304,7 +322,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                Tile t = tile_of(p, w, num_m, num_n);
+                Tile t = tile_of<BM>(p, w, num_m, num_n);
                 if (!t.ok) continue;
                 const int brow = t.group * p.n_out + t.n0;
                 for (int kb = 0; kb < kblocks; ++kb) {
@@ -339,7 +357,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                Tile t = tile_of(p, w, num_m, num_n);
+                Tile t = tile_of<BM>(p, w, num_m, num_n);
                 if (!t.ok) continue;
                 if (!wait_bounded(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true))
                     break;
@@ -381,7 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int row = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            Tile t = tile_of(p, w, num_m, num_n);
+            Tile t = tile_of<BM>(p, w, num_m, num_n);
             if (!t.ok) {
                 if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
                 continue;
@@ -442,12 +460,334 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
 }
 
+// ============================================================================
+// SM-pair variant: a cluster of 2 CTAs on two SMs runs tcgen05.mma.cta_group::2
+// with M = 256 (128 rows per SM), N = 256, K = 16. Each CTA stages its own 128
+// rows of A and its half (128 of the 256 output columns) of B per k-block, so
+// a stage is 32 KB and the ring is 6 deep; each SM's TMEM holds its 128 rows
+// of the 256 x 256 accumulator (two buffers of 256 columns).
+//   rank 0 ("leader"): TMA for its halves, arms the stage barrier for the
+//                      pair's 64 KB, issues the MMAs, commits to both CTAs
+//   rank 1:            TMA for its halves, completing on the leader's barrier
+//   both:              epilogue of their own 128 rows; arrive on the
+//                      leader's accumulator-empty barrier
+// Work unit: a 256 x 256 tile of one expert (m-tiles of 256 rows).
+constexpr int PAIR_BM = 256;
+#ifndef MOE_PAIR_STAGES
+#define MOE_PAIR_STAGES 6
+#endif
+constexpr int P_STAGES = MOE_PAIR_STAGES;
+constexpr int P_A_BYTES = 128 * BK * 2;
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024;
+constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)(PAIR_BM >> 4) << 24);
+
+struct PairShared {
+    uint64_t full[P_STAGES];
+    uint64_t empty[P_STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(PairShared) <= BAR_BYTES, "barrier block too large");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier that may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                 int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(IDESC_PAIR), "r"(acc)
+        : "memory");
+}
+
+// Arrive (once the MMAs issued so far complete) on the barrier at this
+// shared-memory offset in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __noinline__ bool wait_bounded_pair(PairShared *sh, uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                               bool raise, bool cluster_scope) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (raise && sh->abort_flag) return false;
+            uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                if (raise) {
+                    sh->abort_flag = 1;
+                    flag_error(MOE_DEVERR_TIMEOUT);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    PairShared *sh = reinterpret_cast<PairShared *>(smem + P_STAGES * P_STAGE_BYTES);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&sh->full[s]), 1);
+            mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sh->tfull[a]), 1);
+            mbar_init(smem_u32(&sh->tempty[a]), 8);
+        }
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sh->tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_base;
+
+    const int num_m = num_m_tiles<PAIR_BM>(p);
+    const int num_n = (p.n_out + BN - 1) / BN;
+    const int total = num_m * num_n;
+    const int kblocks = p.k_dim / BK;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            uint32_t stage = 0, phase = 0;
+            int issued_phase[P_STAGES];
+            for (int s = 0; s < P_STAGES; ++s) issued_phase[s] = -1;
+            bool stop = false;
+            for (int w = cluster_id; w < total && !stop; w += num_clusters) {
+                Tile t = tile_of<PAIR_BM>(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                const int arow = t.row0 + (int)rank * 128;
+                const int brow = t.group * p.n_out + t.n0 + (int)rank * (BN / 2);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded_pair(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true,
+                                           false)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb_local = smem_u32(&sh->full[stage]);
+                    const uint32_t fb_leader = map_to_rank(fb_local, 0);
+                    uint8_t *a_s = smem + stage * P_STAGE_BYTES;
+                    if (leader) mbar_arrive_expect_tx(fb_local, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(smem_u32(a_s), &tmA, fb_leader, kb * BK, arow);
+                    tma_load_2d_pair(smem_u32(a_s + P_A_BYTES), &tmB, fb_leader, kb * BK, brow);
+                    issued_phase[stage] = (int)phase;
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (stop && leader) {
+                for (int s = 0; s < P_STAGES; ++s)
+                    if (issued_phase[s] >= 0)
+                        wait_bounded_pair(sh, smem_u32(&sh->full[s]), (uint32_t)issued_phase[s], DRAIN_LIMIT_NS,
+                                          false, true);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (leader only)
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool stop = false;
+            for (int w = cluster_id; w < total && !stop; w += num_clusters) {
+                Tile t = tile_of<PAIR_BM>(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                if (!wait_bounded_pair(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true, true))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!wait_bounded_pair(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true, true)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * P_STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + P_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        mma_bf16_pair(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
+                                      (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair(smem_u32(&sh->empty[stage]));
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (stop) break;
+                mma_commit_pair(smem_u32(&sh->tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            mma_commit_pair(smem_u32(&sh->drain));
+            wait_bounded_pair(sh, smem_u32(&sh->drain), 0, DRAIN_LIMIT_NS, false, false);
+        } else if (lane == 0) {
+            // the leader's final commit also arrives here: wait for it so that no
+            // arrival from this pair's MMAs is still in flight when the CTA exits
+            wait_bounded_pair(sh, smem_u32(&sh->drain), 0, WAIT_LIMIT_NS, false, false);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2-5, both CTAs)
+        const int q = warp & 3;
+        const int row = (int)rank * 128 + q * 32 + lane;  // row within the 256-row tile
+        const uint32_t tempty_leader0 = map_to_rank(smem_u32(&sh->tempty[0]), 0);
+        const uint32_t tempty_leader1 = map_to_rank(smem_u32(&sh->tempty[1]), 0);
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = cluster_id; w < total; w += num_clusters) {
+            Tile t = tile_of<PAIR_BM>(p, w, num_m, num_n);
+            if (!t.ok) {
+                if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
+                continue;
+            }
+            if (!wait_bounded_pair(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true, false)) break;
+            tc_fence_after();
+            const bool store = row < t.rows;
+            uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
+            const float *bias = p.bias + (size_t)t.group * p.n_out;
+            const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                const int col = t.n0 + c0;
+                if (col >= p.n_out) break;  // warp-uniform
+                uint32_t r[32];
+                tmem_ld32(tbase + c0, r);
+                uint32_t packed[16];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 b = __ldg(reinterpret_cast<const float4 *>(bias + col + j));
+                    float v0 = __uint_as_float(r[j + 0]) + b.x;
+                    float v1 = __uint_as_float(r[j + 1]) + b.y;
+                    float v2 = __uint_as_float(r[j + 2]) + b.z;
+                    float v3 = __uint_as_float(r[j + 3]) + b.w;
+                    if (p.gelu) {
+                        v0 = gelu_erf(v0);
+                        v1 = gelu_erf(v1);
+                        v2 = gelu_erf(v2);
+                        v3 = gelu_erf(v3);
+                    }
+                    packed[j / 2] = pack_bf16x2(v0, v1);
+                    packed[j / 2 + 1] = pack_bf16x2(v2, v3);
+                }
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                            packed[4 * j + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no remote arrive or multicast commit still targets either CTA
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // The m-tile list of the routed experts, from the expert offsets:
-// expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / BM) tiles.
-// One block of 1024 threads; N <= 1024.
+// expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / tile_rows)
+// tiles, cut into raster groups of at most `raster` tiles (see tile_of).
+// One block of 1024 threads; N <= 1024; at most 65535 tiles.
 __global__ void __launch_bounds__(1024)
-build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int max_tiles,
-                    int4 *__restrict__ mtiles, int *__restrict__ num_mtiles) {
+build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int tile_rows, int raster,
+                    int max_tiles, int4 *__restrict__ mtiles, int *__restrict__ num_mtiles) {
     __shared__ int sc[1024];
     const int e = threadIdx.x;
     int cnt = 0, r0 = 0, r1 = 0;
@@ -458,7 +798,7 @@ build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, 
         if (r0 < 0 || r1 < r0 || r1 > total_rows) {
             bad = true;
         } else {
-            cnt = (r1 - r0 + BM - 1) / BM;
+            cnt = (r1 - r0 + tile_rows - 1) / tile_rows;
         }
     }
     if (bad) flag_error(MOE_DEVERR_TILE_LIST);
@@ -475,9 +815,11 @@ build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, 
     for (int i = 0; i < cnt; ++i) {
         int m = start + i;
         if (m < max_tiles) {
-            int rr = r0 + i * BM;
-            int rows = r1 - rr < BM ? r1 - rr : BM;
-            mtiles[m] = make_int4(rr, rows, e, 0);
+            int rr = r0 + i * tile_rows;
+            int rows = r1 - rr < tile_rows ? r1 - rr : tile_rows;
+            const int gfirst = start + (i / raster) * raster;   // raster groups stay inside expert e
+            const int gsize = min(raster, cnt - (i / raster) * raster);
+            mtiles[m] = make_int4(rr, rows, e, (gfirst << 16) | gsize);
         }
     }
     if (e == 1023) *num_mtiles = v < max_tiles ? v : max_tiles;

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -60,6 +61,7 @@ moe_status check_shape(const moe_shape *s) {
     if ((int64_t)s->T * s->K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)s->N * s->d_ff >= (int64_t(1) << 31) || (int64_t)s->N * s->d_model >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
+    if (((int64_t)s->T * s->K + 127) / 128 + s->N > 65535) return MOE_ERR_UNSUPPORTED;  // m-tile list index
     return MOE_OK;
 }
 
@@ -85,7 +87,7 @@ struct RouteWs {
 RouteWs carve_route(Carve &c, const moe_shape *s) {
     RouteWs w;
     w.logits = c.take<float>((size_t)s->T * s->N);
-    w.partial = c.take<float>((size_t)moe::route::topk_grid(s->T) * s->N);
+    w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
     return w;
 }
 
@@ -175,7 +177,6 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 
 constexpr int kSmallGateMaxN = 16;
-constexpr size_t kSmallGateMaxSmem = 200 * 1024;
 
 moe_status device_state(DeviceState **out) {
     int dev = 0;
@@ -190,11 +191,8 @@ moe_status device_state(DeviceState **out) {
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe::route::gate_logits_smallN_kernel<8>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallGateMaxSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe::route::gate_logits_smallN_kernel<16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallGateMaxSmem);
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_pair_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::P_SMEM_BYTES);
         st.init_err = e;
     });
     if (st.init_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -242,42 +240,44 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, u
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
-                     float *prob_sum, const RouteWs &w, cudaStream_t st) {
+                     float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
     (void)dev;
-    const size_t wg_bytes = (size_t)N * d * 2;
-    if (N <= kSmallGateMaxN && wg_bytes <= kSmallGateMaxSmem) {
-        const int warps = moe::route::kGateThreads / 32;
-        int grid = (T + warps - 1) / warps;
-        if (grid > 1184) grid = 1184;
+    if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
+    int rows;
+    if (N <= kSmallGateMaxN) {
+        // gate + TopK + softmax + statistics in one kernel
+        rows = moe::route::small_router_grid(T);
+        const int thr = moe::route::kRouterWarps * 32;
         if (N <= 8)
-            moe::route::gate_logits_smallN_kernel<8>
-                <<<grid, moe::route::kGateThreads, wg_bytes, st>>>(x, Wg, T, d, N, w.logits);
+            moe::route::router_smallN_kernel<8><<<rows, thr, 0, st>>>(x, Wg, sel_bias, T, d, N, K, topk_idx,
+                                                                      topk_w, demand, w.partial);
         else
-            moe::route::gate_logits_smallN_kernel<16>
-                <<<grid, moe::route::kGateThreads, wg_bytes, st>>>(x, Wg, T, d, N, w.logits);
+            moe::route::router_smallN_kernel<16><<<rows, thr, 0, st>>>(x, Wg, sel_bias, T, d, N, K, topk_idx,
+                                                                       topk_w, demand, w.partial);
+        count_launch();
     } else {
         dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
         moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N, w.logits);
-    }
-    count_launch();
-    if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
-    const int grid = moe::route::topk_grid(T);
-    const size_t smem = (size_t)moe::route::kTopkWarps * N * sizeof(float) + (size_t)N * sizeof(int);
-    const int lpl = (N + 31) / 32;
-    const int thr = moe::route::kTopkWarps * 32;
+        count_launch();
+        rows = moe::route::topk_grid(T);
+        const size_t smem = (size_t)moe::route::kTopkWarps * N * sizeof(float) + (size_t)N * sizeof(int);
+        const int lpl = (N + 31) / 32;
+        const int thr = moe::route::kTopkWarps * 32;
 #define MOE_TOPK(L)                                                                                     \
-    moe::route::topk_softmax_kernel<L><<<grid, thr, smem, st>>>(w.logits, sel_bias, T, N, K, topk_idx, \
+    moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, sel_bias, T, N, K, topk_idx, \
                                                                 topk_w, demand, w.partial)
-    if (lpl <= 1) MOE_TOPK(1);
-    else if (lpl <= 2) MOE_TOPK(2);
-    else if (lpl <= 4) MOE_TOPK(4);
-    else if (lpl <= 8) MOE_TOPK(8);
-    else if (lpl <= 16) MOE_TOPK(16);
-    else MOE_TOPK(32);
+        if (lpl <= 1) MOE_TOPK(1);
+        else if (lpl <= 2) MOE_TOPK(2);
+        else if (lpl <= 4) MOE_TOPK(4);
+        else if (lpl <= 8) MOE_TOPK(8);
+        else if (lpl <= 16) MOE_TOPK(16);
+        else MOE_TOPK(32);
 #undef MOE_TOPK
-    count_launch();
-    moe::route::prob_finalize_kernel<<<(N + 127) / 128, 128, 0, st>>>(w.partial, grid, N, prob_sum);
+        count_launch();
+    }
+    moe::route::route_finalize_kernel<<<1, 1024, 0, st>>>(w.partial, rows, N, T, K, s->aux_alpha, demand, prob_sum,
+                                                          aux);
     count_launch();
     return launch_status();
 }
@@ -299,18 +299,51 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
     moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
         topk_idx, T, N, K, C, w.base, offsets, slot_of, row_token);
     count_launch();
-    moe::dispatch::permute_kernel<<<T, 256, 0, st>>>(x, slot_of, T, K, d, rows, x_perm);
+    {
+        const int vec = d / 8;
+        const int thr = vec < 256 ? 64 : 256;
+        dim3 grid((T + moe::dispatch::kRowTok - 1) / moe::dispatch::kRowTok, (vec + thr - 1) / thr);
+        moe::dispatch::permute_kernel<<<grid, thr, 0, st>>>(x, slot_of, T, K, d, rows, x_perm);
+    }
     count_launch();
     return launch_status();
 }
 
-moe_status launch_gemm(DeviceState *dev, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
+// Which grouped-GEMM kernel runs. The SM-pair kernel (256-row tiles) cuts the
+// operand traffic per SM by a third but pads each expert's last tile to 256
+// rows; measured on the Mixtral-shaped layer it is slower than the single-SM
+// kernel (128-row tiles), so the default is the single-SM kernel.
+// MOE_GEMM_VARIANT=single|pair (environment, read once) forces one of them.
+enum GemmVariant { kAuto = 0, kSingle = 1, kPair = 2 };
+constexpr int kRasterSingle = 8;  // m-tiles (128 rows) per raster group
+constexpr int kRasterPair = 4;    // m-tiles (256 rows) per raster group
+int gemm_variant_override() {
+    static const int v = []() {
+        const char *e = std::getenv("MOE_GEMM_VARIANT");
+        if (e == nullptr) return (int)kAuto;
+        if (std::strcmp(e, "single") == 0) return (int)kSingle;
+        if (std::strcmp(e, "pair") == 0) return (int)kPair;
+        return (int)kAuto;
+    }();
+    return v;
+}
+
+bool use_pair(int64_t expected_rows_per_group) {
+    const int o = gemm_variant_override();
+    if (o == kSingle) return false;
+    if (o == kPair) return true;
+    (void)expected_rows_per_group;
+    return false;
+}
+
+moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
                        cudaStream_t st) {
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, moe::gg::BM)) return MOE_ERR_CUDA;
-    if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, moe::gg::BN)) return MOE_ERR_CUDA;
+    const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
+    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
+    if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
     moe::gg::Params p;
     p.mtiles = mtiles;
     p.num_mtiles = num_mtiles;
@@ -323,14 +356,23 @@ moe_status launch_gemm(DeviceState *dev, const void *A, uint64_t a_rows, const v
     p.bias = bias;
     p.out = out;
     p.gelu = gelu ? 1 : 0;
-    p.raster = 8;
-    const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::BM - 1) / moe::gg::BM;
+    const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
+    p.raster = pair ? kRasterPair : kRasterSingle;
+    const int m_upper = mtiles ? max_tiles : (dense_rows + tile_m - 1) / tile_m;
     const int n_tiles = (n_out + moe::gg::BN - 1) / moe::gg::BN;
-    int64_t work = (int64_t)m_upper * n_tiles;
-    int grid = dev->num_sms;
-    if (work < grid) grid = (int)work;
-    if (grid < 1) grid = 1;
-    moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, p);
+    const int64_t work = (int64_t)m_upper * n_tiles;
+    if (pair) {
+        int clusters = dev->num_sms / 2;
+        if (work < clusters) clusters = (int)work;
+        if (clusters < 1) clusters = 1;
+        moe::gg::grouped_gemm_pair_kernel<<<2 * clusters, moe::gg::NUM_THREADS, moe::gg::P_SMEM_BYTES, st>>>(ta, tb,
+                                                                                                        p);
+    } else {
+        int grid = dev->num_sms;
+        if (work < grid) grid = (int)work;
+        if (grid < 1) grid = 1;
+        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, p);
+    }
     count_launch();
     return MOE_OK;
 }
@@ -341,23 +383,33 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     const int T = s->T, N = s->N, K = s->K, d = s->d_model, f = s->d_ff;
     const int rows = T * K;
     const int mt = max_mtiles(s);
-    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, mt, w.mtiles, w.num_mtiles);
+    int64_t per_expert = (int64_t)T * K / N;
+    const int C = capacity_of(s);
+    if (per_expert > C) per_expert = C;
+    const bool pair_routed = use_pair(per_expert);
+    const bool pair_shared = use_pair(T);
+    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows,
+                                                     pair_routed ? moe::gg::PAIR_BM : moe::gg::BM,
+                                                     pair_routed ? kRasterPair : kRasterSingle, mt, w.mtiles,
+                                                     w.num_mtiles);
     count_launch();
     moe_status r;
     // routed experts: H = GELU(x_perm W1^T + b1), y_perm = H W2^T + b2
-    r = launch_gemm(dev, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
+    r = launch_gemm(dev, pair_routed, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
                     w.num_mtiles, mt, 0, true, st);
     if (r != MOE_OK) return r;
     if (s->has_shared) {
-        r = launch_gemm(dev, x, T, wt->Ws1, f, d, f, 1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T, true, st);
+        r = launch_gemm(dev, pair_shared, x, T, wt->Ws1, f, d, f, 1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T, true,
+                        st);
         if (r != MOE_OK) return r;
     }
     if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
-    r = launch_gemm(dev, w.H, rows, wt->W2, (uint64_t)N * d, f, d, N, wt->b2, y_perm, rows, w.mtiles,
+    r = launch_gemm(dev, pair_routed, w.H, rows, wt->W2, (uint64_t)N * d, f, d, N, wt->b2, y_perm, rows, w.mtiles,
                     w.num_mtiles, mt, 0, false, st);
     if (r != MOE_OK) return r;
     if (s->has_shared) {
-        r = launch_gemm(dev, w.Hs, T, wt->Ws2, d, f, d, 1, wt->bs2, z, T, nullptr, nullptr, 0, T, false, st);
+        r = launch_gemm(dev, pair_shared, w.Hs, T, wt->Ws2, d, f, d, 1, wt->bs2, z, T, nullptr, nullptr, 0, T, false,
+                        st);
         if (r != MOE_OK) return r;
     }
     return launch_status();
@@ -365,8 +417,19 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
 
 moe_status run_combine(const moe_shape *s, const uint16_t *y_perm, const int32_t *slot_of,
                        const float *topk_w, const uint16_t *z, uint16_t *y, cudaStream_t st) {
-    moe::dispatch::combine_kernel<<<s->T, 256, 0, st>>>(y_perm, slot_of, topk_w, z, s->T, s->K, s->d_model,
-                                                        s->T * s->K, y);
+    const int vec = s->d_model / 8;
+    const int thr = vec < 256 ? 64 : 256;
+    const int K = s->K;
+    const int kmax = K <= 1 ? 1 : (K <= 2 ? 2 : (K <= 4 ? 4 : 8));
+    dim3 grid((s->T + 8 / kmax - 1) / (8 / kmax), (vec + thr - 1) / thr);
+#define MOE_COMBINE(KM)                                                                                    \
+    moe::dispatch::combine_kernel<KM><<<grid, thr, 0, st>>>(y_perm, slot_of, topk_w, z, s->T, K, s->d_model, \
+                                                            s->T * K, y)
+    if (kmax == 1) MOE_COMBINE(1);
+    else if (kmax == 2) MOE_COMBINE(2);
+    else if (kmax == 4) MOE_COMBINE(4);
+    else MOE_COMBINE(8);
+#undef MOE_COMBINE
     count_launch();
     return launch_status();
 }
@@ -432,7 +495,8 @@ moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *
     if ((r = device_state(&dev)) != MOE_OK) return r;
     Carve c(workspace);
     RouteWs w = carve_route(c, shape);
-    return run_route(shape, dev, x, Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, w, as_stream(stream));
+    return run_route(shape, dev, x, Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, nullptr, w,
+                     as_stream(stream));
 }
 
 moe_status moe_dispatch(const moe_shape *shape, const int32_t *topk_idx, const moe_bf16 *x, int32_t *kept,
@@ -519,8 +583,8 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
                cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
     };
     if (!mark(0)) return MOE_ERR_CUDA;
-    if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, w.route, st)) !=
-        MOE_OK)
+    if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
+                       st)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st)) != MOE_OK)
@@ -530,7 +594,6 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     if ((r = run_ffn(shape, dev, w.x_perm, offsets, weights, x, w.y_perm, w.z, w.ffn, st, mid)) != MOE_OK) return r;
     if (!mark(4)) return MOE_ERR_CUDA;
     if ((r = run_combine(shape, w.y_perm, slot_of, topk_w, w.z, y, st)) != MOE_OK) return r;
-    if ((r = run_aux(shape, demand, prob_sum, aux, st)) != MOE_OK) return r;
     if (!mark(5)) return MOE_ERR_CUDA;
     return MOE_OK;
 }

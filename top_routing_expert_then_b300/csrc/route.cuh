@@ -15,56 +15,180 @@ namespace route {
 constexpr int kGateThreads = 256;
 
 // ---------------------------------------------------------------------------
-// Gate GEMM, small N: one warp per token, W_g resident in shared memory.
-// Lane j owns the 8-element column chunks j, j+32, ... of the token row and
-// accumulates all N logits for them; a butterfly reduction finishes each logit.
-template <int NMAX>
-__global__ void __launch_bounds__(kGateThreads)
-gate_logits_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ Wg, int T,
-                          int d, int N, float *__restrict__ logits) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint4 *wg_s = reinterpret_cast<uint4 *>(smem_raw);  // [N][d/8]
-    const int chunks = d >> 3;
-    const uint4 *wg_g = reinterpret_cast<const uint4 *>(Wg);
-    for (int i = threadIdx.x; i < N * chunks; i += blockDim.x) wg_s[i] = wg_g[i];
-    __syncthreads();
+// Small N (<= 16): the whole router in one kernel. A block of 4 warps takes 4
+// tokens at a time; warp w owns the 8-element column chunks c with
+// (c / 32) % 4 == w, lane j the chunks with c % 32 == j, and accumulates all N
+// logits of the 4 tokens over its chunks (W_g is read through L1: it is small
+// and shared by every block on the SM). The partial sums meet in shared memory
+// and warp 0 adds them in warp order, then runs TopK / softmax for the 4
+// tokens (every lane computes the same values; lane k writes rank k).
+constexpr int kRouterWarps = 4;
+constexpr int kTokensPerBlock = 4;
+constexpr int kMaxK = 8;
+constexpr int kMaxPartialRows = 1024;
 
+// Blocks of the small-N router: a function of T only, so the partial
+// probability sums (and hence prob_sum) are identical on every device.
+inline int small_router_grid(int T) {
+    int g = (T + kTokensPerBlock - 1) / kTokensPerBlock;
+    return g < 1 ? 1 : (g > kMaxPartialRows ? kMaxPartialRows : g);
+}
+
+template <int NMAX>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ Wg,
+                     const float *__restrict__ sel_bias, int T, int d, int N, int K,
+                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                     int32_t *__restrict__ demand, float *__restrict__ prob_partial) {
+    __shared__ float red[kRouterWarps][kTokensPerBlock][NMAX];
+    __shared__ int dcount[NMAX];
+    const int chunks = d >> 3;
     const int lane = lane_id();
-    const int warps = blockDim.x >> 5;
-    for (int t = blockIdx.x * warps + warp_id(); t < T; t += gridDim.x * warps) {
-        float acc[NMAX];
+    const int warp = warp_id();
+    if (threadIdx.x < NMAX) dcount[threadIdx.x] = 0;
+    float bias[NMAX];
+    float pacc[NMAX];
 #pragma unroll
-        for (int e = 0; e < NMAX; ++e) acc[e] = 0.f;
-        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
-        for (int c = lane; c < chunks; c += 32) {
-            uint4 xv = __ldg(xr + c);
-            float xf[8];
-            unpack_bf16x2(xv.x, xf[0], xf[1]);
-            unpack_bf16x2(xv.y, xf[2], xf[3]);
-            unpack_bf16x2(xv.z, xf[4], xf[5]);
-            unpack_bf16x2(xv.w, xf[6], xf[7]);
+    for (int e = 0; e < NMAX; ++e) {
+        bias[e] = (sel_bias != nullptr && e < N) ? sel_bias[e] : 0.f;
+        pacc[e] = 0.f;
+    }
+    const uint4 *wg = reinterpret_cast<const uint4 *>(Wg);
+
+    for (int t0 = blockIdx.x * kTokensPerBlock; t0 < T; t0 += gridDim.x * kTokensPerBlock) {
+        float acc[kTokensPerBlock][NMAX];
+#pragma unroll
+        for (int i = 0; i < kTokensPerBlock; ++i)
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) acc[i][e] = 0.f;
+#pragma unroll 2
+        for (int c = warp * 32 + lane; c < chunks; c += kRouterWarps * 32) {
+            uint4 xv[kTokensPerBlock];
+#pragma unroll
+            for (int i = 0; i < kTokensPerBlock; ++i)
+                xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            uint4 wv[NMAX];
+#pragma unroll
+            for (int e = 0; e < NMAX; ++e) wv[e] = (e < N) ? __ldg(wg + (size_t)e * chunks + c) : make_uint4(0u, 0u, 0u, 0u);
+            float xf[kTokensPerBlock][8];
+#pragma unroll
+            for (int i = 0; i < kTokensPerBlock; ++i) {
+                unpack_bf16x2(xv[i].x, xf[i][0], xf[i][1]);
+                unpack_bf16x2(xv[i].y, xf[i][2], xf[i][3]);
+                unpack_bf16x2(xv[i].z, xf[i][4], xf[i][5]);
+                unpack_bf16x2(xv[i].w, xf[i][6], xf[i][7]);
+            }
 #pragma unroll
             for (int e = 0; e < NMAX; ++e) {
-                if (e < N) {
-                    uint4 wv = wg_s[e * chunks + c];
-                    float wf[8];
-                    unpack_bf16x2(wv.x, wf[0], wf[1]);
-                    unpack_bf16x2(wv.y, wf[2], wf[3]);
-                    unpack_bf16x2(wv.z, wf[4], wf[5]);
-                    unpack_bf16x2(wv.w, wf[6], wf[7]);
+                float wf[8];
+                unpack_bf16x2(wv[e].x, wf[0], wf[1]);
+                unpack_bf16x2(wv[e].y, wf[2], wf[3]);
+                unpack_bf16x2(wv[e].z, wf[4], wf[5]);
+                unpack_bf16x2(wv[e].w, wf[6], wf[7]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[e] = fmaf(xf[j], wf[j], acc[e]);
-                }
+                for (int i = 0; i < kTokensPerBlock; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][e] = fmaf(xf[i][j], wf[j], acc[i][e]);
             }
         }
 #pragma unroll
-        for (int e = 0; e < NMAX; ++e) {
+        for (int i = 0; i < kTokensPerBlock; ++i)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+            for (int e = 0; e < NMAX; ++e) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
+            }
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kTokensPerBlock; ++i)
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e) red[warp][i][e] = acc[i][e];
         }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < kTokensPerBlock; ++i) {
+                const int t = t0 + i;
+                if (t >= T) break;  // warp-uniform
+                float s[NMAX];
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e) {
+                    float a = red[0][i][e];
+#pragma unroll
+                    for (int w = 1; w < kRouterWarps; ++w) a += red[w][i][e];
+                    s[e] = a;
+                }
+                // softmax over all N unbiased logits (balance-loss statistic)
+                float m = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e)
+                    if (e < N) m = fmaxf(m, s[e]);
+                float ex[NMAX];
+                float z = 0.f;
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e) {
+                    ex[e] = (e < N) ? expf(s[e] - m) : 0.f;
+                    z += ex[e];
+                }
+                const float inv_z = 1.f / z;
+#pragma unroll
+                for (int e = 0; e < NMAX; ++e) pacc[e] += ex[e] * inv_z;
+                // TopK on u = s + b: larger u first, equal u -> smaller id first
+                unsigned taken = 0u;
+                int sel_e[kMaxK];
+                float sel_s[kMaxK];
+#pragma unroll
+                for (int k = 0; k < kMaxK; ++k) {
+                    sel_e[k] = 0;
+                    sel_s[k] = 0.f;
+                    if (k < K) {
+                        float bu = -INFINITY, bs = 0.f;
+                        int be = -1;
+#pragma unroll
+                        for (int e = 0; e < NMAX; ++e) {
+                            const float u = s[e] + bias[e];
+                            if (e < N && !((taken >> e) & 1u) && (be < 0 || u > bu)) {
+                                bu = u;
+                                be = e;
+                                bs = s[e];
+                            }
+                        }
+                        sel_e[k] = be;
+                        sel_s[k] = bs;
+                        taken |= 1u << be;
+                    }
+                }
+                float mk = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kMaxK; ++k)
+                    if (k < K) mk = fmaxf(mk, sel_s[k]);
+                float num[kMaxK];
+                float den = 0.f;
+#pragma unroll
+                for (int k = 0; k < kMaxK; ++k) {
+                    num[k] = (k < K) ? expf(sel_s[k] - mk) : 0.f;
+                    den += num[k];
+                }
+#pragma unroll
+                for (int k = 0; k < kMaxK; ++k) {
+                    if (k < K && lane == k) {
+                        topk_idx[(size_t)t * K + k] = sel_e[k];
+                        topk_w[(size_t)t * K + k] = num[k] / den;
+                        atomicAdd(&dcount[sel_e[k]], 1);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 0 && lane < N) {
+        float a = 0.f;
 #pragma unroll
         for (int e = 0; e < NMAX; ++e)
-            if (e < N && lane == (e & 31)) logits[(size_t)t * N + e] = acc[e];
+            if (e == lane) a = pacc[e];
+        prob_partial[(size_t)blockIdx.x * N + lane] = a;
+        if (dcount[lane]) atomicAdd(&demand[lane], dcount[lane]);
     }
 }
 
@@ -156,7 +280,6 @@ gate_logits_tiled_kernel(const uint16_t *__restrict__ x, const uint16_t *__restr
 // reduced over the block's warps in a fixed order and written as one partial
 // row per block: no floating-point atomics, so results are run-to-run stable.
 constexpr int kTopkWarps = 8;
-constexpr int kMaxK = 8;
 
 template <int LPL>
 __global__ void __launch_bounds__(kTopkWarps * 32)
@@ -277,21 +400,39 @@ topk_softmax_kernel(const float *__restrict__ logits, const float *__restrict__ 
     }
 }
 
-// prob_sum[e] = sum of the per-block partial rows, in block order, in double.
-__global__ void prob_finalize_kernel(const float *__restrict__ prob_partial, int rows, int N,
-                                     float *__restrict__ prob_sum) {
-    int e = blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= N) return;
-    double a = 0.0;
-    for (int r = 0; r < rows; ++r) a += (double)prob_partial[(size_t)r * N + e];
-    prob_sum[e] = (float)a;
+// One block of 1024 threads. prob_sum[e] = sum of the per-block partial rows
+// in double, each expert reduced by one warp in a fixed lane/shuffle order.
+// With aux != nullptr it also writes the balance loss
+//   aux = alpha * N * sum_e (demand[e] / (T K)) * (prob_sum[e] / T)
+// (lmnt.cn/news/351908 sec. 5.1-5.2) from the same fp32 prob_sum values.
+__global__ void __launch_bounds__(1024)
+route_finalize_kernel(const float *__restrict__ prob_partial, int rows, int N, int T, int K, float alpha,
+                      const int32_t *__restrict__ demand, float *__restrict__ prob_sum, float *__restrict__ aux) {
+    const int lane = lane_id(), warp = warp_id();
+    const int warps = blockDim.x >> 5;
+    for (int e = warp; e < N; e += warps) {
+        double a = 0.0;
+        for (int r = lane; r < rows; r += 32) a += (double)prob_partial[(size_t)r * N + e];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) prob_sum[e] = (float)a;
+    }
+    if (aux == nullptr) return;
+    __syncthreads();
+    if (warp == 0) {
+        double s = 0.0;
+        for (int e = lane; e < N; e += 32)
+            s += ((double)demand[e] / ((double)T * (double)K)) * ((double)prob_sum[e] / (double)T);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) aux[0] = (float)((double)alpha * (double)N * s);
+    }
 }
 
-// Number of blocks of the TopK kernel: a function of T only, so the partial
-// sums (and hence prob_sum) are identical on every device.
+// Number of blocks of the TopK kernel (general N): a function of T only.
 inline int topk_grid(int T) {
     int g = (T + kTopkWarps - 1) / kTopkWarps;
-    return g < 1024 ? (g < 1 ? 1 : g) : 1024;
+    return g < 1 ? 1 : (g > kMaxPartialRows ? kMaxPartialRows : g);
 }
 
 }  // namespace route
