@@ -39,6 +39,20 @@ METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
 
 
+def gemm_traffic(kernel_source: str):
+    """DRAM bytes per step of the grouped GEMM from the committed ncu summary,
+    or None when the kernel source changed since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "grouped_gemm_mixtral_prefill.json")) as fh:
+            prof = json.load(fh)
+        with open(os.path.join(ROOT, kernel_source), "rb") as fh:
+            h = hashlib.sha256(fh.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    return prof["dram_bytes_per_step"] if prof.get("source_sha256") == h else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -339,7 +353,10 @@ def main():
         "config": workload_config(cfg, {"kept_rows": R, "parallelism": f"replicas{world}"}),
         "roofline": {"kernel": "grouped_gemm_kernel (both expert Linears, tcgen05)", "bound": "tensor",
                      "achieved": achieved_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": achieved_tflops / peak_t, "traffic": None,
+                     "frac": achieved_tflops / peak_t,
+                     "traffic": gemm_traffic("top_routing_expert_then_b300/csrc/grouped_gemm.cuh")
+                     if cfg.name == "mixtral_prefill" else None,
+                     "traffic_unit": "DRAM bytes per step (both launches), ncu",
                      "peak_kind": f"{P['source']} sustained bf16",
                      "frac_of_burst": achieved_tflops / P["bf16_tflops"],
                      "flops_per_step": ffn_flops, "ms_per_step": gemm_ms},
