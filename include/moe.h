@@ -149,6 +149,27 @@ MOE_API moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const mo
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
                      float *prob_sum, void *workspace, size_t workspace_bytes, void *stream);
 
+/* moe_route without a caller workspace. The pages have no counterpart of
+ * this entry point; it exists for callers that cannot hand the library device
+ * scratch memory (a plugin whose host framework plans all device memory up
+ * front and has no slot for per-operator scratch, or a latency-critical loop
+ * that must not call cudaMalloc once it runs, since cudaMalloc can
+ * synchronise the device and can fail when memory is fragmented).
+ * Same arguments (minus the workspace), outputs and results as moe_route.
+ * Scratch: one fixed 8 MiB array inside libmoe.so's device memory, present
+ * on every GPU that loads the library until the process exits. The routing
+ * scratch is 4*T*N + 4096*N bytes (each part rounded up to 256); shapes that
+ * need more than 8 MiB return MOE_ERR_UNSUPPORTED. The function allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls share the one array: calls whose work
+ * overlaps on the GPU (different streams, or different host threads on one
+ * device) race on it and must be serialised by the caller. */
+MOE_API moe_status moe_route_noalloc(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *Wg,
+                                     const float *sel_bias, int32_t *topk_idx, float *topk_w,
+                                     int32_t *demand, float *prob_sum, void *stream);
+
 /* Dispatch (lmnt.cn/news/351908 sec. 3.1 regroup by expert, sec. 3.3 capacity):
  * assignment (t, k) with e = topk_idx[t, k] gets position p = number of
  * earlier tokens t' < t that also chose e; it is kept iff p < capacity and

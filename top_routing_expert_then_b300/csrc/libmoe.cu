@@ -457,6 +457,45 @@ bool weights_ok(const moe_shape *s, const moe_weights *w, bool need_gate) {
 
 }  // namespace
 
+// ==================================================================== routing without a workspace
+// Some callers cannot pass us device scratch memory: a plugin inside a host
+// framework whose memory planner has no slot for per-operator scratch, or a
+// latency-critical loop that must not call cudaMalloc after start-up
+// (cudaMalloc can synchronise the device and fail under fragmentation).
+// moe_route_noalloc serves them from one fixed array in the library's own
+// device memory. The array is a file-scope __device__ object, so every GPU
+// that loads this library holds it until the process exits.
+constexpr size_t kRouteScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char moe_route_scratch[kRouteScratchBytes];
+
+namespace {
+struct ScratchAddress {
+    std::once_flag once;
+    void *ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+ScratchAddress g_route_scratch_addr[kMaxDevices];
+
+// Device address of moe_route_scratch on the current device. In host code the
+// symbol's name is only a host-side stand-in; the address must come from
+// cudaGetSymbolAddress, once per device, with that device current.
+moe_status route_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    ScratchAddress &a = g_route_scratch_addr[dev];
+    std::call_once(a.once, [&a]() {
+        a.err = cudaGetSymbolAddress(&a.ptr, moe_route_scratch);
+        if (a.err != cudaSuccess) cudaGetLastError();
+    });
+    if (a.err != cudaSuccess || a.ptr == nullptr) return MOE_ERR_CUDA;
+    *out = a.ptr;
+    return MOE_OK;
+}
+}  // namespace
+
 // ==================================================================== C ABI
 
 extern "C" {
@@ -494,6 +533,24 @@ moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *
     DeviceState *dev;
     if ((r = device_state(&dev)) != MOE_OK) return r;
     Carve c(workspace);
+    RouteWs w = carve_route(c, shape);
+    return run_route(shape, dev, x, Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, nullptr, w,
+                     as_stream(stream));
+}
+
+moe_status moe_route_noalloc(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *Wg, const float *sel_bias,
+                             int32_t *topk_idx, float *topk_w, int32_t *demand, float *prob_sum, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x || !Wg || !topk_idx || !topk_w || !demand || !prob_sum) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes(shape, MOE_WS_ROUTE) > kRouteScratchBytes) return MOE_ERR_UNSUPPORTED;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    void *scratch = nullptr;
+    if ((r = route_scratch(&scratch)) != MOE_OK) return r;
+    // every scratch word the kernels read is written earlier in the same call
+    Carve c(scratch);
     RouteWs w = carve_route(c, shape);
     return run_route(shape, dev, x, Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, nullptr, w,
                      as_stream(stream));

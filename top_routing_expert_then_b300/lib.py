@@ -78,6 +78,7 @@ def load():
         "moe_workspace_bytes": ([S, i32], sz),
         "moe_status_string": ([i32], ctypes.c_char_p),
         "moe_route": ([S, P, P, P, P, P, P, P, P, sz, P], i32),
+        "moe_route_noalloc": ([S, P, P, P, P, P, P, P, P], i32),
         "moe_dispatch": ([S, P, P, P, P, P, P, P, P, sz, P], i32),
         "moe_expert_ffn": ([S, P, P, ctypes.POINTER(MoeWeights), P, P, P, P, sz, P], i32),
         "moe_combine": ([S, P, P, P, P, P, P], i32),
@@ -174,6 +175,23 @@ def route(shape: MoeShape, x, Wg, sel_bias=None, ws=None, stream=None):
         ctypes.byref(shape), _ptr(x, torch.bfloat16, "x", T * shape.d_model),
         _ptr(Wg, torch.bfloat16, "Wg", N * shape.d_model), _ptr(sel_bias, torch.float32, "sel_bias", N),
         idx.data_ptr(), w.data_ptr(), demand.data_ptr(), psum.data_ptr(), wp, wn, _stream(stream)))
+    return idx, w, demand, psum
+
+
+def route_noalloc(shape: MoeShape, x, Wg, sel_bias=None, stream=None):
+    """moe_route without a workspace: the library's own fixed scratch array
+    serves as scratch (for callers that cannot allocate device memory).
+    -> (topk_idx, topk_w, demand, prob_sum)"""
+    T, N, K = shape.T, shape.N, shape.K
+    dev = x.device
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    demand = torch.empty((N,), dtype=torch.int32, device=dev)
+    psum = torch.empty((N,), dtype=torch.float32, device=dev)
+    _check("moe_route_noalloc", load().moe_route_noalloc(
+        ctypes.byref(shape), _ptr(x, torch.bfloat16, "x", T * shape.d_model),
+        _ptr(Wg, torch.bfloat16, "Wg", N * shape.d_model), _ptr(sel_bias, torch.float32, "sel_bias", N),
+        idx.data_ptr(), w.data_ptr(), demand.data_ptr(), psum.data_ptr(), _stream(stream)))
     return idx, w, demand, psum
 
 
