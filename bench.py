@@ -256,8 +256,13 @@ def main():
     if lib.device_error() != 0:
         raise RuntimeError("device error during warm-up")
     R = int(ro.expert_offsets[-1].item())
+    hit = int((ro.kept > 0).sum().item())
     T, d, f = cfg.T, cfg.d_model, cfg.d_ff
     ffn_flops = 4.0 * R * d * f + (4.0 * T * d * f if cfg.has_shared else 0.0)
+    # algorithmic bytes of the two grouped GEMMs: weights of every expert that
+    # received rows (+ shared), x_perm in, H out and back in, y_perm out
+    rows_all = R + (T if cfg.has_shared else 0)
+    ffn_bytes = (hit + (1 if cfg.has_shared else 0)) * 2.0 * d * f * 2 + rows_all * (2 * d + 4 * f + 2 * d)
 
     # ---- timed region: K steps, per-stage marks on the launching stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
@@ -299,6 +304,10 @@ def main():
     gemm_ms = stage_ms[2] + stage_ms[3]
     achieved_tflops = ffn_flops / (gemm_ms * 1e-3) / 1e12
     peak_t = P["bf16_tflops_sustained"]
+    achieved_gbs = ffn_bytes / (gemm_ms * 1e-3) / 1e9
+    # the binding roof: tensor when the GEMMs' FLOP per byte exceeds the
+    # machine balance (sustained bf16 / HBM), else HBM
+    tensor_bound = ffn_flops / ffn_bytes > peak_t * 1e12 / (P["hbm_gbs"] * 1e9)
 
     # HBM-bound stages: algorithmic bytes per step
     K, N = cfg.K, cfg.N
@@ -351,13 +360,17 @@ def main():
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"kept_rows": R, "parallelism": f"replicas{world}"}),
-        "roofline": {"kernel": "grouped_gemm_kernel (both expert Linears, tcgen05)", "bound": "tensor",
-                     "achieved": achieved_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": achieved_tflops / peak_t,
+        "roofline": {"kernel": "grouped_gemm_kernel (both expert Linears, tcgen05)",
+                     "bound": "tensor" if tensor_bound else "hbm",
+                     "achieved": achieved_tflops if tensor_bound else achieved_gbs,
+                     "peak": peak_t if tensor_bound else P["hbm_gbs"],
+                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": achieved_tflops / peak_t if tensor_bound else achieved_gbs / P["hbm_gbs"],
+                     "tflops": achieved_tflops, "gbs": achieved_gbs, "bytes_per_step": ffn_bytes,
                      "traffic": gemm_traffic("top_routing_expert_then_b300/csrc/grouped_gemm.cuh")
                      if cfg.name == "mixtral_prefill" else None,
                      "traffic_unit": "DRAM bytes per step (both launches), ncu",
-                     "peak_kind": f"{P['source']} sustained bf16",
+                     "peak_kind": f"{P['source']} sustained bf16" if tensor_bound else f"{P['source']} HBM copy",
                      "frac_of_burst": achieved_tflops / P["bf16_tflops"],
                      "flops_per_step": ffn_flops, "ms_per_step": gemm_ms},
         "stages_us": {n: round(1e3 * m, 2) for n, m in zip(stage_names, stage_ms)},

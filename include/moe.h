@@ -157,9 +157,9 @@ MOE_API moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const mo
  * synchronise the device and can fail when memory is fragmented).
  * Same arguments (minus the workspace), outputs and results as moe_route.
  * Scratch: one fixed 8 MiB array inside libmoe.so's device memory, present
- * on every GPU that loads the library until the process exits. The routing
- * scratch is 4*T*N + 4096*N bytes (each part rounded up to 256); shapes that
- * need more than 8 MiB return MOE_ERR_UNSUPPORTED. The function allocates
+ * on every GPU that loads the library until the process exits. A shape may
+ * use it when moe_workspace_bytes(shape, MOE_WS_ROUTE) <= 8 MiB; larger
+ * shapes return MOE_ERR_UNSUPPORTED. The function allocates
  * nothing: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call

@@ -24,8 +24,12 @@
 //              accumulator buffers (2 x 256 columns) so the epilogue of one
 //              tile overlaps the main loop of the next
 //   warps 2-5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, bias,
-//              GELU, bf16, 16-byte stores; rows past the expert's block and
-//              columns past n_out are computed but not stored
+//              GELU, bf16; full 32-row blocks leave through a shared-memory
+//              buffer and a TMA store, an expert's last partial block row by
+//              row; rows past the expert's block and columns past n_out are
+//              computed but not stored. A second mode
+//              writes the raw fp32 accumulators of each K split (used for the
+//              gate logits).
 //
 // Every wait is bounded (globaltimer). On a timeout the block sets
 // MOE_DEVERR_TIMEOUT, stops issuing work, drains its own copies and MMAs in
@@ -51,7 +55,19 @@ constexpr int NUM_THREADS = 192;
 constexpr int ACC_COLS = BN;          // fp32 accumulator columns per buffer
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+// Epilogue staging: each of the 4 epilogue warps owns two 32 x 32 bf16
+// buffers (2 KB each) from which a TMA store writes full 32-row blocks.
+constexpr int EPI_BUF_BYTES = 32 * 32 * 2;
+constexpr int EPI_BYTES = 4 * 2 * EPI_BUF_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
+#ifndef MOE_L2_PREFETCH_KBLOCKS
+#define MOE_L2_PREFETCH_KBLOCKS 0
+#endif
+// The producer asks for the weight (B) tile of k-block kb + PF_DIST into L2
+// while loading k-block kb: weights stream from HBM exactly once, and the
+// ring of 4 stages (~1 us of MMA work) is shorter than an HBM round trip
+// under load, so without the prefetch every stage would wait on DRAM.
+constexpr int PF_DIST = MOE_L2_PREFETCH_KBLOCKS;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
 
@@ -71,8 +87,11 @@ struct Params {
     int num_groups;           // experts in B / bias
     int out_rows;             // rows of `out` (bounds check)
     const float *bias;        // [num_groups, n_out]
-    uint16_t *out;            // [out_rows, n_out] bf16
+    uint16_t *out;            // [out_rows, n_out] bf16 (bf16 mode)
     int gelu;                 // 1: GELU epilogue
+    float *out_f32;           // non-null: raw fp32 accumulators instead (no bias, no GELU),
+                              // split s written to out_f32 + s * out_rows * n_out
+    int k_splits;             // fp32 mode: the K range is cut into this many splits
     int raster;               // m-tiles per raster group (dense mode; the list mode stores groups)
 };
 
@@ -114,6 +133,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Ask the TMA unit to pull a tile into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -267,16 +294,59 @@ __device__ __forceinline__ float gelu_erf(float v) {
     return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+// Store one warp's 32 rows x 32 columns of bf16 results (lane = row; 16
+// packed words per lane). A block whose 32 rows are all valid goes through
+// the warp's shared-memory buffer and one TMA store (full 64-byte row
+// segments); a partial block (an expert's last rows) is written row by row.
+__device__ __forceinline__ void store_chunk_bf16(const CUtensorMap *tmC, uint8_t *ebuf, int &buf, int lane,
+                                                 const uint32_t (&packed)[16], int rows_valid, int row_block,
+                                                 int col, uint16_t *out_row) {
+    if (rows_valid == 32) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        uint8_t *b = ebuf + buf * EPI_BUF_BYTES;
+        uint4 *dst = reinterpret_cast<uint4 *>(b + lane * 64);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, smem_u32(b), col, row_block);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        buf ^= 1;
+    } else if (lane < rows_valid) {
+        uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    }
+}
+
+// All TMA stores this warp issued have finished writing global memory.
+__device__ __forceinline__ void store_drain(int lane) {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- kernel
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmC, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Shared *sh = reinterpret_cast<Shared *>(smem + STAGES * STAGE_BYTES);
+    Shared *sh = reinterpret_cast<Shared *>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -311,8 +381,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     const int num_m = num_m_tiles<BM>(p);
     const int num_n = (p.n_out + BN - 1) / BN;
-    const int total = num_m * num_n;
+    const int splits = p.k_splits > 0 ? p.k_splits : 1;
+    const int total = num_m * num_n * splits;
     const int kblocks = p.k_dim / BK;
+    const int kb_per_split = (kblocks + splits - 1) / splits;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -322,10 +394,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                Tile t = tile_of<BM>(p, w, num_m, num_n);
+                Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int brow = t.group * p.n_out + t.n0;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const int kb0 = (w % splits) * kb_per_split;
+                const int kb1 = min(kblocks, kb0 + kb_per_split);
+                if (PF_DIST > 0)
+                    for (int kb = kb0; kb < kb1 && kb < kb0 + PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (PF_DIST > 0 && kb + PF_DIST < kb1) tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
                     if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
@@ -357,13 +434,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                Tile t = tile_of<BM>(p, w, num_m, num_n);
+                Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 if (!wait_bounded(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const int kb0 = (w % splits) * kb_per_split;
+                const int kb1 = min(kblocks, kb0 + kb_per_split);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
@@ -374,7 +453,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
-                                 (kb | kk) != 0 ? 1u : 0u);
+                                 (kb != kb0 || kk != 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&sh->empty[stage]));
                     if (++stage == STAGES) {
@@ -397,9 +476,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ---------------------------------------------------- epilogue (warps 2-5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
+        uint8_t *ebuf = smem + STAGES * STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
+        int ebuf_idx = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            Tile t = tile_of<BM>(p, w, num_m, num_n);
+            Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
             if (!t.ok) {
                 if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
                 continue;
@@ -407,7 +488,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!wait_bounded(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
             tc_fence_after();
             const bool store = row < t.rows;
+            const int rows_valid = max(0, min(32, t.rows - q * 32));
             uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
+            float *out32_row = p.out_f32 == nullptr
+                                   ? nullptr
+                                   : p.out_f32 + ((size_t)(w % splits) * p.out_rows + (t.row0 + row)) * p.n_out;
             const float *bias = p.bias + (size_t)t.group * p.n_out;
             const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -415,6 +500,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (col >= p.n_out) break;  // warp-uniform
                 uint32_t r[32];
                 tmem_ld32(tbase + c0, r);
+                if (out32_row != nullptr) {
+                    // fp32 mode: n_out is a multiple of 4, columns past it are not stored
+                    const int ncols = min(32, p.n_out - col);
+                    if (store) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(out32_row + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (4 * j < ncols) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    }
+                    continue;
+                }
                 uint32_t packed[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
@@ -432,13 +528,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     packed[j / 2] = pack_bf16x2(v0, v1);
                     packed[j / 2 + 1] = pack_bf16x2(v2, v3);
                 }
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                            packed[4 * j + 3]);
-                }
+                store_chunk_bf16(&tmC, ebuf, ebuf_idx, lane, packed, rows_valid, t.row0 + q * 32, col, out_row);
             }
             tc_fence_before();
             __syncwarp();
@@ -448,6 +538,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 acc_phase ^= 1u;
             }
         }
+        store_drain(lane);
     }
 
     tc_fence_before();
@@ -480,7 +571,7 @@ constexpr int P_STAGES = MOE_PAIR_STAGES;
 constexpr int P_A_BYTES = 128 * BK * 2;
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
 constexpr uint32_t IDESC_PAIR = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                 ((uint32_t)(PAIR_BM >> 4) << 24);
 
@@ -563,7 +654,11 @@ __device__ __noinline__ bool wait_bounded_pair(PairShared *sh, uint32_t bar, uin
                                                bool raise, bool cluster_scope) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        // CTA-scope acquire for every barrier: cluster-scope waits measured
+        // ~10% slower (the accumulator-empty barrier is still arrived with
+        // release.cluster by the peer's epilogue)
+        (void)cluster_scope;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 255u) {
             if (raise && sh->abort_flag) return false;
             uint64_t now = globaltimer_ns();
@@ -582,11 +677,11 @@ __device__ __noinline__ bool wait_bounded_pair(PairShared *sh, uint32_t bar, uin
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const Params p) {
+                         const __grid_constant__ CUtensorMap tmC, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    PairShared *sh = reinterpret_cast<PairShared *>(smem + P_STAGES * P_STAGE_BYTES);
+    PairShared *sh = reinterpret_cast<PairShared *>(smem + P_STAGES * P_STAGE_BYTES + EPI_BYTES);
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -640,7 +735,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 if (!t.ok) continue;
                 const int arow = t.row0 + (int)rank * 128;
                 const int brow = t.group * p.n_out + t.n0 + (int)rank * (BN / 2);
+                if (PF_DIST > 0)
+                    for (int kb = 0; kb < kblocks && kb < PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
                 for (int kb = 0; kb < kblocks; ++kb) {
+                    if (PF_DIST > 0 && kb + PF_DIST < kblocks) tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
                     if (!wait_bounded_pair(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true,
                                            false)) {
                         stop = true;
@@ -680,7 +778,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_bounded_pair(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true, true)) {
+                    // CTA-scope acquire: the peer's TMA bytes are counted on this barrier by the
+                    // async proxy, which the MMA (also async proxy) then reads
+                    if (!wait_bounded_pair(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true, false)) {
                         stop = true;
                         break;
                     }
@@ -716,6 +816,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         // ---------------------------------------------------- epilogue (warps 2-5, both CTAs)
         const int q = warp & 3;
         const int row = (int)rank * 128 + q * 32 + lane;  // row within the 256-row tile
+        uint8_t *ebuf = smem + P_STAGES * P_STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
+        int ebuf_idx = 0;
         const uint32_t tempty_leader0 = map_to_rank(smem_u32(&sh->tempty[0]), 0);
         const uint32_t tempty_leader1 = map_to_rank(smem_u32(&sh->tempty[1]), 0);
         uint32_t acc = 0, acc_phase = 0;
@@ -727,7 +829,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             }
             if (!wait_bounded_pair(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true, false)) break;
             tc_fence_after();
-            const bool store = row < t.rows;
+            const int rows_valid = max(0, min(32, t.rows - ((int)rank * 128 + q * 32)));
             uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
             const float *bias = p.bias + (size_t)t.group * p.n_out;
             const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
@@ -753,13 +855,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     packed[j / 2] = pack_bf16x2(v0, v1);
                     packed[j / 2 + 1] = pack_bf16x2(v2, v3);
                 }
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out_row + col);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                            packed[4 * j + 3]);
-                }
+                store_chunk_bf16(&tmC, ebuf, ebuf_idx, lane, packed, rows_valid,
+                                 t.row0 + (int)rank * 128 + q * 32, col, out_row);
             }
             tc_fence_before();
             __syncwarp();
@@ -769,6 +866,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 acc_phase ^= 1u;
             }
         }
+        store_drain(lane);
     }
 
     tc_fence_before();

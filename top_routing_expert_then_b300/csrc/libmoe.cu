@@ -83,11 +83,31 @@ int max_mtiles(const moe_shape *s) {
 struct RouteWs {
     float *logits;
     float *partial;
+    unsigned int *done;
 };
+// The gate runs on the tensor cores (grouped GEMM, fp32 output) when N > 16
+// and N % 32 == 0; with few 128 x 256 tiles it splits K so that about one
+// wave of blocks (148 SMs) has work. The split count depends on the shape
+// only, so results are the same on every device.
+bool tensor_gate(const moe_shape *s) { return s->N > 16 && s->N % 32 == 0; }
+
+int gate_splits(const moe_shape *s) {
+    if (!tensor_gate(s)) return 1;
+    const int64_t tiles = (int64_t)((s->T + 127) / 128) * ((s->N + 255) / 256);
+    int64_t sp = 148 / (tiles > 0 ? tiles : 1);
+    if (sp > 4) sp = 4;
+    if (sp < 1) sp = 1;
+    const int kb = s->d_model / 64;
+    // no empty split: every split keeps at least one 64-wide k-block
+    const int per = (int)((kb + sp - 1) / sp);
+    return (kb + per - 1) / per;
+}
+
 RouteWs carve_route(Carve &c, const moe_shape *s) {
     RouteWs w;
-    w.logits = c.take<float>((size_t)s->T * s->N);
+    w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
     w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
+    w.done = c.take<unsigned int>(4);
     return w;
 }
 
@@ -193,6 +213,15 @@ moe_status device_state(DeviceState **out) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_pair_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::P_SMEM_BYTES);
+        const void *routers[] = {
+            (const void *)moe::route::router_smallN_kernel<8, 1>, (const void *)moe::route::router_smallN_kernel<8, 2>,
+            (const void *)moe::route::router_smallN_kernel<8, 4>, (const void *)moe::route::router_smallN_kernel<8, 8>,
+            (const void *)moe::route::router_smallN_kernel<16, 1>, (const void *)moe::route::router_smallN_kernel<16, 2>,
+            (const void *)moe::route::router_smallN_kernel<16, 4>, (const void *)moe::route::router_smallN_kernel<16, 8>};
+        for (const void *k : routers)
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)moe::route::kRouterSmemBudget + 1024);
         st.init_err = e;
     });
     if (st.init_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -223,49 +252,79 @@ bool get_encoder() {
     return g_encode != nullptr;
 }
 
-// Row-major bf16 [rows, cols] tensor, box = box_rows x 64 columns, 128-byte swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major bf16 [rows, cols] tensor. Operand maps: box = box_rows x 64
+// columns with the 128-byte swizzle the MMA descriptors expect. Output maps
+// (epilogue TMA stores): box = 32 x 32, no swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               uint32_t box_cols = moe::gg::BK, bool swizzle128 = true) {
     if (!get_encoder()) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)moe::gg::BK, box_rows};
+    cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------------ stage launchers (no validation)
 
+moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
+                       int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
+                       const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
+                       cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1);
+
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
                      float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
-    (void)dev;
+    const int splits = gate_splits(s);
     if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
     int rows;
     if (N <= kSmallGateMaxN) {
         // gate + TopK + softmax + statistics in one kernel
         rows = moe::route::small_router_grid(T);
         const int thr = moe::route::kRouterWarps * 32;
-        if (N <= 8)
-            moe::route::router_smallN_kernel<8><<<rows, thr, 0, st>>>(x, Wg, sel_bias, T, d, N, K, topk_idx,
-                                                                      topk_w, demand, w.partial);
-        else
-            moe::route::router_smallN_kernel<16><<<rows, thr, 0, st>>>(x, Wg, sel_bias, T, d, N, K, topk_idx,
-                                                                       topk_w, demand, w.partial);
+        const int stages = moe::route::small_router_stages(d);
+        const size_t smem = moe::route::small_router_smem(d);
+        const int cpw_needed = ((d / 8) + moe::route::kRouterWarps - 1) / moe::route::kRouterWarps;
+        const int jmax = cpw_needed <= 32 ? 1 : (cpw_needed <= 64 ? 2 : (cpw_needed <= 128 ? 4 : 8));
+#define MOE_ROUTER(NM, JM)                                                                                    \
+    moe::route::router_smallN_kernel<NM, JM><<<rows, thr, smem, st>>>(x, Wg, sel_bias, T, d, N, K, stages, \
+                                                                      topk_idx, topk_w, demand, w.partial)
+        if (N <= 8) {
+            if (jmax == 1) MOE_ROUTER(8, 1);
+            else if (jmax == 2) MOE_ROUTER(8, 2);
+            else if (jmax == 4) MOE_ROUTER(8, 4);
+            else MOE_ROUTER(8, 8);
+        } else {
+            if (jmax == 1) MOE_ROUTER(16, 1);
+            else if (jmax == 2) MOE_ROUTER(16, 2);
+            else if (jmax == 4) MOE_ROUTER(16, 4);
+            else MOE_ROUTER(16, 8);
+        }
+#undef MOE_ROUTER
         count_launch();
     } else {
-        dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
-        moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N, w.logits);
-        count_launch();
+        if (tensor_gate(s)) {
+            // logits = x Wg^T on the tensor cores, raw fp32 K-split partials
+            moe_status g = launch_gemm(dev, false, x, (uint64_t)T, Wg, (uint64_t)N, d, N, 1, nullptr, nullptr, T,
+                                       nullptr, nullptr, 0, T, false, st, w.logits, splits);
+            if (g != MOE_OK) return g;
+        } else {
+            dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
+            moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N,
+                                                                                            w.logits);
+            count_launch();
+        }
         rows = moe::route::topk_grid(T);
         const size_t smem = (size_t)moe::route::kTopkWarps * N * sizeof(float) + (size_t)N * sizeof(int);
         const int lpl = (N + 31) / 32;
         const int thr = moe::route::kTopkWarps * 32;
 #define MOE_TOPK(L)                                                                                     \
-    moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, sel_bias, T, N, K, topk_idx, \
+    moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, splits, sel_bias, T, N, K, topk_idx, \
                                                                 topk_w, demand, w.partial)
         if (lpl <= 1) MOE_TOPK(1);
         else if (lpl <= 2) MOE_TOPK(2);
@@ -276,8 +335,9 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 #undef MOE_TOPK
         count_launch();
     }
-    moe::route::route_finalize_kernel<<<1, 1024, 0, st>>>(w.partial, rows, N, T, K, s->aux_alpha, demand, prob_sum,
-                                                          aux);
+    if (aux != nullptr && cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(w.partial, rows, N, T, K, s->aux_alpha, demand,
+                                                                      prob_sum, aux, w.done);
     count_launch();
     return launch_status();
 }
@@ -339,11 +399,16 @@ bool use_pair(int64_t expected_rows_per_group) {
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st) {
-    CUtensorMap ta, tb;
+                       cudaStream_t st, float *out_f32, int k_splits) {
+    CUtensorMap ta, tb, tc;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
     if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
     if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
+    if (out != nullptr) {
+        if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
+    } else {
+        tc = ta;  // fp32 mode: the epilogue stores directly and never reads this map
+    }
     moe::gg::Params p;
     p.mtiles = mtiles;
     p.num_mtiles = num_mtiles;
@@ -356,22 +421,25 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     p.bias = bias;
     p.out = out;
     p.gelu = gelu ? 1 : 0;
+    p.out_f32 = out_f32;
+    p.k_splits = k_splits;
+    if (pair && (out_f32 != nullptr || k_splits != 1)) return MOE_ERR_UNSUPPORTED;
     const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
     p.raster = pair ? kRasterPair : kRasterSingle;
     const int m_upper = mtiles ? max_tiles : (dense_rows + tile_m - 1) / tile_m;
     const int n_tiles = (n_out + moe::gg::BN - 1) / moe::gg::BN;
-    const int64_t work = (int64_t)m_upper * n_tiles;
+    const int64_t work = (int64_t)m_upper * n_tiles * k_splits;
     if (pair) {
         int clusters = dev->num_sms / 2;
         if (work < clusters) clusters = (int)work;
         if (clusters < 1) clusters = 1;
-        moe::gg::grouped_gemm_pair_kernel<<<2 * clusters, moe::gg::NUM_THREADS, moe::gg::P_SMEM_BYTES, st>>>(ta, tb,
+        moe::gg::grouped_gemm_pair_kernel<<<2 * clusters, moe::gg::NUM_THREADS, moe::gg::P_SMEM_BYTES, st>>>(ta, tb, tc,
                                                                                                         p);
     } else {
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
-        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, p);
+        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p);
     }
     count_launch();
     return MOE_OK;

@@ -15,178 +15,274 @@ namespace route {
 constexpr int kGateThreads = 256;
 
 // ---------------------------------------------------------------------------
-// Small N (<= 16): the whole router in one kernel. A block of 4 warps takes 4
-// tokens at a time; warp w owns the 8-element column chunks c with
-// (c / 32) % 4 == w, lane j the chunks with c % 32 == j, and accumulates all N
-// logits of the 4 tokens over its chunks (W_g is read through L1: it is small
-// and shared by every block on the SM). The partial sums meet in shared memory
-// and warp 0 adds them in warp order, then runs TopK / softmax for the 4
-// tokens (every lane computes the same values; lane k writes rank k).
-constexpr int kRouterWarps = 4;
-constexpr int kTokensPerBlock = 4;
+// Small N (<= 16): the whole router in one kernel.
+//  * x streams through shared memory: thread 0 issues one bulk copy
+//    (cp.async.bulk, mbarrier completion) per token row, 4 tokens per stage,
+//    up to 4 stages in flight per block.
+//  * Warp w owns the 8-element column chunks [w*CPW, (w+1)*CPW); its slice of
+//    W_g (all N experts) is loaded into registers once per block.
+//  * Per stage every warp forms partial logits of the 4 tokens over its
+//    chunks; the 8 partials meet in shared memory. Warp tk (< 4) then adds
+//    them in warp order for token tk, lane e holding expert e, and runs the
+//    full softmax, K rounds of warp arg-max and the K-way softmax with
+//    shuffles; lane k writes rank k.
+constexpr int kRouterWarps = 8;
+constexpr int kTokensPerStage = 4;
 constexpr int kMaxK = 8;
 constexpr int kMaxPartialRows = 1024;
+constexpr int kRouterBlocks = 148;
+constexpr int kRouterMaxStages = 4;
+constexpr size_t kRouterSmemBudget = 192 * 1024;
 
-// Blocks of the small-N router: a function of T only, so the partial
-// probability sums (and hence prob_sum) are identical on every device.
+// Blocks of the small-N router: a function of T only (not of the device), so
+// the per-block partial probability sums are identical on every GPU.
 inline int small_router_grid(int T) {
-    int g = (T + kTokensPerBlock - 1) / kTokensPerBlock;
-    return g < 1 ? 1 : (g > kMaxPartialRows ? kMaxPartialRows : g);
+    int g = (T + kTokensPerStage - 1) / kTokensPerStage;
+    return g < 1 ? 1 : (g > kRouterBlocks ? kRouterBlocks : g);
+}
+inline int small_router_stages(int d) {
+    size_t per = (size_t)kTokensPerStage * d * 2;
+    int s = (int)(kRouterSmemBudget / per);
+    return s < 1 ? 1 : (s > kRouterMaxStages ? kRouterMaxStages : s);
+}
+inline size_t small_router_smem(int d) {
+    return (size_t)small_router_stages(d) * kTokensPerStage * d * 2 + 64;
 }
 
-template <int NMAX>
-__global__ void __launch_bounds__(kRouterWarps * 32)
+__device__ __forceinline__ uint32_t r_smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ bool r_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait (about 4 s): false after the limit, with the error bit set.
+__device__ __noinline__ bool r_wait(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (r_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > 4000000000ull) {
+                flag_error(MOE_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bulk copies of the stage's token rows (thread 0 only).
+__device__ __forceinline__ void router_issue(uint32_t bar, uint8_t *dst, const uint16_t *x, int t0, int T,
+                                             int d) {
+    const uint32_t row_bytes = (uint32_t)d * 2;
+    int n = T - t0;
+    n = n < kTokensPerStage ? n : kTokensPerStage;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(row_bytes * n)
+                 : "memory");
+    for (int i = 0; i < n; ++i) {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                r_smem_u32(dst + (size_t)i * row_bytes)),
+            "l"(reinterpret_cast<uint64_t>(x + (size_t)(t0 + i) * d)), "r"(row_bytes), "r"(bar)
+            : "memory");
+    }
+}
+
+template <int NMAX, int JMAX>
+__global__ void __launch_bounds__(kRouterWarps * 32, 1)
 router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ Wg,
-                     const float *__restrict__ sel_bias, int T, int d, int N, int K,
+                     const float *__restrict__ sel_bias, int T, int d, int N, int K, int stages,
                      int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                      int32_t *__restrict__ demand, float *__restrict__ prob_partial) {
-    __shared__ float red[kRouterWarps][kTokensPerBlock][NMAX];
+    extern __shared__ __align__(128) uint8_t xs[];  // [stages][4][d] bf16
+    __shared__ __align__(8) uint64_t full[kRouterMaxStages];
+    __shared__ float red[2][kRouterWarps][kTokensPerStage][NMAX];
     __shared__ int dcount[NMAX];
+    __shared__ float psum_w[kTokensPerStage][NMAX];
+    __shared__ int abort_flag;
     const int chunks = d >> 3;
     const int lane = lane_id();
     const int warp = warp_id();
-    if (threadIdx.x < NMAX) dcount[threadIdx.x] = 0;
-    float bias[NMAX];
-    float pacc[NMAX];
-#pragma unroll
-    for (int e = 0; e < NMAX; ++e) {
-        bias[e] = (sel_bias != nullptr && e < N) ? sel_bias[e] : 0.f;
-        pacc[e] = 0.f;
-    }
-    const uint4 *wg = reinterpret_cast<const uint4 *>(Wg);
+    constexpr int CPW = 32 * JMAX;  // chunks per warp
+    const size_t stage_bytes = (size_t)kTokensPerStage * d * 2;
 
-    for (int t0 = blockIdx.x * kTokensPerBlock; t0 < T; t0 += gridDim.x * kTokensPerBlock) {
-        float acc[kTokensPerBlock][NMAX];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRouterMaxStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(r_smem_u32(&full[s])), "r"(1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        abort_flag = 0;
+    }
+    if (threadIdx.x < NMAX) dcount[threadIdx.x] = 0;
+    __syncthreads();
+
+    const int ngroups = (T + kTokensPerStage - 1) / kTokensPerStage;
+    const int my_groups = blockIdx.x < ngroups ? (ngroups - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages && i < my_groups; ++i)
+            router_issue(r_smem_u32(&full[i]), xs + i * stage_bytes, x,
+                         (blockIdx.x + i * gridDim.x) * kTokensPerStage, T, d);
+    }
+
+    // this warp's W_g slice, all experts, in registers
+    uint4 wreg[NMAX][JMAX];
 #pragma unroll
-        for (int i = 0; i < kTokensPerBlock; ++i)
+    for (int e = 0; e < NMAX; ++e)
 #pragma unroll
-            for (int e = 0; e < NMAX; ++e) acc[i][e] = 0.f;
-#pragma unroll 2
-        for (int c = warp * 32 + lane; c < chunks; c += kRouterWarps * 32) {
-            uint4 xv[kTokensPerBlock];
+        for (int j = 0; j < JMAX; ++j) {
+            const int c = warp * CPW + lane + 32 * j;
+            wreg[e][j] = (e < N && c < chunks) ? __ldg(reinterpret_cast<const uint4 *>(Wg + (size_t)e * d) + c)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+    const float bias_lane = (sel_bias != nullptr && lane < N) ? sel_bias[lane] : 0.f;
+    float pacc_lane = 0.f;  // routing warps: sum over their tokens of softmax_N[lane]
+
+    for (int i = 0; i < my_groups; ++i) {
+        const int g = blockIdx.x + i * gridDim.x;
+        const int t0 = g * kTokensPerStage;
+        const int st = i % stages;
+        if (!r_wait(r_smem_u32(&full[st]), (uint32_t)((i / stages) & 1))) abort_flag = 1;
+        __syncthreads();
+        if (abort_flag) break;  // block-uniform
+        const uint16_t *xst = reinterpret_cast<const uint16_t *>(xs + st * stage_bytes);
+        float acc[kTokensPerStage][NMAX];
 #pragma unroll
-            for (int i = 0; i < kTokensPerBlock; ++i)
-                xv[i] = (t0 + i < T) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * d) + c)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-            uint4 wv[NMAX];
+        for (int tk = 0; tk < kTokensPerStage; ++tk)
 #pragma unroll
-            for (int e = 0; e < NMAX; ++e) wv[e] = (e < N) ? __ldg(wg + (size_t)e * chunks + c) : make_uint4(0u, 0u, 0u, 0u);
-            float xf[kTokensPerBlock][8];
+            for (int e = 0; e < NMAX; ++e) acc[tk][e] = 0.f;
 #pragma unroll
-            for (int i = 0; i < kTokensPerBlock; ++i) {
-                unpack_bf16x2(xv[i].x, xf[i][0], xf[i][1]);
-                unpack_bf16x2(xv[i].y, xf[i][2], xf[i][3]);
-                unpack_bf16x2(xv[i].z, xf[i][4], xf[i][5]);
-                unpack_bf16x2(xv[i].w, xf[i][6], xf[i][7]);
-            }
+        for (int j = 0; j < JMAX; ++j) {
+            const int c = warp * CPW + lane + 32 * j;
+            if (c < chunks) {
+                float xf[kTokensPerStage][8];
 #pragma unroll
-            for (int e = 0; e < NMAX; ++e) {
-                float wf[8];
-                unpack_bf16x2(wv[e].x, wf[0], wf[1]);
-                unpack_bf16x2(wv[e].y, wf[2], wf[3]);
-                unpack_bf16x2(wv[e].z, wf[4], wf[5]);
-                unpack_bf16x2(wv[e].w, wf[6], wf[7]);
+                for (int tk = 0; tk < kTokensPerStage; ++tk) {
+                    uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                    if (t0 + tk < T) xv = reinterpret_cast<const uint4 *>(xst + (size_t)tk * d)[c];
+                    unpack_bf16x2(xv.x, xf[tk][0], xf[tk][1]);
+                    unpack_bf16x2(xv.y, xf[tk][2], xf[tk][3]);
+                    unpack_bf16x2(xv.z, xf[tk][4], xf[tk][5]);
+                    unpack_bf16x2(xv.w, xf[tk][6], xf[tk][7]);
+                }
 #pragma unroll
-                for (int i = 0; i < kTokensPerBlock; ++i)
+                for (int e = 0; e < NMAX; ++e) {
+                    if (e < N) {
+                        float wf[8];
+                        unpack_bf16x2(wreg[e][j].x, wf[0], wf[1]);
+                        unpack_bf16x2(wreg[e][j].y, wf[2], wf[3]);
+                        unpack_bf16x2(wreg[e][j].z, wf[4], wf[5]);
+                        unpack_bf16x2(wreg[e][j].w, wf[6], wf[7]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][e] = fmaf(xf[i][j], wf[j], acc[i][e]);
+                        for (int tk = 0; tk < kTokensPerStage; ++tk)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc[tk][e] = fmaf(xf[tk][q], wf[q], acc[tk][e]);
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int i = 0; i < kTokensPerBlock; ++i)
+        for (int tk = 0; tk < kTokensPerStage; ++tk)
 #pragma unroll
-            for (int e = 0; e < NMAX; ++e) {
+            for (int e = 0; e < NMAX; ++e)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], o);
-            }
+                for (int o = 16; o > 0; o >>= 1) acc[tk][e] += __shfl_xor_sync(0xffffffffu, acc[tk][e], o);
         if (lane == 0) {
 #pragma unroll
-            for (int i = 0; i < kTokensPerBlock; ++i)
+            for (int tk = 0; tk < kTokensPerStage; ++tk)
 #pragma unroll
-                for (int e = 0; e < NMAX; ++e) red[warp][i][e] = acc[i][e];
+                for (int e = 0; e < NMAX; ++e) red[i & 1][warp][tk][e] = acc[tk][e];
         }
-        __syncthreads();
-        if (warp == 0) {
+        __syncthreads();  // stage consumed, partials visible
+        if (threadIdx.x == 0 && i + stages < my_groups) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            router_issue(r_smem_u32(&full[st]), xs + st * stage_bytes, x,
+                         (blockIdx.x + (i + stages) * gridDim.x) * kTokensPerStage, T, d);
+        }
+        if (warp < kTokensPerStage && t0 + warp < T) {
+            // warp tk routes token t0 + tk; lane e holds expert e (N <= 16 < 32)
+            const int t = t0 + warp;
+            const bool live = lane < N;
+            float sv = 0.f;
+            if (live) {
+                sv = red[i & 1][0][warp][lane];
 #pragma unroll
-            for (int i = 0; i < kTokensPerBlock; ++i) {
-                const int t = t0 + i;
-                if (t >= T) break;  // warp-uniform
-                float s[NMAX];
+                for (int w = 1; w < kRouterWarps; ++w) sv += red[i & 1][w][warp][lane];
+            }
+            // softmax over all N unbiased logits (balance-loss statistic)
+            float m = live ? sv : -INFINITY;
 #pragma unroll
-                for (int e = 0; e < NMAX; ++e) {
-                    float a = red[0][i][e];
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float ex = live ? expf(sv - m) : 0.f;
+            float z = ex;
 #pragma unroll
-                    for (int w = 1; w < kRouterWarps; ++w) a += red[w][i][e];
-                    s[e] = a;
-                }
-                // softmax over all N unbiased logits (balance-loss statistic)
-                float m = -INFINITY;
+            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+            pacc_lane += ex / z;
+            // TopK on u = s + b: K rounds of warp arg-max, larger u first,
+            // equal u -> smaller expert id first
+            const float u = sv + bias_lane;
+            bool taken = !live;
+            int sel_e = 0;
+            float sel_s = 0.f, mk = -INFINITY;
+            float my_s = 0.f;
+            int my_k = -1;
+            for (int k = 0; k < K; ++k) {
+                float bu = taken ? -INFINITY : u;
+                int be = taken ? 0x7fffffff : lane;
+                float bs = sv;
 #pragma unroll
-                for (int e = 0; e < NMAX; ++e)
-                    if (e < N) m = fmaxf(m, s[e]);
-                float ex[NMAX];
-                float z = 0.f;
-#pragma unroll
-                for (int e = 0; e < NMAX; ++e) {
-                    ex[e] = (e < N) ? expf(s[e] - m) : 0.f;
-                    z += ex[e];
-                }
-                const float inv_z = 1.f / z;
-#pragma unroll
-                for (int e = 0; e < NMAX; ++e) pacc[e] += ex[e] * inv_z;
-                // TopK on u = s + b: larger u first, equal u -> smaller id first
-                unsigned taken = 0u;
-                int sel_e[kMaxK];
-                float sel_s[kMaxK];
-#pragma unroll
-                for (int k = 0; k < kMaxK; ++k) {
-                    sel_e[k] = 0;
-                    sel_s[k] = 0.f;
-                    if (k < K) {
-                        float bu = -INFINITY, bs = 0.f;
-                        int be = -1;
-#pragma unroll
-                        for (int e = 0; e < NMAX; ++e) {
-                            const float u = s[e] + bias[e];
-                            if (e < N && !((taken >> e) & 1u) && (be < 0 || u > bu)) {
-                                bu = u;
-                                be = e;
-                                bs = s[e];
-                            }
-                        }
-                        sel_e[k] = be;
-                        sel_s[k] = bs;
-                        taken |= 1u << be;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ou = __shfl_xor_sync(0xffffffffu, bu, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+                    if (ou > bu || (ou == bu && oe < be)) {
+                        bu = ou;
+                        be = oe;
+                        bs = os;
                     }
                 }
-                float mk = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < kMaxK; ++k)
-                    if (k < K) mk = fmaxf(mk, sel_s[k]);
-                float num[kMaxK];
-                float den = 0.f;
-#pragma unroll
-                for (int k = 0; k < kMaxK; ++k) {
-                    num[k] = (k < K) ? expf(sel_s[k] - mk) : 0.f;
-                    den += num[k];
+                if (lane == be) taken = true;
+                if (lane == k) {
+                    my_k = k;
+                    my_s = bs;
+                    sel_e = be;
                 }
+                mk = fmaxf(mk, bs);
+                (void)sel_s;
+            }
+            // softmax over the K selected, unbiased logits; lane k owns rank k
+            const float num = (my_k >= 0) ? expf(my_s - mk) : 0.f;
+            float den = num;
 #pragma unroll
-                for (int k = 0; k < kMaxK; ++k) {
-                    if (k < K && lane == k) {
-                        topk_idx[(size_t)t * K + k] = sel_e[k];
-                        topk_w[(size_t)t * K + k] = num[k] / den;
-                        atomicAdd(&dcount[sel_e[k]], 1);
-                    }
-                }
+            for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            if (my_k >= 0) {
+                topk_idx[(size_t)t * K + my_k] = sel_e;
+                topk_w[(size_t)t * K + my_k] = num / den;
+                atomicAdd(&dcount[sel_e], 1);
             }
         }
-        __syncthreads();
     }
+    // every bulk copy this block issued has landed before the block exits
+    if (threadIdx.x == 0 && abort_flag) {
+        for (int i2 = 0; i2 < stages && i2 < my_groups; ++i2) r_wait(r_smem_u32(&full[i2]), 0u);
+    }
+    __syncthreads();
+    if (warp < kTokensPerStage && lane < N) psum_w[warp][lane] = pacc_lane;
+    __syncthreads();
     if (warp == 0 && lane < N) {
-        float a = 0.f;
+        float a = psum_w[0][lane];
 #pragma unroll
-        for (int e = 0; e < NMAX; ++e)
-            if (e == lane) a = pacc[e];
+        for (int w = 1; w < kTokensPerStage; ++w) a += psum_w[w][lane];
         prob_partial[(size_t)blockIdx.x * N + lane] = a;
         if (dcount[lane]) atomicAdd(&demand[lane], dcount[lane]);
     }
@@ -273,7 +369,8 @@ gate_logits_tiled_kernel(const uint16_t *__restrict__ x, const uint16_t *__restr
 }
 
 // ---------------------------------------------------------------------------
-// TopK then softmax, one warp per token. Lane l holds the logits of experts
+// TopK then softmax, one warp per token. `logits` holds `splits` partial-sum
+// planes [splits][T][N] (1 for the CUDA-core gate). Lane l holds the logits of experts
 // l, l+32, ... (LPL of them). K rounds of a warp arg-max on (u desc, id asc)
 // pick the experts; the softmax runs over their unbiased logits. The full-N
 // softmax probabilities are accumulated per lane (each lane owns its experts),
@@ -283,7 +380,7 @@ constexpr int kTopkWarps = 8;
 
 template <int LPL>
 __global__ void __launch_bounds__(kTopkWarps * 32)
-topk_softmax_kernel(const float *__restrict__ logits, const float *__restrict__ sel_bias, int T,
+topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *__restrict__ sel_bias, int T,
                     int N, int K, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
                     int32_t *__restrict__ demand, float *__restrict__ prob_partial) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -310,7 +407,14 @@ topk_softmax_kernel(const float *__restrict__ logits, const float *__restrict__ 
 #pragma unroll
         for (int i = 0; i < LPL; ++i) {
             int e = lane + 32 * i;
-            s[i] = (e < N) ? logits[(size_t)t * N + e] : -INFINITY;
+            if (e < N) {
+                // the gate GEMM may leave K-split partial sums: add them in split order
+                float a = logits[(size_t)t * N + e];
+                for (int sp = 1; sp < splits; ++sp) a += logits[((size_t)sp * T + t) * N + e];
+                s[i] = a;
+            } else {
+                s[i] = -INFINITY;
+            }
             m = fmaxf(m, s[i]);
         }
 #pragma unroll
@@ -400,39 +504,53 @@ topk_softmax_kernel(const float *__restrict__ logits, const float *__restrict__ 
     }
 }
 
-// One block of 1024 threads. prob_sum[e] = sum of the per-block partial rows
-// in double, each expert reduced by one warp in a fixed lane/shuffle order.
-// With aux != nullptr it also writes the balance loss
+// prob_sum[e] = sum of the per-block partial rows, in double, in a fixed
+// order. Block b owns experts [32 b, 32 b + 32): thread (x, y) adds rows
+// y, y + 32, ... of expert 32 b + x (coalesced across x), then the 32 row
+// lanes are added in y order. With aux != nullptr the last block to finish
+// (counted on *done, which the caller zeroes) writes the balance loss
 //   aux = alpha * N * sum_e (demand[e] / (T K)) * (prob_sum[e] / T)
-// (lmnt.cn/news/351908 sec. 5.1-5.2) from the same fp32 prob_sum values.
+// (lmnt.cn/news/351908 sec. 5.1-5.2) from the fp32 prob_sum values, summed
+// in a fixed order; which block is last does not change the result.
 __global__ void __launch_bounds__(1024)
 route_finalize_kernel(const float *__restrict__ prob_partial, int rows, int N, int T, int K, float alpha,
-                      const int32_t *__restrict__ demand, float *__restrict__ prob_sum, float *__restrict__ aux) {
-    const int lane = lane_id(), warp = warp_id();
-    const int warps = blockDim.x >> 5;
-    for (int e = warp; e < N; e += warps) {
-        double a = 0.0;
-        for (int r = lane; r < rows; r += 32) a += (double)prob_partial[(size_t)r * N + e];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0) prob_sum[e] = (float)a;
+                      const int32_t *__restrict__ demand, float *__restrict__ prob_sum, float *__restrict__ aux,
+                      unsigned int *__restrict__ done) {
+    __shared__ double part[32][33];
+    __shared__ bool last;
+    const int x = threadIdx.x & 31, y = threadIdx.x >> 5;
+    const int e = blockIdx.x * 32 + x;
+    double a = 0.0;
+    if (e < N) {
+#pragma unroll 4
+        for (int r = y; r < rows; r += 32) a += (double)prob_partial[(size_t)r * N + e];
+    }
+    part[y][x] = a;
+    __syncthreads();
+    if (y == 0 && e < N) {
+        double s = 0.0;
+        for (int j = 0; j < 32; ++j) s += part[j][x];
+        prob_sum[e] = (float)s;
     }
     if (aux == nullptr) return;
+    __threadfence();
     __syncthreads();
-    if (warp == 0) {
-        double s = 0.0;
-        for (int e = lane; e < N; e += 32)
-            s += ((double)demand[e] / ((double)T * (double)K)) * ((double)prob_sum[e] / (double)T);
+    if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last || y != 0) return;
+    __threadfence();
+    double s = 0.0;
+    for (int k = x; k < N; k += 32)
+        s += ((double)demand[k] / ((double)T * (double)K)) * ((double)__ldcg(prob_sum + k) / (double)T);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) aux[0] = (float)((double)alpha * (double)N * s);
-    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (x == 0) aux[0] = (float)((double)alpha * (double)N * s);
 }
 
 // Number of blocks of the TopK kernel (general N): a function of T only.
 inline int topk_grid(int T) {
     int g = (T + kTopkWarps - 1) / kTopkWarps;
-    return g < 1 ? 1 : (g > kMaxPartialRows ? kMaxPartialRows : g);
+    return g < 1 ? 1 : (g > 256 ? 256 : g);
 }
 
 }  // namespace route
