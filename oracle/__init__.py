@@ -91,6 +91,7 @@ class OracleResult:
     z: Optional[np.ndarray]       # [T, d] uint16 or None
     y: Optional[np.ndarray]       # [T, d] uint16; rows of unwanted tokens are 0
     aux: float
+    z_loss: float
 
 
 class Oracle:
@@ -115,6 +116,8 @@ class Oracle:
         lib.oracle_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
         lib.oracle_aux_loss.argtypes = [i32, i32, i32, f64, P, P]
         lib.oracle_aux_loss.restype = f64
+        lib.oracle_z_loss.argtypes = [i32, i32, P, f64]
+        lib.oracle_z_loss.restype = f64
         self.lib = lib
 
     # ---- scalar helpers
@@ -213,10 +216,15 @@ class Oracle:
         P = _np(P, np.float64)
         return float(self.lib.oracle_aux_loss(T, demand.shape[0], K, float(alpha), _p(demand), _p(P)))
 
+    def z_loss(self, s, beta: float) -> float:
+        s = _np(s, np.float64)
+        T, N = s.shape
+        return float(self.lib.oracle_z_loss(T, N, _p(s), float(beta)))
+
     # ---- the whole layer
     def forward(self, x, Wg, W1, b1, W2, b2, K: int, capacity_factor: float, aux_alpha: float,
                 sel_bias=None, Ws1=None, bs1=None, Ws2=None, bs2=None, want=None,
-                skip_ffn: bool = False) -> OracleResult:
+                skip_ffn: bool = False, z_beta: float = 1e-3) -> OracleResult:
         """Full layer forward. Routing, dispatch and the aux loss always cover
         every token; ``want`` (bool/uint8 [T], optional) limits the FFN and the
         combine to a sample of tokens (the others' outputs are left 0)."""
@@ -228,6 +236,7 @@ class Oracle:
         C = self.capacity(T, N, capacity_factor)
         kept, offsets, slot_of, row_token = self.dispatch(idx, N, C)
         aux = self.aux_loss(demand, P, T, K, aux_alpha)
+        zl = self.z_loss(s, z_beta)
         y_perm = z = y = None
         if not skip_ffn:
             want_u8 = None if want is None else np.ascontiguousarray(np.asarray(want).astype(np.uint8))
@@ -235,7 +244,7 @@ class Oracle:
             if Ws1 is not None:
                 z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
             y = self.combine(y_perm, slot_of, w, d, z, want_u8)
-        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux)
+        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl)
 
 
 _default: Optional[Oracle] = None
@@ -260,4 +269,4 @@ def forward_inputs(inp, want=None, skip_ffn: bool = False) -> OracleResult:
     c = inp.cfg
     return default().forward(inp.x, inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, c.K, c.capacity_factor,
                              c.aux_alpha, inp.sel_bias, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
-                             want=want, skip_ffn=skip_ffn)
+                             want=want, skip_ffn=skip_ffn, z_beta=getattr(c, "z_beta", 1e-3))

@@ -19,7 +19,8 @@
  *           sec. 3.1 (dispatch = regroup token order into per-expert blocks),
  *           sec. 3.2 (combine equation; same order as dispatch),
  *           sec. 3.3 (capacity equation; overflow dropped to the residual),
- *           sec. 5.1-5.2 (balance loss alpha*N*sum f_i P_i and its code).
+ *           sec. 5.1-5.2 (balance loss alpha*N*sum f_i P_i and its code),
+ *           sec. 5.3 (router z-loss beta * mean_t logsumexp_t^2).
  *  [Yunthe] "MoE混合专家模型实战：专家路由与稀疏激活的推理成本优化方案"
  *           (yunthe.com): output equation y = sum_{i in TopK} g_i(x) E_i(x),
  *           the MoELayer listing (expert = Linear -> GELU -> Linear), and the
@@ -365,6 +366,29 @@ void oracle_combine(int T, int d, int K, const uint16_t *y_perm, const int32_t *
             y[(size_t)t * d + c] = bf16_round(acc);
         }
     }
+}
+
+/* ---------------------------------------------------------------- router z-loss */
+
+/* [Infra] sec. 5.3 (z-loss equation and its code): L_z = beta * (1/T) *
+ * sum_t (log sum_i exp(s[t, i]))^2 over the unbiased logits. The log-sum-exp
+ * is evaluated as m + log(sum exp(s - m)) with m the row maximum. */
+double oracle_z_loss(int T, int N, const double *s, double beta)
+{
+    double acc = 0.0;
+    for (int t = 0; t < T; ++t) {
+        const double *st = s + (size_t)t * N;
+        double m = -INFINITY;
+        for (int e = 0; e < N; ++e)
+            if (st[e] > m)
+                m = st[e];
+        double z = 0.0;
+        for (int e = 0; e < N; ++e)
+            z += exp(st[e] - m);
+        double lse = m + log(z);
+        acc += lse * lse;
+    }
+    return beta * acc / (double)T;
 }
 
 /* ---------------------------------------------------------------- balance loss */

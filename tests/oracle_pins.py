@@ -385,9 +385,30 @@ def pin_aux(orc):
     assert abs(orc.aux_loss(demand, P, 10, 1, alpha) - alpha * 4) < 1e-12
 
 
+# ------------------------------------------------------------------ router z-loss
+
+def pin_z_loss(orc):
+    """beta * mean_t logsumexp(s_t)^2: scipy's logsumexp on random logits;
+    equal logits c give (c + log N)^2; one expert gives mean(s^2); large
+    logits stay finite (max-shifted evaluation)."""
+    rng = np.random.default_rng(13)
+    beta = 1e-3
+    s = rng.standard_normal((50, 7)) * 5
+    ref = beta * np.mean(scipy.special.logsumexp(s, axis=1) ** 2)
+    assert abs(orc.z_loss(s, beta) - ref) <= 1e-13 * abs(ref)
+    c = 2.5
+    assert abs(orc.z_loss(np.full((9, 16), c), 1.0) - (c + math.log(16)) ** 2) < 1e-12
+    one = rng.standard_normal((20, 1))
+    assert abs(orc.z_loss(one, 1.0) - float(np.mean(one[:, 0] ** 2))) < 1e-12
+    big = np.array([[800.0, 799.0, 0.0]])
+    v = orc.z_loss(big, 1.0)
+    assert math.isfinite(v) and abs(v - scipy.special.logsumexp(big[0]) ** 2) < 1e-9 * v
+    assert orc.z_loss(s, 0.0) == 0.0
+
+
 ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts,
-    pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux,
+    pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
 ]

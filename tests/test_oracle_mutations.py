@@ -31,6 +31,8 @@ MUTATIONS = [
     ("aux_f_over_T", [("((double)T * (double)K)", "((double)T)")]),
     ("round_ties_away", [("nearbyint(ldexp(a, 7 - E))", "round(ldexp(a, 7 - E))")]),
     ("prob_not_normalised", [("P[e] += ex[e] / zn;", "P[e] += ex[e];")]),
+    ("z_loss_not_squared", [("acc += lse * lse;", "acc += lse;")]),
+    ("z_loss_no_max_shift", [("double lse = m + log(z);", "double lse = log(z);")]),
     ("dispatch_rank_order_by_k", [("for (int t = 0; t < T; ++t) {\n        for (int k = 0; k < K; ++k) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;",
                                    "for (int k = 0; k < K; ++k) {\n        for (int t = 0; t < T; ++t) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;")]),
 ]
