@@ -14,6 +14,7 @@
  *   combine y[t] = z[t] + sum_k w[t,k] E_{idx[t,k]}(x[t]) in fixed k order
  *           (z = optional always-on shared expert, weight 1)
  *   aux     alpha * N * sum_i f_i P_i (Switch-style balance loss)
+ *   z-loss  beta * mean_t logsumexp(s_t)^2 (router logit magnitude penalty)
  * Sources: lmnt.cn/news/351908 (sec. 2.1 score equation, sec. 3.1-3.3
  * dispatch/combine/capacity, sec. 5.1-5.2 balance loss); "MoE混合专家模型实战：
  * 专家路由与稀疏激活的推理成本优化方案" (yunthe.com: output equation, expert
@@ -86,6 +87,7 @@ typedef struct {
     float capacity_factor;   /* <= 0: dropless, capacity = T */
     int32_t has_shared;      /* 1: one always-on shared expert of shape (d_model, d_ff) */
     float aux_alpha;         /* balance-loss coefficient alpha */
+    float z_beta;            /* router z-loss coefficient beta (lmnt.cn/news/351908 sec. 5.3) */
 } moe_shape;
 
 /* Layer weights, all DEVICE pointers. */
@@ -112,6 +114,8 @@ typedef struct {
     int32_t *expert_offsets; /* [N + 1] exclusive prefix sum of kept */
     int32_t *slot_of;        /* [T, K] row of (t, k) in the per-expert blocks, -1 = dropped */
     float *aux;              /* [1] balance loss */
+    float *z_loss;           /* [1] router z-loss beta * (1/T) * sum_t logsumexp(s_t)^2
+                                (lmnt.cn/news/351908 sec. 5.3), fp32 per token, fp64 sum */
 } moe_route_out;
 
 /* Workspace sizes. */

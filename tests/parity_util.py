@@ -89,6 +89,8 @@ def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages
     assert np.array_equal(ro.slot_of.cpu().numpy(), ref.slot_of), "slot_of"
     aux = float(ro.aux.cpu()[0])
     assert abs(aux - ref.aux) <= AUX_RTOL * abs(ref.aux), ("aux", aux, ref.aux)
+    zl = float(ro.z_loss.cpu()[0])
+    assert abs(zl - ref.z_loss) <= AUX_RTOL * abs(ref.z_loss), ("z_loss", zl, ref.z_loss)
 
     yb = bits_np(y)
     rows = slice(None) if want is None else want.astype(bool)

@@ -54,7 +54,7 @@ moe_status check_shape(const moe_shape *s) {
     if (s->T <= 0 || s->d_model <= 0 || s->d_ff <= 0 || s->N <= 0 || s->K <= 0)
         return MOE_ERR_INVALID_ARG;
     if (s->K > s->N) return MOE_ERR_INVALID_ARG;
-    if (std::isnan(s->capacity_factor) || std::isnan(s->aux_alpha)) return MOE_ERR_INVALID_ARG;
+    if (std::isnan(s->capacity_factor) || std::isnan(s->aux_alpha) || std::isnan(s->z_beta)) return MOE_ERR_INVALID_ARG;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_INVALID_ARG;
     if (s->d_model % 64 != 0 || s->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (s->K > moe::route::kMaxK || s->N > 1024) return MOE_ERR_UNSUPPORTED;
@@ -83,6 +83,7 @@ int max_mtiles(const moe_shape *s) {
 struct RouteWs {
     float *logits;
     float *partial;
+    float *lse_partial;
     unsigned int *done;
 };
 // The gate runs on the tensor cores (grouped GEMM, fp32 output) when N > 16
@@ -107,6 +108,7 @@ RouteWs carve_route(Carve &c, const moe_shape *s) {
     RouteWs w;
     w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
     w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
+    w.lse_partial = c.take<float>((size_t)moe::route::kMaxPartialRows);
     w.done = c.take<unsigned int>(4);
     return w;
 }
@@ -278,7 +280,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
-                     float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st) {
+                     float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
     const int splits = gate_splits(s);
     if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -293,7 +295,8 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         const int jmax = cpw_needed <= 32 ? 1 : (cpw_needed <= 64 ? 2 : (cpw_needed <= 128 ? 4 : 8));
 #define MOE_ROUTER(NM, JM)                                                                                    \
     moe::route::router_smallN_kernel<NM, JM><<<rows, thr, smem, st>>>(x, Wg, sel_bias, T, d, N, K, stages, \
-                                                                      topk_idx, topk_w, demand, w.partial)
+                                                                      topk_idx, topk_w, demand, w.partial, \
+                                                                      w.lse_partial)
         if (N <= 8) {
             if (jmax == 1) MOE_ROUTER(8, 1);
             else if (jmax == 2) MOE_ROUTER(8, 2);
@@ -325,7 +328,7 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         const int thr = moe::route::kTopkWarps * 32;
 #define MOE_TOPK(L)                                                                                     \
     moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, splits, sel_bias, T, N, K, topk_idx, \
-                                                                topk_w, demand, w.partial)
+                                                                topk_w, demand, w.partial, w.lse_partial)
         if (lpl <= 1) MOE_TOPK(1);
         else if (lpl <= 2) MOE_TOPK(2);
         else if (lpl <= 4) MOE_TOPK(4);
@@ -335,9 +338,11 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 #undef MOE_TOPK
         count_launch();
     }
-    if (aux != nullptr && cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess) return MOE_ERR_CUDA;
-    moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(w.partial, rows, N, T, K, s->aux_alpha, demand,
-                                                                      prob_sum, aux, w.done);
+    if ((aux != nullptr || z_loss != nullptr) && cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(w.partial, w.lse_partial, rows, N, T, K,
+                                                                      s->aux_alpha, s->z_beta, demand, prob_sum, aux,
+                                                                      z_loss, w.done);
     count_launch();
     return launch_status();
 }
@@ -702,6 +707,7 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     int32_t *offsets = o.expert_offsets ? o.expert_offsets : w.offsets;
     int32_t *slot_of = o.slot_of ? o.slot_of : w.slot_of;
     float *aux = o.aux ? o.aux : w.aux;
+    float *z_loss = o.z_loss ? o.z_loss : w.aux + 1;
 
     auto mark = [&](int i) -> bool {
         return events == nullptr || events[i] == nullptr ||
@@ -709,7 +715,7 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     };
     if (!mark(0)) return MOE_ERR_CUDA;
     if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
-                       st)) != MOE_OK)
+                       st, z_loss)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st)) != MOE_OK)

@@ -104,12 +104,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
 router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ Wg,
                      const float *__restrict__ sel_bias, int T, int d, int N, int K, int stages,
                      int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-                     int32_t *__restrict__ demand, float *__restrict__ prob_partial) {
+                     int32_t *__restrict__ demand, float *__restrict__ prob_partial,
+                     float *__restrict__ lse_partial) {
     extern __shared__ __align__(128) uint8_t xs[];  // [stages][4][d] bf16
     __shared__ __align__(8) uint64_t full[kRouterMaxStages];
     __shared__ float red[2][kRouterWarps][kTokensPerStage][NMAX];
     __shared__ int dcount[NMAX];
     __shared__ float psum_w[kTokensPerStage][NMAX];
+    __shared__ float lsq_w[kTokensPerStage];
     __shared__ int abort_flag;
     const int chunks = d >> 3;
     const int lane = lane_id();
@@ -147,6 +149,7 @@ router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
         }
     const float bias_lane = (sel_bias != nullptr && lane < N) ? sel_bias[lane] : 0.f;
     float pacc_lane = 0.f;  // routing warps: sum over their tokens of softmax_N[lane]
+    float lsq = 0.f;        // routing warps: sum over their tokens of logsumexp^2 (z-loss)
 
     for (int i = 0; i < my_groups; ++i) {
         const int g = blockIdx.x + i * gridDim.x;
@@ -228,6 +231,8 @@ router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             pacc_lane += ex / z;
+            const float lse = m + logf(z);
+            lsq += lse * lse;
             // TopK on u = s + b: K rounds of warp arg-max, larger u first,
             // equal u -> smaller expert id first
             const float u = sv + bias_lane;
@@ -278,6 +283,7 @@ router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
     }
     __syncthreads();
     if (warp < kTokensPerStage && lane < N) psum_w[warp][lane] = pacc_lane;
+    if (warp < kTokensPerStage && lane == 0) lsq_w[warp] = lsq;
     __syncthreads();
     if (warp == 0 && lane < N) {
         float a = psum_w[0][lane];
@@ -285,6 +291,12 @@ router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
         for (int w = 1; w < kTokensPerStage; ++w) a += psum_w[w][lane];
         prob_partial[(size_t)blockIdx.x * N + lane] = a;
         if (dcount[lane]) atomicAdd(&demand[lane], dcount[lane]);
+    }
+    if (threadIdx.x == 0) {
+        float a = lsq_w[0];
+#pragma unroll
+        for (int w = 1; w < kTokensPerStage; ++w) a += lsq_w[w];
+        lse_partial[blockIdx.x] = a;
     }
 }
 
@@ -382,8 +394,10 @@ template <int LPL>
 __global__ void __launch_bounds__(kTopkWarps * 32)
 topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *__restrict__ sel_bias, int T,
                     int N, int K, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
-                    int32_t *__restrict__ demand, float *__restrict__ prob_partial) {
+                    int32_t *__restrict__ demand, float *__restrict__ prob_partial,
+                    float *__restrict__ lse_partial) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ float lsq_w[kTopkWarps];
     float *psum = reinterpret_cast<float *>(smem_raw);                       // [warps][N]
     int *dcount = reinterpret_cast<int *>(psum + kTopkWarps * N);            // [N]
     for (int e = threadIdx.x; e < N; e += blockDim.x) dcount[e] = 0;
@@ -401,6 +415,7 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
         bias[i] = (sel_bias != nullptr && e < N) ? sel_bias[e] : 0.f;
     }
 
+    float lsq = 0.f;  // sum over this warp's tokens of logsumexp(s_t)^2 (z-loss)
     for (int t = blockIdx.x * kTopkWarps + warp; t < T; t += gridDim.x * kTopkWarps) {
         float s[LPL];
         float m = -INFINITY;
@@ -423,12 +438,14 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
         float z = 0.f;
 #pragma unroll
         for (int i = 0; i < LPL; ++i) {
-            ex[i] = (lane + 32 * i < N) ? __expf(s[i] - m) : 0.f;
+            ex[i] = (lane + 32 * i < N) ? expf(s[i] - m) : 0.f;
             z += ex[i];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         const float inv_z = 1.f / z;
+        const float lse = m + logf(z);
+        lsq += lse * lse;
 #pragma unroll
         for (int i = 0; i < LPL; ++i) pacc[i] += ex[i] * inv_z;
 
@@ -495,7 +512,13 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
         int e = lane + 32 * i;
         if (e < N) psum[warp * N + e] = pacc[i];
     }
+    if (lane == 0) lsq_w[warp] = lsq;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        float a = 0.f;
+        for (int w = 0; w < kTopkWarps; ++w) a += lsq_w[w];
+        lse_partial[blockIdx.x] = a;
+    }
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
         float a = 0.f;
         for (int w = 0; w < kTopkWarps; ++w) a += psum[w * N + e];
@@ -507,14 +530,17 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
 // prob_sum[e] = sum of the per-block partial rows, in double, in a fixed
 // order. Block b owns experts [32 b, 32 b + 32): thread (x, y) adds rows
 // y, y + 32, ... of expert 32 b + x (coalesced across x), then the 32 row
-// lanes are added in y order. With aux != nullptr the last block to finish
-// (counted on *done, which the caller zeroes) writes the balance loss
+// lanes are added in y order. The last block to finish (counted on *done,
+// which the caller zeroes) writes, when asked, the balance loss
 //   aux = alpha * N * sum_e (demand[e] / (T K)) * (prob_sum[e] / T)
-// (lmnt.cn/news/351908 sec. 5.1-5.2) from the fp32 prob_sum values, summed
-// in a fixed order; which block is last does not change the result.
+// (lmnt.cn/news/351908 sec. 5.1-5.2) and the router z-loss
+//   z_loss = beta * (1/T) * sum_t logsumexp(s_t)^2       (sec. 5.3)
+// from per-block partial sums, in a fixed order; which block is last does
+// not change the result.
 __global__ void __launch_bounds__(1024)
-route_finalize_kernel(const float *__restrict__ prob_partial, int rows, int N, int T, int K, float alpha,
-                      const int32_t *__restrict__ demand, float *__restrict__ prob_sum, float *__restrict__ aux,
+route_finalize_kernel(const float *__restrict__ prob_partial, const float *__restrict__ lse_partial, int rows,
+                      int N, int T, int K, float alpha, float beta, const int32_t *__restrict__ demand,
+                      float *__restrict__ prob_sum, float *__restrict__ aux, float *__restrict__ z_loss,
                       unsigned int *__restrict__ done) {
     __shared__ double part[32][33];
     __shared__ bool last;
@@ -532,19 +558,29 @@ route_finalize_kernel(const float *__restrict__ prob_partial, int rows, int N, i
         for (int j = 0; j < 32; ++j) s += part[j][x];
         prob_sum[e] = (float)s;
     }
-    if (aux == nullptr) return;
+    if (aux == nullptr && z_loss == nullptr) return;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!last || y != 0) return;
     __threadfence();
-    double s = 0.0;
-    for (int k = x; k < N; k += 32)
-        s += ((double)demand[k] / ((double)T * (double)K)) * ((double)__ldcg(prob_sum + k) / (double)T);
+    if (aux != nullptr) {
+        double s = 0.0;
+        for (int k = x; k < N; k += 32)
+            s += ((double)demand[k] / ((double)T * (double)K)) * ((double)__ldcg(prob_sum + k) / (double)T);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (x == 0) aux[0] = (float)((double)alpha * (double)N * s);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (x == 0) aux[0] = (float)((double)alpha * (double)N * s);
+    }
+    if (z_loss != nullptr) {
+        // router z-loss (lmnt.cn/news/351908 sec. 5.3): beta * mean_t logsumexp_t^2
+        double s = 0.0;
+        for (int r = x; r < rows; r += 32) s += (double)lse_partial[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (x == 0) z_loss[0] = (float)((double)beta * s / (double)T);
+    }
 }
 
 // Number of blocks of the TopK kernel (general N): a function of T only.

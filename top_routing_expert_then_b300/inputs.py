@@ -49,6 +49,7 @@ class MoEConfig:
     sel_bias: bool = False
     zipf: bool = False
     aux_alpha: float = 0.01
+    z_beta: float = 1e-3
     note: str = ""
 
     def with_(self, **kw) -> "MoEConfig":
