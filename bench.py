@@ -165,6 +165,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(dist, value: float, device) -> float:
+    """The slowest rank's time: every rank's number, reduced with MAX (the
+    only cross-rank traffic besides barriers; replicas exchange no data)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_rank: int, steps: int, elapsed_ms: float) -> float:
+    """Tokens per second summed over all ranks (weak scaling: each rank runs
+    its own batch of tokens_per_rank every step)."""
+    return world * tokens_per_rank * steps / (elapsed_ms * 1e-3)
+
+
 def workload_config(cfg, extra=None):
     c = {"workload": f"{cfg.name}: T={cfg.T} d_model={cfg.d_model} d_ff={cfg.d_ff} N={cfg.N} K={cfg.K} "
                      f"capacity_factor={'dropless' if cfg.capacity_factor <= 0 else cfg.capacity_factor}"
@@ -217,7 +234,7 @@ def main():
     ap.add_argument("--config", default="mixtral_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-sample", type=int, default=64, help="tokens in the CPU-oracle sample")
+    ap.add_argument("--cpu-sample", type=int, default=1024, help="tokens in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args()
@@ -291,11 +308,7 @@ def main():
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if pg:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(pg, start.elapsed_time(stop), dev)
     if lib.device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -315,7 +328,7 @@ def main():
     dispatch_bytes = T * K * 4 * 4 + T * d * 2 + R * d * 2
     combine_bytes = R * d * 2 + T * d * 2 + (T * d * 2 if cfg.has_shared else 0) + T * K * 8
 
-    value = world * T * args.steps / (elapsed_ms * 1e-3)
+    value = whole_job_rate(world, T, args.steps, elapsed_ms)
 
     # ---- end to end through the public API with host buffers
     x_host = inp.x.cpu().pin_memory()
@@ -334,12 +347,8 @@ def main():
         layer.forward_hostio(x_host, y_host, xd, yd, inp.sel_bias, route_out=ro)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T * args.e2e_steps / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    e2e_value = whole_job_rate(world, T, args.e2e_steps, e2e_ms)
 
     if rank != 0:
         if pg:
