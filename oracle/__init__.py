@@ -92,6 +92,7 @@ class OracleResult:
     y: Optional[np.ndarray]       # [T, d] uint16; rows of unwanted tokens are 0
     aux: float
     z_loss: float
+    aux_kl: float = 0.0
 
 
 class Oracle:
@@ -110,6 +111,9 @@ class Oracle:
         lib.oracle_gate_logits.argtypes = [i32, i32, i32, P, P, P]
         lib.oracle_route.argtypes = [i32, i32, i32, P, P, P, P, P, P]
         lib.oracle_dispatch.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
+        lib.oracle_dispatch_ordered.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P]
+        lib.oracle_aux_kl.argtypes = [i32, i32, i32, f64, P]
+        lib.oracle_aux_kl.restype = f64
         lib.oracle_expert_rows.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
@@ -151,15 +155,23 @@ class Oracle:
         self.lib.oracle_route(T, N, K, _p(s), _p(sb), _p(idx), _p(w), _p(demand), _p(P))
         return idx, w, demand, P
 
-    def dispatch(self, idx, N: int, C: int):
+    def dispatch(self, idx, N: int, C: int, rank_major: bool = False):
         idx = _np(idx, np.int32)
         T, K = idx.shape
         kept = np.empty((N,), dtype=np.int32)
         offsets = np.empty((N + 1,), dtype=np.int32)
         slot_of = np.empty((T, K), dtype=np.int32)
         row_token = np.empty((T * K,), dtype=np.int32)
-        self.lib.oracle_dispatch(T, N, K, C, _p(idx), _p(kept), _p(offsets), _p(slot_of), _p(row_token))
+        if rank_major:
+            self.lib.oracle_dispatch_ordered(T, N, K, C, 1, _p(idx), _p(kept), _p(offsets), _p(slot_of),
+                                             _p(row_token))
+        else:
+            self.lib.oracle_dispatch(T, N, K, C, _p(idx), _p(kept), _p(offsets), _p(slot_of), _p(row_token))
         return kept, offsets, slot_of, row_token
+
+    def aux_kl(self, demand, T: int, K: int, coef: float) -> float:
+        demand = _np(demand, np.int32)
+        return float(self.lib.oracle_aux_kl(T, demand.shape[0], K, float(coef), _p(demand)))
 
     def expert_rows(self, x, rows, W1e, b1e, W2e, b2e) -> np.ndarray:
         """One expert's FFN on x[rows[i]]."""
@@ -224,7 +236,8 @@ class Oracle:
     # ---- the whole layer
     def forward(self, x, Wg, W1, b1, W2, b2, K: int, capacity_factor: float, aux_alpha: float,
                 sel_bias=None, Ws1=None, bs1=None, Ws2=None, bs2=None, want=None,
-                skip_ffn: bool = False, z_beta: float = 1e-3) -> OracleResult:
+                skip_ffn: bool = False, z_beta: float = 1e-3, rank_major: bool = False,
+                kl_coef: float = 0.02) -> OracleResult:
         """Full layer forward. Routing, dispatch and the aux loss always cover
         every token; ``want`` (bool/uint8 [T], optional) limits the FFN and the
         combine to a sample of tokens (the others' outputs are left 0)."""
@@ -234,9 +247,10 @@ class Oracle:
         s = self.gate_logits(x, Wg)
         idx, w, demand, P = self.route(s, K, sel_bias)
         C = self.capacity(T, N, capacity_factor)
-        kept, offsets, slot_of, row_token = self.dispatch(idx, N, C)
+        kept, offsets, slot_of, row_token = self.dispatch(idx, N, C, rank_major)
         aux = self.aux_loss(demand, P, T, K, aux_alpha)
         zl = self.z_loss(s, z_beta)
+        akl = self.aux_kl(demand, T, K, kl_coef)
         y_perm = z = y = None
         if not skip_ffn:
             want_u8 = None if want is None else np.ascontiguousarray(np.asarray(want).astype(np.uint8))
@@ -244,7 +258,7 @@ class Oracle:
             if Ws1 is not None:
                 z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
             y = self.combine(y_perm, slot_of, w, d, z, want_u8)
-        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl)
+        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl, akl)
 
 
 _default: Optional[Oracle] = None
@@ -269,4 +283,5 @@ def forward_inputs(inp, want=None, skip_ffn: bool = False) -> OracleResult:
     c = inp.cfg
     return default().forward(inp.x, inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, c.K, c.capacity_factor,
                              c.aux_alpha, inp.sel_bias, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
-                             want=want, skip_ffn=skip_ffn, z_beta=getattr(c, "z_beta", 1e-3))
+                             want=want, skip_ffn=skip_ffn, z_beta=getattr(c, "z_beta", 1e-3),
+                             rank_major=getattr(c, "rank_major", False), kl_coef=getattr(c, "kl_coef", 0.02))

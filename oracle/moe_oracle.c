@@ -210,8 +210,21 @@ void oracle_route(int T, int N, int K, const double *s, const float *sel_bias,
  *   slot_of [T, K]   global row of assignment (t, k) in the regrouped buffer,
  *                    or -1 when it was dropped
  *   row_token [T*K]  token of each kept row (entries >= R are set to -1) */
+void oracle_dispatch_ordered(int T, int N, int K, int C, int rank_major, const int32_t *idx,
+                             int32_t *kept, int32_t *offsets, int32_t *slot_of, int32_t *row_token);
+
 void oracle_dispatch(int T, int N, int K, int C, const int32_t *idx,
                      int32_t *kept, int32_t *offsets, int32_t *slot_of, int32_t *row_token)
+{
+    oracle_dispatch_ordered(T, N, K, C, 0, idx, kept, offsets, slot_of, row_token);
+}
+
+/* Same dispatch with a choice of priority for the capacity cut: rank_major = 0
+ * scans tokens in order (t outer, k inner: the default reading); rank_major =
+ * 1 scans every token's first choice before any second choice (k outer, t
+ * inner), the loop order of the yunthe.com MoELayer listing's combine. */
+void oracle_dispatch_ordered(int T, int N, int K, int C, int rank_major, const int32_t *idx,
+                             int32_t *kept, int32_t *offsets, int32_t *slot_of, int32_t *row_token)
 {
     int32_t *seen = (int32_t *)calloc((size_t)N, sizeof(int32_t));
     for (int t = 0; t < T; ++t)
@@ -225,8 +238,10 @@ void oracle_dispatch(int T, int N, int K, int C, const int32_t *idx,
     }
     for (int r = 0; r < T * K; ++r)
         row_token[r] = -1;
-    for (int t = 0; t < T; ++t) {
-        for (int k = 0; k < K; ++k) {
+    const int outer = rank_major ? K : T, inner = rank_major ? T : K;
+    for (int a = 0; a < outer; ++a) {
+        for (int b = 0; b < inner; ++b) {
+            const int t = rank_major ? b : a, k = rank_major ? a : b;
             int e = idx[(size_t)t * K + k];
             int p = seen[e]++;
             if (p < C) {
@@ -366,6 +381,24 @@ void oracle_combine(int T, int d, int K, const uint16_t *y_perm, const int32_t *
             y[(size_t)t * d + c] = bf16_round(acc);
         }
     }
+}
+
+/* ---------------------------------------------------------------- KL balance loss */
+
+/* "MoE逐token路由与活跃参数率实战解析" sec. 3.1 and its MoELayer listing: the
+ * per-expert frequency f_e = demand_e / (T K) is compared with the uniform
+ * distribution, loss = coef * KL(U || f) = coef * sum_e (1/N) (log(1/N) -
+ * log f_e) (what F.kl_div(f.log(), uniform, reduction='sum') evaluates).
+ * An expert with no assignment makes the loss +infinity. */
+double oracle_aux_kl(int T, int N, int K, double coef, const int32_t *demand)
+{
+    double acc = 0.0;
+    const double u = 1.0 / (double)N;
+    for (int e = 0; e < N; ++e) {
+        double f = (double)demand[e] / ((double)T * (double)K);
+        acc += u * (log(u) - log(f));
+    }
+    return coef * acc;
 }
 
 /* ---------------------------------------------------------------- router z-loss */

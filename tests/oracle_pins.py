@@ -222,6 +222,58 @@ def _brute_dispatch(idx, N, C):
     return slot, np.array(rows, dtype=np.int64), kept
 
 
+def _brute_dispatch_rank_major(idx, N, C):
+    """Stable sort of all (expert, rank, token) triples, first C per expert."""
+    T, K = idx.shape
+    triples = sorted(((int(idx[t, k]), k, t) for t in range(T) for k in range(K)))
+    slot = -np.ones((T, K), np.int64)
+    rows, per = [], {}
+    for e, k, t in triples:
+        if per.get(e, 0) < C:
+            per[e] = per.get(e, 0) + 1
+            slot[t, k] = len(rows)
+            rows.append(t)
+    return slot, np.array(rows, dtype=np.int64), np.array([per.get(e, 0) for e in range(N)])
+
+
+def pin_dispatch_rank_major(orc):
+    """Rank-major capacity priority: every first choice is served before any
+    second choice; brute force over (expert, rank, token) triples, and with
+    room for everyone it keeps the same rows as token order."""
+    rng = np.random.default_rng(14)
+    for T, N, K, C in [(40, 5, 2, 6), (33, 8, 3, 4), (20, 4, 1, 3), (30, 6, 3, 30)]:
+        idx, _, demand, _ = orc.route(rng.standard_normal((T, N)), K)
+        kept, offsets, slot_of, row_token = orc.dispatch(idx, N, C, rank_major=True)
+        slot, rows, kept_ref = _brute_dispatch_rank_major(idx, N, C)
+        assert np.array_equal(slot_of, slot)
+        R = len(rows)
+        assert np.array_equal(row_token[:R], rows) and np.all(row_token[R:] == -1)
+        assert np.array_equal(kept, kept_ref) and np.array_equal(kept, np.minimum(demand, C))
+        tok = orc.dispatch(idx, N, C)
+        assert np.array_equal(tok[0], kept)           # kept counts never depend on the order
+        if C >= T:
+            assert np.array_equal(tok[2] >= 0, slot_of >= 0)
+    # a case where the orders disagree: token 0's second choice vs token 1's first
+    idx = np.array([[0, 1], [1, 0]], np.int32)
+    _, _, s_tok, _ = orc.dispatch(idx, 2, 1)
+    _, _, s_rank, _ = orc.dispatch(idx, 2, 1, rank_major=True)
+    assert s_tok.tolist() == [[0, 1], [-1, -1]]      # token 0 takes both seats
+    assert s_rank.tolist() == [[0, -1], [1, -1]]     # first choices take them
+
+
+def pin_aux_kl(orc):
+    """coef * KL(uniform || f): 0 for uniform demand; torch's kl_div on the
+    same frequencies (the listing's own call); +inf for an idle expert."""
+    assert abs(orc.aux_kl(np.array([5, 5, 5, 5], np.int32), 10, 2, 0.02)) < 1e-15
+    rng = np.random.default_rng(15)
+    demand = rng.integers(1, 50, 7).astype(np.int32)
+    T, K = int(demand.sum()), 1
+    f = torch.from_numpy(demand.astype(np.float64) / (T * K))
+    ref = 0.02 * float(F.kl_div(f.log(), torch.full((7,), 1 / 7, dtype=torch.float64), reduction="sum"))
+    assert abs(orc.aux_kl(demand, T, K, 0.02) - ref) < 1e-14
+    assert orc.aux_kl(np.array([4, 0], np.int32), 2, 2, 0.02) == math.inf
+
+
 def pin_dispatch_bruteforce(orc):
     rng = np.random.default_rng(5)
     for T, N, K, C in [(40, 5, 2, 6), (40, 5, 2, 40), (33, 8, 3, 4), (20, 4, 1, 3), (16, 6, 6, 9)]:
@@ -411,4 +463,5 @@ ALL_PINS = [
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
+    pin_dispatch_rank_major, pin_aux_kl,
 ]

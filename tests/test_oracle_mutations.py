@@ -28,13 +28,21 @@ MUTATIONS = [
     ("combine_weight_index", [("acc += (double)w[(size_t)t * K + k] *",
                                "acc += (double)w[(size_t)t * K + (K - 1 - k)] *")]),
     ("shared_not_added", [("double acc = z ? bf16_val(z[(size_t)t * d + c]) : 0.0;", "double acc = 0.0;")]),
-    ("aux_f_over_T", [("((double)T * (double)K)", "((double)T)")]),
+    ("aux_f_over_T", [("acc += ((double)demand[e] / ((double)T * (double)K)) * P[e];",
+                       "acc += ((double)demand[e] / ((double)T)) * P[e];")]),
     ("round_ties_away", [("nearbyint(ldexp(a, 7 - E))", "round(ldexp(a, 7 - E))")]),
     ("prob_not_normalised", [("P[e] += ex[e] / zn;", "P[e] += ex[e];")]),
     ("z_loss_not_squared", [("acc += lse * lse;", "acc += lse;")]),
     ("z_loss_no_max_shift", [("double lse = m + log(z);", "double lse = log(z);")]),
-    ("dispatch_rank_order_by_k", [("for (int t = 0; t < T; ++t) {\n        for (int k = 0; k < K; ++k) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;",
-                                   "for (int k = 0; k < K; ++k) {\n        for (int t = 0; t < T; ++t) {\n            int e = idx[(size_t)t * K + k];\n            int p = seen[e]++;")]),
+    ("rank_major_ignored", [("const int outer = rank_major ? K : T, inner = rank_major ? T : K;",
+                             "const int outer = T, inner = K; (void)rank_major;"),
+                            ("const int t = rank_major ? b : a, k = rank_major ? a : b;",
+                             "const int t = a, k = b;")]),
+    ("kl_direction_swapped", [("acc += u * (log(u) - log(f));", "acc += f * (log(f) - log(u));")]),
+    ("dispatch_priority_inverted", [("const int outer = rank_major ? K : T, inner = rank_major ? T : K;",
+                                     "const int outer = rank_major ? T : K, inner = rank_major ? K : T;"),
+                                    ("const int t = rank_major ? b : a, k = rank_major ? a : b;",
+                                     "const int t = rank_major ? a : b, k = rank_major ? b : a;")]),
 ]
 
 
