@@ -9,7 +9,9 @@
  *   weights softmax over only the K kept, unbiased logits
  *   dispatch token order -> one contiguous block per expert, at most
  *           capacity = ceil(T / N * capacity_factor) tokens per expert, the
- *           rest dropped (they pass through the residual outside the layer)
+ *           rest dropped (they pass through the residual outside the layer);
+ *           which ones survive: earlier tokens first, or (drop_policy)
+ *           earlier ranks first
  *   experts E_e(x) = Linear(d_model -> d_ff) -> GELU -> Linear(d_ff -> d_model)
  *   combine y[t] = z[t] + sum_k w[t,k] E_{idx[t,k]}(x[t]) in fixed k order
  *           (z = optional always-on shared expert, weight 1)
@@ -88,7 +90,14 @@ typedef struct {
     int32_t has_shared;      /* 1: one always-on shared expert of shape (d_model, d_ff) */
     float aux_alpha;         /* balance-loss coefficient alpha */
     float z_beta;            /* router z-loss coefficient beta (lmnt.cn/news/351908 sec. 5.3) */
+    int32_t drop_policy;     /* which assignments a full expert keeps: MOE_DROP_TOKEN_ORDER
+                                (earlier tokens first) or MOE_DROP_RANK_ORDER (every token's
+                                first choice before any second choice, ...) */
+    float kl_coef;           /* coefficient of the KL(uniform || f) balance loss variant */
 } moe_shape;
+
+#define MOE_DROP_TOKEN_ORDER 0
+#define MOE_DROP_RANK_ORDER 1
 
 /* Layer weights, all DEVICE pointers. */
 typedef struct {
@@ -116,6 +125,9 @@ typedef struct {
     float *aux;              /* [1] balance loss */
     float *z_loss;           /* [1] router z-loss beta * (1/T) * sum_t logsumexp(s_t)^2
                                 (lmnt.cn/news/351908 sec. 5.3), fp32 per token, fp64 sum */
+    float *aux_kl;           /* [1] kl_coef * sum_e (1/N) (log(1/N) - log f_e), f_e = demand_e/(T K)
+                                (KL-to-uniform balance loss of the CSDN MoELayer listing);
+                                +inf when an expert receives nothing */
 } moe_route_out;
 
 /* Workspace sizes. */

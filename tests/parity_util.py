@@ -91,6 +91,11 @@ def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages
     assert abs(aux - ref.aux) <= AUX_RTOL * abs(ref.aux), ("aux", aux, ref.aux)
     zl = float(ro.z_loss.cpu()[0])
     assert abs(zl - ref.z_loss) <= AUX_RTOL * abs(ref.z_loss), ("z_loss", zl, ref.z_loss)
+    kl = float(ro.aux_kl.cpu()[0])
+    if np.isfinite(ref.aux_kl):
+        assert abs(kl - ref.aux_kl) <= AUX_RTOL * abs(ref.aux_kl) + 1e-7, ("aux_kl", kl, ref.aux_kl)
+    else:
+        assert kl == ref.aux_kl, ("aux_kl", kl, ref.aux_kl)
 
     yb = bits_np(y)
     rows = slice(None) if want is None else want.astype(bool)
@@ -106,7 +111,7 @@ def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages
     assert np.array_equal(demand.cpu().numpy(), ref.demand)
 
     ref_idx = torch.from_numpy(ref.topk_idx).cuda()
-    kept, offsets, slot_of, row_token, x_perm = lib.dispatch(shape, ref_idx, inp.x)
+    kept, offsets, slot_of, row_token, x_perm = lib.dispatch(shape, ref_idx, inp.x)  # policy from shape
     torch.cuda.synchronize()
     assert np.array_equal(kept.cpu().numpy(), ref.kept)
     assert np.array_equal(offsets.cpu().numpy(), ref.offsets)

@@ -70,6 +70,11 @@ def test_invalid_arguments(L):
     s = lib.make_shape(256, 128, 256, 8, 2, 1.25)
     s.has_shared = 3
     assert _route(L, s) == lib.MOE_ERR_INVALID_ARG
+    s = lib.make_shape(256, 128, 256, 8, 2, 1.25)
+    s.drop_policy = 2                                                                      # unknown priority
+    assert _route(L, s) == lib.MOE_ERR_INVALID_ARG
+    s = lib.make_shape(256, 128, 256, 8, 2, 1.25, kl_coef=float("nan"))
+    assert _route(L, s) == lib.MOE_ERR_INVALID_ARG
     assert _route(L, ok, x=None) == lib.MOE_ERR_INVALID_ARG
     assert _route(L, ok, x=FAKE + 2) == lib.MOE_ERR_INVALID_ARG                            # misaligned
     assert _route(L, ok, ws=None) == lib.MOE_ERR_WORKSPACE

@@ -34,6 +34,9 @@ SMALL = [
     MoEConfig("tight_capacity", 500, 128, 256, 8, 2, 0.05),
     MoEConfig("multi_tile", 2048, 512, 1024, 8, 2, 0.0),
     MoEConfig("skewed_small", 1024, 256, 192, 64, 2, 1.0, zipf=True),
+    MoEConfig("rank_major_drops", 1000, 256, 512, 16, 4, 1.0, rank_major=True),
+    MoEConfig("rank_major_skewed", 2048, 256, 192, 64, 2, 1.0, zipf=True, rank_major=True),
+    MoEConfig("rank_major_ties", 300, 128, 128, 8, 3, 0.5, rank_major=True),
 ]
 
 

@@ -19,18 +19,35 @@ namespace dispatch {
 
 constexpr int kChunk = 128;  // tokens per block (4 warps x 32 lanes)
 
-inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+inline int num_chunks(int rows) { return (rows + kChunk - 1) / kChunk; }
 
-// hist[chunk][e] = assignments to e among the chunk's tokens.
+// Capacity priority. Token order (the default): the assignments of token t
+// come before those of every later token. Rank order: every token's k-th
+// choice comes before any token's (k+1)-th choice. Both are handled as one
+// scan over "virtual tokens" v that name one expert each at most once:
+//   token order  v = t, entries (t, 0..K-1)
+//   rank order   v = k * T + t, entry (t, k) alone
+struct Order {
+    int T, K, rank_major;
+    __device__ __forceinline__ int tv() const { return rank_major ? T * K : T; }
+    __device__ __forceinline__ int kv() const { return rank_major ? 1 : K; }
+    // flat index (t * K + k) of the j-th entry of virtual token v
+    __device__ __forceinline__ int entry(int v, int j) const {
+        return rank_major ? (v % T) * K + v / T : v * K + j;
+    }
+    __device__ __forceinline__ int token(int v) const { return rank_major ? v % T : v; }
+};
+
+// hist[chunk][e] = assignments to e among the chunk's virtual tokens.
 __global__ void __launch_bounds__(kChunk)
-count_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int32_t *__restrict__ hist) {
+count_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int32_t *__restrict__ hist) {
     extern __shared__ int cnt[];  // [N]
     for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    const int t = blockIdx.x * kChunk + threadIdx.x;
-    if (t < T) {
-        for (int k = 0; k < K; ++k) {
-            int e = topk_idx[(size_t)t * K + k];
+    const int v = blockIdx.x * kChunk + threadIdx.x;
+    if (v < o.tv()) {
+        for (int j = 0; j < o.kv(); ++j) {
+            int e = topk_idx[o.entry(v, j)];
             if (e >= 0 && e < N)
                 atomicAdd(&cnt[e], 1);
             else
@@ -76,25 +93,25 @@ scan_kernel(const int32_t *__restrict__ hist, int chunks, int N, int C, int32_t 
 
 // slot_of[t, k] = offsets[e] + p if p < C else -1; row_token[slot] = t.
 __global__ void __launch_bounds__(kChunk)
-assign_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int C,
-              const int32_t *__restrict__ base, const int32_t *__restrict__ offsets,
-              int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token) {
+assign_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int C, const int32_t *__restrict__ base,
+              const int32_t *__restrict__ offsets, int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token) {
     extern __shared__ unsigned bits[];  // [4][N]
     for (int i = threadIdx.x; i < 4 * N; i += blockDim.x) bits[i] = 0u;
     __syncthreads();
     const int w = warp_id(), lane = lane_id();
-    const int t = blockIdx.x * kChunk + threadIdx.x;
-    if (t < T) {
-        for (int k = 0; k < K; ++k) {
-            int e = topk_idx[(size_t)t * K + k];
+    const int v = blockIdx.x * kChunk + threadIdx.x;
+    if (v < o.tv()) {
+        for (int j = 0; j < o.kv(); ++j) {
+            int e = topk_idx[o.entry(v, j)];
             if (e >= 0 && e < N) atomicOr(&bits[w * N + e], 1u << lane);
         }
     }
     __syncthreads();
-    if (t >= T) return;
+    if (v >= o.tv()) return;
     const unsigned below = (1u << lane) - 1u;
-    for (int k = 0; k < K; ++k) {
-        int e = topk_idx[(size_t)t * K + k];
+    for (int j = 0; j < o.kv(); ++j) {
+        const int ent = o.entry(v, j);
+        int e = topk_idx[ent];
         int slot = -1;
         if (e >= 0 && e < N) {
             int p = base[(size_t)blockIdx.x * N + e];
@@ -102,10 +119,10 @@ assign_kernel(const int32_t *__restrict__ topk_idx, int T, int N, int K, int C,
             p += __popc(bits[w * N + e] & below);
             if (p < C) {
                 slot = offsets[e] + p;
-                row_token[slot] = t;
+                row_token[slot] = o.token(v);
             }
         }
-        slot_of[(size_t)t * K + k] = slot;
+        slot_of[ent] = slot;
     }
 }
 

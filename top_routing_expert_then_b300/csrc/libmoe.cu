@@ -56,6 +56,8 @@ moe_status check_shape(const moe_shape *s) {
     if (s->K > s->N) return MOE_ERR_INVALID_ARG;
     if (std::isnan(s->capacity_factor) || std::isnan(s->aux_alpha) || std::isnan(s->z_beta)) return MOE_ERR_INVALID_ARG;
     if (s->has_shared != 0 && s->has_shared != 1) return MOE_ERR_INVALID_ARG;
+    if (s->drop_policy != MOE_DROP_TOKEN_ORDER && s->drop_policy != MOE_DROP_RANK_ORDER) return MOE_ERR_INVALID_ARG;
+    if (std::isnan(s->kl_coef)) return MOE_ERR_INVALID_ARG;
     if (s->d_model % 64 != 0 || s->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (s->K > moe::route::kMaxK || s->N > 1024) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)s->T * s->K >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
@@ -119,7 +121,7 @@ struct DispatchWs {
 };
 DispatchWs carve_dispatch(Carve &c, const moe_shape *s) {
     DispatchWs w;
-    size_t n = (size_t)moe::dispatch::num_chunks(s->T) * s->N;
+    size_t n = (size_t)moe::dispatch::num_chunks(s->T * s->K) * s->N;  // enough for either priority
     w.hist = c.take<int32_t>(n);
     w.base = c.take<int32_t>(n);
     return w;
@@ -283,7 +285,8 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
-                     float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr) {
+                     float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr,
+                     float *aux_kl = nullptr) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
     const int splits = gate_splits(s);
     if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -341,11 +344,12 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 #undef MOE_TOPK
         count_launch();
     }
-    if ((aux != nullptr || z_loss != nullptr) && cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess)
+    if ((aux != nullptr || z_loss != nullptr || aux_kl != nullptr) &&
+        cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
     moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(w.partial, w.lse_partial, rows, N, T, K,
-                                                                      s->aux_alpha, s->z_beta, demand, prob_sum, aux,
-                                                                      z_loss, w.done);
+                                                                      s->aux_alpha, s->z_beta, s->kl_coef, demand,
+                                                                      prob_sum, aux, z_loss, aux_kl, w.done);
     count_launch();
     return launch_status();
 }
@@ -355,17 +359,17 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
                         const DispatchWs &w, cudaStream_t st) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model;
     const int C = capacity_of(s);
-    const int chunks = moe::dispatch::num_chunks(T);
+    const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
+    const int chunks = moe::dispatch::num_chunks(order.rank_major ? T * K : T);
     const int rows = T * K;
     if (cudaMemsetAsync(row_token, 0xFF, sizeof(int32_t) * (size_t)rows, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, T, N, K,
-                                                                                         w.hist);
+    moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, order, N, w.hist);
     count_launch();
     moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets);
     count_launch();
     moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
-        topk_idx, T, N, K, C, w.base, offsets, slot_of, row_token);
+        topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
     count_launch();
     {
         const int vec = d / 8;
@@ -721,6 +725,7 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     int32_t *slot_of = o.slot_of ? o.slot_of : w.slot_of;
     float *aux = o.aux ? o.aux : w.aux;
     float *z_loss = o.z_loss ? o.z_loss : w.aux + 1;
+    float *aux_kl = o.aux_kl ? o.aux_kl : w.aux + 2;
 
     auto mark = [&](int i) -> bool {
         return events == nullptr || events[i] == nullptr ||
@@ -728,7 +733,7 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     };
     if (!mark(0)) return MOE_ERR_CUDA;
     if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
-                       st, z_loss)) != MOE_OK)
+                       st, z_loss, aux_kl)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st)) != MOE_OK)

@@ -539,9 +539,9 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
 // not change the result.
 __global__ void __launch_bounds__(1024)
 route_finalize_kernel(const float *__restrict__ prob_partial, const float *__restrict__ lse_partial, int rows,
-                      int N, int T, int K, float alpha, float beta, const int32_t *__restrict__ demand,
-                      float *__restrict__ prob_sum, float *__restrict__ aux, float *__restrict__ z_loss,
-                      unsigned int *__restrict__ done) {
+                      int N, int T, int K, float alpha, float beta, float kl_coef,
+                      const int32_t *__restrict__ demand, float *__restrict__ prob_sum, float *__restrict__ aux,
+                      float *__restrict__ z_loss, float *__restrict__ aux_kl, unsigned int *__restrict__ done) {
     __shared__ double part[32][33];
     __shared__ bool last;
     const int x = threadIdx.x & 31, y = threadIdx.x >> 5;
@@ -558,7 +558,7 @@ route_finalize_kernel(const float *__restrict__ prob_partial, const float *__res
         for (int j = 0; j < 32; ++j) s += part[j][x];
         prob_sum[e] = (float)s;
     }
-    if (aux == nullptr && z_loss == nullptr) return;
+    if (aux == nullptr && z_loss == nullptr && aux_kl == nullptr) return;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
@@ -580,6 +580,18 @@ route_finalize_kernel(const float *__restrict__ prob_partial, const float *__res
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (x == 0) z_loss[0] = (float)((double)beta * s / (double)T);
+    }
+    if (aux_kl != nullptr) {
+        // KL(uniform || f) balance loss ("MoE逐token路由与活跃参数率实战解析" sec. 3.1
+        // listing): kl_coef * sum_e (1/N) (log(1/N) - log(demand_e / (T K)));
+        // an idle expert gives +inf
+        double s = 0.0;
+        const double u = 1.0 / (double)N;
+        for (int k = x; k < N; k += 32)
+            s += u * (log(u) - log((double)demand[k] / ((double)T * (double)K)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (x == 0) aux_kl[0] = (float)((double)kl_coef * s);
     }
 }
 

@@ -50,6 +50,8 @@ class MoEConfig:
     zipf: bool = False
     aux_alpha: float = 0.01
     z_beta: float = 1e-3
+    rank_major: bool = False   # capacity priority: earlier ranks first instead of earlier tokens
+    kl_coef: float = 0.02      # KL-to-uniform balance-loss variant
     note: str = ""
 
     def with_(self, **kw) -> "MoEConfig":

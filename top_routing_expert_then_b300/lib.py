@@ -38,7 +38,8 @@ class MoEError(RuntimeError):
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("K", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
-                ("has_shared", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("z_beta", ctypes.c_float)]
+                ("has_shared", ctypes.c_int32), ("aux_alpha", ctypes.c_float), ("z_beta", ctypes.c_float),
+                ("drop_policy", ctypes.c_int32), ("kl_coef", ctypes.c_float)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -47,7 +48,7 @@ class MoeWeights(ctypes.Structure):
 
 class MoeRouteOut(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "demand", "prob_sum", "kept",
-                                               "expert_offsets", "slot_of", "aux", "z_loss")]
+                                               "expert_offsets", "slot_of", "aux", "z_loss", "aux_kl")]
 
 
 _lib = None
@@ -127,17 +128,22 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
+MOE_DROP_TOKEN_ORDER, MOE_DROP_RANK_ORDER = 0, 1
+
+
 def make_shape(T, d_model, d_ff, N, K, capacity_factor=0.0, has_shared=False, aux_alpha=0.01,
-               z_beta=1e-3) -> MoeShape:
+               z_beta=1e-3, rank_major=False, kl_coef=0.02) -> MoeShape:
     return MoeShape(int(T), int(d_model), int(d_ff), int(N), int(K), float(capacity_factor),
-                    1 if has_shared else 0, float(aux_alpha), float(z_beta))
+                    1 if has_shared else 0, float(aux_alpha), float(z_beta),
+                    MOE_DROP_RANK_ORDER if rank_major else MOE_DROP_TOKEN_ORDER, float(kl_coef))
 
 
 def shape_of(cfg) -> MoeShape:
     """moe_shape of an object with T, d_model, d_ff, N, K, capacity_factor,
     has_shared, aux_alpha (e.g. an inputs.MoEConfig)."""
     return make_shape(cfg.T, cfg.d_model, cfg.d_ff, cfg.N, cfg.K, cfg.capacity_factor, cfg.has_shared,
-                      cfg.aux_alpha, getattr(cfg, "z_beta", 1e-3))
+                      cfg.aux_alpha, getattr(cfg, "z_beta", 1e-3), getattr(cfg, "rank_major", False),
+                      getattr(cfg, "kl_coef", 0.02))
 
 
 def capacity(shape: MoeShape) -> int:
@@ -291,6 +297,7 @@ class RouteOutputs:
     slot_of: torch.Tensor
     aux: torch.Tensor
     z_loss: torch.Tensor
+    aux_kl: torch.Tensor
 
 
 class MoELayer:
@@ -316,14 +323,15 @@ class MoELayer:
                             torch.empty((N,), dtype=i32, device=dev), torch.empty((N,), dtype=f32, device=dev),
                             torch.empty((N,), dtype=i32, device=dev), torch.empty((N + 1,), dtype=i32, device=dev),
                             torch.empty((T, K), dtype=i32, device=dev), torch.empty((1,), dtype=f32, device=dev),
-                            torch.empty((1,), dtype=f32, device=dev))
+                            torch.empty((1,), dtype=f32, device=dev), torch.empty((1,), dtype=f32, device=dev))
 
     @staticmethod
     def _out_struct(ro: Optional[RouteOutputs]):
         if ro is None:
             return None
         return ctypes.byref(MoeRouteOut(*(getattr(ro, n).data_ptr() for n in (
-            "topk_idx", "topk_w", "demand", "prob_sum", "kept", "expert_offsets", "slot_of", "aux", "z_loss"))))
+            "topk_idx", "topk_w", "demand", "prob_sum", "kept", "expert_offsets", "slot_of", "aux", "z_loss",
+            "aux_kl"))))
 
     def forward(self, x, sel_bias=None, y=None, route_out: Optional[RouteOutputs] = None, stream=None):
         s = self.shape
