@@ -37,6 +37,15 @@ SMALL = [
     MoEConfig("rank_major_drops", 1000, 256, 512, 16, 4, 1.0, rank_major=True),
     MoEConfig("rank_major_skewed", 2048, 256, 192, 64, 2, 1.0, zipf=True, rank_major=True),
     MoEConfig("rank_major_ties", 300, 128, 128, 8, 3, 0.5, rank_major=True),
+    # fused tensor-core router: N padded to 16 (37 -> 48, 200 -> 208), several
+    # lanes per warp (N = 128, 200), more tiles than one wave (T = 20000: one
+    # split, two blocks per SM)
+    MoEConfig("n37_pad", 700, 192, 128, 37, 3, 1.1),
+    MoEConfig("n128_k6_bias", 600, 256, 128, 128, 6, 0.0, sel_bias=True),
+    MoEConfig("n200_bias", 400, 320, 128, 200, 8, 1.0, sel_bias=True),
+    MoEConfig("multi_wave", 20000, 128, 128, 8, 2, 1.0),
+    # general path (N > 256): CUDA-core tiled gate when N % 32 != 0
+    MoEConfig("n300_gate_tiled", 257, 64, 64, 300, 3, 2.0),
 ]
 
 

@@ -20,11 +20,12 @@ from top_routing_expert_then_b300.inputs import MoEConfig, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-# one small-N (fused router) and one general-N (logits in the scratch) shape,
+# one shape on the fused tensor-core router (N <= 256) and one on the general
+# path (N > 256: logits, TopK and finalize kernels, logits in the scratch),
 # drawn with different seeds so consecutive calls see different contents
 CASES = [
     (MoEConfig("noalloc_small_n", 1000, 256, 256, 8, 2, 1.25), 11),
-    (MoEConfig("noalloc_general_n", 1000, 512, 256, 256, 8, 0.0, sel_bias=True), 12),
+    (MoEConfig("noalloc_general_n", 1000, 512, 256, 320, 8, 0.0, sel_bias=True), 12),
 ]
 
 
@@ -51,10 +52,10 @@ def test_noalloc_route_matches_workspace_route_twice_in_a_row():
 
 def test_noalloc_route_rejects_shapes_beyond_its_scratch():
     # routing workspace above 8 MiB: refused before anything is enqueued
-    big = lib.make_shape(16384, 64, 64, 256, 8, 0.0)
+    big = lib.make_shape(16384, 64, 64, 512, 8, 0.0)
     assert lib.workspace_bytes(big, lib.MOE_WS_ROUTE) > 8 << 20
     x = torch.zeros((16384, 64), dtype=torch.bfloat16, device="cuda")
-    wg = torch.zeros((256, 64), dtype=torch.bfloat16, device="cuda")
+    wg = torch.zeros((512, 64), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(lib.MoEError) as e:
         lib.route_noalloc(big, x, wg)
     assert e.value.status == lib.MOE_ERR_UNSUPPORTED

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -16,6 +17,7 @@
 #include "dispatch.cuh"
 #include "grouped_gemm.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 namespace {
 
@@ -83,15 +85,35 @@ int max_mtiles(const moe_shape *s) {
 // ------------------------------------------------------------------ workspace layouts
 
 struct RouteWs {
-    float *logits;
-    float *partial;
-    float *lse_partial;
-    unsigned int *done;
+    float *logits;                 // general path: gate logits (K-split planes)
+    float *partial;                // general path: per-block probability sums
+    float *lse_partial;            // per-block sums of logsumexp^2
+    unsigned long long *acc;       // fused path: fixed-point probability sums  } zeroed
+    int32_t *dem;                  // fused path: assignments per expert         } by one
+    unsigned int *done;            // finished-block ticket                      } memset
 };
-// The gate runs on the tensor cores (grouped GEMM, fp32 output) when N > 16
-// and N % 32 == 0; with few 128 x 256 tiles it splits K so that about one
-// wave of blocks (148 SMs) has work. The split count depends on the shape
-// only, so results are the same on every device.
+
+// Routing for N <= 256 runs as one fused kernel (tensor-core gate, TopK,
+// softmax, statistics and losses). MOE_ROUTE_VARIANT=legacy (environment,
+// read once) selects the general path instead: CUDA-core router for N <= 16,
+// otherwise gate GEMM + TopK kernel + finalize kernel. N > 256 always takes
+// the general path.
+bool legacy_route() {
+    static const bool v = []() {
+        const char *e = std::getenv("MOE_ROUTE_VARIANT");
+        return e != nullptr && std::strcmp(e, "legacy") == 0;
+    }();
+    return v;
+}
+bool fused_route(const moe_shape *s) { return s->N <= moe::rtc::kMaxN && !legacy_route(); }
+int fused_route_grid(const moe_shape *s) {
+    return moe::rtc::num_tiles(s->T) * moe::rtc::splits(s->T, s->d_model);
+}
+
+// General path: the gate runs on the tensor cores (grouped GEMM, fp32 output)
+// when N > 16 and N % 32 == 0; with few 128 x 256 tiles it splits K so that
+// about one wave of blocks (148 SMs) has work. The split count depends on the
+// shape only, so results are the same on every device.
 bool tensor_gate(const moe_shape *s) { return s->N > 16 && s->N % 32 == 0; }
 
 int gate_splits(const moe_shape *s) {
@@ -107,10 +129,18 @@ int gate_splits(const moe_shape *s) {
 }
 
 RouteWs carve_route(Carve &c, const moe_shape *s) {
-    RouteWs w;
-    w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
-    w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
-    w.lse_partial = c.take<float>((size_t)moe::route::kMaxPartialRows);
+    RouteWs w{};
+    const bool fused = fused_route(s);
+    size_t rows = moe::route::kMaxPartialRows;
+    if (fused) {
+        rows = std::max(rows, (size_t)fused_route_grid(s));
+    } else {
+        w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
+        w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
+    }
+    w.lse_partial = c.take<float>(rows);
+    w.acc = c.take<unsigned long long>(s->N);
+    w.dem = c.take<int32_t>(s->N);
     w.done = c.take<unsigned int>(4);
     return w;
 }
@@ -200,6 +230,23 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
+// The fused router instantiated per (lanes' experts, cluster size).
+template <int L>
+const void *fused_route_kernel_s(int S) {
+    switch (S) {
+        case 1: return (const void *)moe::rtc::route_tc_kernel<L, 1>;
+        case 2: return (const void *)moe::rtc::route_tc_kernel<L, 2>;
+        case 4: return (const void *)moe::rtc::route_tc_kernel<L, 4>;
+        default: return (const void *)moe::rtc::route_tc_kernel<L, 8>;
+    }
+}
+const void *fused_route_kernel(int lpl, int S) {
+    if (lpl <= 1) return fused_route_kernel_s<1>(S);
+    if (lpl <= 2) return fused_route_kernel_s<2>(S);
+    if (lpl <= 4) return fused_route_kernel_s<4>(S);
+    return fused_route_kernel_s<8>(S);
+}
+
 constexpr int kSmallGateMaxN = 16;
 
 moe_status device_state(DeviceState **out) {
@@ -229,6 +276,11 @@ moe_status device_state(DeviceState **out) {
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)moe::route::kRouterSmemBudget + 1024);
+        for (int lpl = 1; lpl <= 8; lpl <<= 1)
+            for (int sp = 1; sp <= moe::rtc::kMaxSplits; sp <<= 1)
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(fused_route_kernel(lpl, sp), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)moe::rtc::kMaxSmem);
         st.init_err = e;
     });
     if (st.init_err != cudaSuccess) return MOE_ERR_CUDA;
@@ -288,6 +340,61 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
                      float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr,
                      float *aux_kl = nullptr) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
+    if (fused_route(s)) {
+        const size_t zero_bytes = (size_t)(reinterpret_cast<char *>(w.done + 4) - reinterpret_cast<char *>(w.acc));
+        if (cudaMemsetAsync(w.acc, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+        CUtensorMap tx, tw;
+        if (!make_tmap(&tx, x, (uint64_t)T, (uint64_t)d, moe::rtc::kTile)) return MOE_ERR_CUDA;
+        if (!make_tmap(&tw, Wg, (uint64_t)N, (uint64_t)d, (uint32_t)moe::rtc::npad(N))) return MOE_ERR_CUDA;
+        moe::rtc::Params p;
+        p.T = T;
+        p.d = d;
+        p.N = N;
+        p.Npad = moe::rtc::npad(N);
+        p.K = K;
+        const int S = moe::rtc::splits(T, d);
+        p.stages = moe::rtc::stages(T, d, N);
+        p.l_offset = (uint32_t)moe::rtc::l_offset(T, d, N, p.stages);
+        p.idesc = moe::rtc::idesc(N);
+        p.tmem_cols = moe::rtc::tmem_cols(N);
+        p.sel_bias = sel_bias;
+        p.topk_idx = topk_idx;
+        p.topk_w = topk_w;
+        p.prob_acc = w.acc;
+        p.dem_acc = w.dem;
+        p.done = w.done;
+        p.lse_partial = w.lse_partial;
+        p.demand = demand;
+        p.prob_sum = prob_sum;
+        p.aux = aux;
+        p.z_loss = z_loss;
+        p.aux_kl = aux_kl;
+        p.alpha = s->aux_alpha;
+        p.beta = s->z_beta;
+        p.kl_coef = s->kl_coef;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)fused_route_grid(s));
+        cfg.blockDim = dim3(moe::rtc::kThreads);
+        cfg.dynamicSmemBytes = moe::rtc::smem_bytes(T, d, N);
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)S;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const int lpl = (p.Npad + 31) / 32;
+        const void *fn = fused_route_kernel(lpl, S);
+        void *args[] = {&tx, &tw, &p};
+        cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+        count_launch();
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        return launch_status();
+    }
     const int splits = gate_splits(s);
     if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
     int rows;

@@ -273,7 +273,10 @@ router_smallN_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
             if (my_k >= 0) {
                 topk_idx[(size_t)t * K + my_k] = sel_e;
                 topk_w[(size_t)t * K + my_k] = num / den;
-                atomicAdd(&dcount[sel_e], 1);
+                if ((unsigned)sel_e < (unsigned)N)
+                    atomicAdd(&dcount[sel_e], 1);
+                else
+                    flag_error(MOE_DEVERR_EXPERT_ID);  // no orderable logit (NaN input)
             }
         }
     }
@@ -503,7 +506,10 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
             if (k < K && lane == k) {
                 topk_idx[(size_t)t * K + k] = sel_e[k];
                 topk_w[(size_t)t * K + k] = num[k] / den;
-                atomicAdd(&dcount[sel_e[k]], 1);
+                if ((unsigned)sel_e[k] < (unsigned)N)
+                    atomicAdd(&dcount[sel_e[k]], 1);
+                else
+                    flag_error(MOE_DEVERR_EXPERT_ID);  // no orderable logit (NaN input)
             }
         }
     }
@@ -524,6 +530,121 @@ topk_softmax_kernel(const float *__restrict__ logits, int splits, const float *_
         for (int w = 0; w < kTopkWarps; ++w) a += psum[w * N + e];
         prob_partial[(size_t)blockIdx.x * N + e] = a;
         if (dcount[e]) atomicAdd(&demand[e], dcount[e]);
+    }
+}
+
+// One balance-loss summand f_e P_e = (demand_e / (T K)) (prob_sum_e / T).
+__device__ __forceinline__ float aux_term(int de, float ps, float TKf, float Tf) {
+    return ((float)de / TKf) * (ps / Tf);
+}
+
+// One KL(u || f) summand in a form whose terms are all >= 0:
+//   f h(u / f),  h(r) = r log r - r + 1,
+// which adds (f - u) to u log(u / f); those extra pieces sum to zero over the
+// experts because sum_e f_e = sum_e u = 1 (every token makes K assignments).
+// r - 1 = (T K - N d_e) / (N d_e) is formed from exact integers; for
+// |r - 1| < 1/2, h(1 + delta) = delta^2 sum_{n >= 2} (-delta)^(n-2) / (n (n - 1))
+// (Taylor series of h at 1, 30 terms by Horner's rule: truncation below 1e-11
+// relative) avoids the cancellation of the closed form. An idle expert gives +inf.
+__device__ __forceinline__ float kl_summand(int de, long long TK, int N) {
+    if (de <= 0) return INFINITY;
+    const long long nd = (long long)N * de;
+    const float f = (float)de / (float)TK;
+    const float delta = (float)(TK - nd) / (float)nd;
+    float h;
+    if (fabsf(delta) < 0.5f) {
+        float acc = 0.f;
+#pragma unroll
+        for (int n = 31; n >= 2; --n) acc = fmaf(acc, -delta, 1.0f / (float)(n * (n - 1)));
+        h = delta * delta * acc;
+    } else {
+        const float r = (float)TK / (float)nd;
+        h = r * logf(r) - r + 1.f;
+    }
+    return f * h;
+}
+
+// Compensated fp32 sum (Neumaier): s + c carries the running total with the
+// rounding error of each addition kept in c. fp32 is used because fp64
+// arithmetic is slow on this GPU; with the compensation the error stays at a
+// few fp32 ulps of the total for the few thousand terms summed here.
+struct KSum {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const float t = s + x;
+        if (!isfinite(t)) {  // an infinite term (idle expert in the KL loss) or NaN: no compensation
+            s = t;
+            c = 0.f;
+            return;
+        }
+        c += fabsf(s) >= fabsf(x) ? (s - t) + x : (x - t) + s;
+        s = t;
+    }
+    __device__ __forceinline__ void add(const KSum &o) {
+        add(o.s);
+        add(o.c);
+    }
+    __device__ __forceinline__ float value() const { return s + c; }
+};
+
+__device__ __forceinline__ KSum shfl_xor_ksum(const KSum &v, int o) {
+    KSum r;
+    r.s = __shfl_xor_sync(0xffffffffu, v.s, o);
+    r.c = __shfl_xor_sync(0xffffffffu, v.c, o);
+    return r;
+}
+
+// Fixed-order block sums of three compensated sums per thread (any blockDim
+// <= 1024, a multiple of 32); the results are valid in thread 0.
+__device__ __forceinline__ void block_sum3(KSum &a, KSum &b, KSum &c, KSum *scratch /* 3 x 32 */) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a.add(shfl_xor_ksum(a, o));
+        b.add(shfl_xor_ksum(b, o));
+        c.add(shfl_xor_ksum(c, o));
+    }
+    if (lane_id() == 0) {
+        scratch[warp_id()] = a;
+        scratch[32 + warp_id()] = b;
+        scratch[64 + warp_id()] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a = b = c = KSum();
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            a.add(scratch[w]);
+            b.add(scratch[32 + w]);
+            c.add(scratch[64 + w]);
+        }
+    }
+}
+
+// The losses from per-expert totals already in global memory (prob_sum as
+// fp32 sums of probabilities, demand as counts) and `rows` per-block partial
+// sums of logsumexp^2. Called by every thread of one block.
+//   aux    = alpha N sum_e (demand_e / (T K)) (prob_sum_e / T)   (sec. 5.1-5.2)
+//   z_loss = beta (1/T) sum_t logsumexp(s_t)^2                     (sec. 5.3)
+//   aux_kl = kl_coef sum_e (1/N) log((1/N) / f_e)  (KL balance loss of the
+//            CSDN "MoE逐token路由与活跃参数率实战解析" MoELayer listing)
+__device__ void block_losses(int N, int T, int K, const int32_t *demand, const float *prob_sum,
+                             const float *lse_partial, int rows, float alpha, float beta, float kl_coef,
+                             float *aux, float *z_loss, float *aux_kl, KSum *scratch) {
+    const long long TK = (long long)T * K;
+    const float TKf = (float)TK, Tf = (float)T;
+    KSum a_aux, a_kl, a_z;
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        const int de = __ldcg(demand + e);
+        const float pe = __ldcg(prob_sum + e);
+        if (aux != nullptr) a_aux.add(aux_term(de, pe, TKf, Tf));
+        if (aux_kl != nullptr) a_kl.add(kl_summand(de, TK, N));
+    }
+    if (z_loss != nullptr)
+        for (int r = threadIdx.x; r < rows; r += blockDim.x) a_z.add(__ldcg(lse_partial + r));
+    block_sum3(a_aux, a_kl, a_z, scratch);
+    if (threadIdx.x == 0) {
+        if (aux != nullptr) aux[0] = alpha * (float)N * a_aux.value();
+        if (z_loss != nullptr) z_loss[0] = beta * (a_z.value() / (float)T);
+        if (aux_kl != nullptr) aux_kl[0] = kl_coef * a_kl.value();
     }
 }
 
@@ -563,36 +684,10 @@ route_finalize_kernel(const float *__restrict__ prob_partial, const float *__res
     __syncthreads();
     if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
     __syncthreads();
-    if (!last || y != 0) return;
+    if (!last) return;
     __threadfence();
-    if (aux != nullptr) {
-        double s = 0.0;
-        for (int k = x; k < N; k += 32)
-            s += ((double)demand[k] / ((double)T * (double)K)) * ((double)__ldcg(prob_sum + k) / (double)T);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (x == 0) aux[0] = (float)((double)alpha * (double)N * s);
-    }
-    if (z_loss != nullptr) {
-        // router z-loss (lmnt.cn/news/351908 sec. 5.3): beta * mean_t logsumexp_t^2
-        double s = 0.0;
-        for (int r = x; r < rows; r += 32) s += (double)lse_partial[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (x == 0) z_loss[0] = (float)((double)beta * s / (double)T);
-    }
-    if (aux_kl != nullptr) {
-        // KL(uniform || f) balance loss ("MoE逐token路由与活跃参数率实战解析" sec. 3.1
-        // listing): kl_coef * sum_e (1/N) (log(1/N) - log(demand_e / (T K)));
-        // an idle expert gives +inf
-        double s = 0.0;
-        const double u = 1.0 / (double)N;
-        for (int k = x; k < N; k += 32)
-            s += u * (log(u) - log((double)demand[k] / ((double)T * (double)K)));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (x == 0) aux_kl[0] = (float)((double)kl_coef * s);
-    }
+    __shared__ KSum scratch[96];
+    block_losses(N, T, K, demand, prob_sum, lse_partial, rows, alpha, beta, kl_coef, aux, z_loss, aux_kl, scratch);
 }
 
 // Number of blocks of the TopK kernel (general N): a function of T only.
