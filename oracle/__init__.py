@@ -117,6 +117,10 @@ class Oracle:
         lib.oracle_expert_rows.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
+        lib.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_shared_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.oracle_fp8_value.restype = f64
+        lib.oracle_fp8_value.argtypes = [ctypes.c_uint8]
         lib.oracle_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
         lib.oracle_aux_loss.argtypes = [i32, i32, i32, f64, P, P]
         lib.oracle_aux_loss.restype = f64
@@ -199,6 +203,37 @@ class Oracle:
                                    _p(W2), _p(b2), _p(want), _p(y_perm))
         return y_perm
 
+    def fp8_value(self, code: int) -> float:
+        return float(self.lib.oracle_fp8_value(int(code)))
+
+    def expert_ffn_fp8(self, x, offsets, row_token, W1q, s1, b1, W2q, s2, b2, want=None) -> np.ndarray:
+        """expert_ffn with FP8 E4M3 weight codes (uint8) and per-output-channel scales."""
+        x = _np(x, np.uint16)
+        offsets, row_token = _np(offsets, np.int32), _np(row_token, np.int32)
+        W1q, W2q = _np(W1q, np.uint8), _np(W2q, np.uint8)
+        s1, s2 = _np(s1, np.float32), _np(s2, np.float32)
+        b1, b2 = _np(b1, np.float32), _np(b2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        N, f = W1q.shape[0], W1q.shape[1]
+        y_perm = np.zeros((max(int(offsets[N]), 0), d), dtype=np.uint16)
+        self.lib.oracle_expert_ffn_fp8(T, d, f, N, _p(offsets), _p(row_token), _p(x), _p(W1q), _p(s1), _p(b1),
+                                       _p(W2q), _p(s2), _p(b2), _p(want), _p(y_perm))
+        return y_perm
+
+    def shared_ffn_fp8(self, x, Ws1q, ss1, bs1, Ws2q, ss2, bs2, want=None) -> np.ndarray:
+        x = _np(x, np.uint16)
+        Ws1q, Ws2q = _np(Ws1q, np.uint8), _np(Ws2q, np.uint8)
+        ss1, ss2 = _np(ss1, np.float32), _np(ss2, np.float32)
+        bs1, bs2 = _np(bs1, np.float32), _np(bs2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        f = Ws1q.shape[0]
+        z = np.zeros((T, d), dtype=np.uint16)
+        self.lib.oracle_shared_ffn_fp8(T, d, f, _p(x), _p(Ws1q), _p(ss1), _p(bs1), _p(Ws2q), _p(ss2), _p(bs2),
+                                       _p(want), _p(z))
+        return z
+
     def shared_ffn(self, x, Ws1, bs1, Ws2, bs2, want=None) -> np.ndarray:
         x = _np(x, np.uint16)
         Ws1, Ws2 = _np(Ws1, np.uint16), _np(Ws2, np.uint16)
@@ -237,10 +272,13 @@ class Oracle:
     def forward(self, x, Wg, W1, b1, W2, b2, K: int, capacity_factor: float, aux_alpha: float,
                 sel_bias=None, Ws1=None, bs1=None, Ws2=None, bs2=None, want=None,
                 skip_ffn: bool = False, z_beta: float = 1e-3, rank_major: bool = False,
-                kl_coef: float = 0.02) -> OracleResult:
+                kl_coef: float = 0.02, quant=None) -> OracleResult:
         """Full layer forward. Routing, dispatch and the aux loss always cover
         every token; ``want`` (bool/uint8 [T], optional) limits the FFN and the
-        combine to a sample of tokens (the others' outputs are left 0)."""
+        combine to a sample of tokens (the others' outputs are left 0).
+        ``quant`` (optional) holds FP8 expert weights instead of W1/W2/Ws1/Ws2:
+        an object with W1q, s1, W2q, s2 (and Ws1q, ss1, Ws2q, ss2 with a shared
+        expert)."""
         x = _np(x, np.uint16)
         T, d = x.shape
         N = _np(Wg, np.uint16).shape[0]
@@ -254,9 +292,15 @@ class Oracle:
         y_perm = z = y = None
         if not skip_ffn:
             want_u8 = None if want is None else np.ascontiguousarray(np.asarray(want).astype(np.uint8))
-            y_perm = self.expert_ffn(x, offsets, row_token, W1, b1, W2, b2, want_u8)
-            if Ws1 is not None:
-                z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
+            if quant is None:
+                y_perm = self.expert_ffn(x, offsets, row_token, W1, b1, W2, b2, want_u8)
+                if Ws1 is not None:
+                    z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
+            else:
+                q = quant
+                y_perm = self.expert_ffn_fp8(x, offsets, row_token, q.W1q, q.s1, b1, q.W2q, q.s2, b2, want_u8)
+                if bs1 is not None:
+                    z = self.shared_ffn_fp8(x, q.Ws1q, q.ss1, bs1, q.Ws2q, q.ss2, bs2, want_u8)
             y = self.combine(y_perm, slot_of, w, d, z, want_u8)
         return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl, akl)
 
@@ -284,4 +328,5 @@ def forward_inputs(inp, want=None, skip_ffn: bool = False) -> OracleResult:
     return default().forward(inp.x, inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, c.K, c.capacity_factor,
                              c.aux_alpha, inp.sel_bias, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
                              want=want, skip_ffn=skip_ffn, z_beta=getattr(c, "z_beta", 1e-3),
-                             rank_major=getattr(c, "rank_major", False), kl_coef=getattr(c, "kl_coef", 0.02))
+                             rank_major=getattr(c, "rank_major", False), kl_coef=getattr(c, "kl_coef", 0.02),
+                             quant=getattr(inp, "quant", None))

@@ -262,27 +262,79 @@ static double gelu_erf(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); 
 
 double oracle_gelu(double v) { return gelu_erf(v); }
 
+/* ---------------------------------------------------- quantised weights */
+
+/* FP8 E4M3 (the "e4m3fn" variant: no infinities; codes 0x7f/0xff are NaN),
+ * decoded from its definition: sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 holds the subnormals m * 2^-9. */
+static double fp8e4m3_val(uint8_t q)
+{
+    int sgn = q >> 7, ex = (q >> 3) & 15, man = q & 7;
+    double v;
+    if (ex == 15 && man == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)man, -9);
+    else
+        v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+    return sgn ? -v : v;
+}
+
+double oracle_fp8_value(uint8_t q) { return fp8e4m3_val(q); }
+
+/* An expert weight matrix [rows, cols] in nn.Linear layout: bf16 values, or
+ * (weight-only quantisation: the lmnt.cn/news/351908 sec. 4.3 remark on
+ * storing expert weights in 8 or 4 bits, and the CSDN page's sec. 3.2 FP8
+ * weights at one byte per parameter) FP8 E4M3 codes with one fp32 scale per
+ * row, i.e. per output channel, whose dequantised value is code * scale. */
+typedef struct {
+    const uint16_t *bf;
+    const uint8_t *q;
+    const float *scale;
+} wmat;
+
+static double wval(const wmat *m, size_t row, size_t col, size_t cols)
+{
+    if (m->q)
+        return fp8e4m3_val(m->q[row * cols + col]) * (double)m->scale[row];
+    return bf16_val(m->bf[row * cols + col]);
+}
+
+/* Expert e of a stack of N matrices [N, rows, cols]. */
+static wmat wexpert(const wmat *m, int e, size_t rows, size_t cols)
+{
+    wmat r = *m;
+    if (r.q) {
+        r.q += (size_t)e * rows * cols;
+        r.scale += (size_t)e * rows;
+    } else {
+        r.bf += (size_t)e * rows * cols;
+    }
+    return r;
+}
+
+/* ---------------------------------------------------------------- FFN */
+
 /* [Yunthe] MoELayer listing: expert = Linear(d_model -> d_ff) -> GELU ->
- * Linear(d_ff -> d_model), nn.Linear layout [out, in].
+ * Linear(d_ff -> d_model), nn.Linear layout [out, in] (bf16 or quantised),
+ * biases fp32:
  *   h = bf16(GELU(x W1^T + b1)),   out = bf16(h W2^T + b2). */
-static void ffn_row(int d, int f, const uint16_t *xrow, const uint16_t *W1e, const float *b1e,
-                    const uint16_t *W2e, const float *b2e, double *xd, double *h, uint16_t *out)
+static void ffn_row(int d, int f, const uint16_t *xrow, const wmat *W1e, const float *b1e,
+                    const wmat *W2e, const float *b2e, double *xd, double *h, uint16_t *out)
 {
     for (int i = 0; i < d; ++i)
         xd[i] = bf16_val(xrow[i]);
     for (int j = 0; j < f; ++j) {
-        const uint16_t *wr = W1e + (size_t)j * d;
         double acc = 0.0;
         for (int i = 0; i < d; ++i)
-            acc += xd[i] * bf16_val(wr[i]);
+            acc += xd[i] * wval(W1e, (size_t)j, (size_t)i, (size_t)d);
         acc += (double)b1e[j];
         h[j] = bf16_val(bf16_round(gelu_erf(acc)));
     }
     for (int c = 0; c < d; ++c) {
-        const uint16_t *wr = W2e + (size_t)c * f;
         double acc = 0.0;
         for (int j = 0; j < f; ++j)
-            acc += h[j] * bf16_val(wr[j]);
+            acc += h[j] * wval(W2e, (size_t)c, (size_t)j, (size_t)f);
         acc += (double)b2e[c];
         out[c] = bf16_round(acc);
     }
@@ -297,9 +349,10 @@ void oracle_expert_rows(int d, int f, int nrows, const int32_t *rows, const uint
     {
         double *xd = (double *)malloc(sizeof(double) * (size_t)d);
         double *h = (double *)malloc(sizeof(double) * (size_t)f);
+        const wmat w1 = {W1e, NULL, NULL}, w2 = {W2e, NULL, NULL};
 #pragma omp for schedule(dynamic, 1)
         for (int i = 0; i < nrows; ++i)
-            ffn_row(d, f, x + (size_t)rows[i] * d, W1e, b1e, W2e, b2e, xd, h, out + (size_t)i * d);
+            ffn_row(d, f, x + (size_t)rows[i] * d, &w1, b1e, &w2, b2e, xd, h, out + (size_t)i * d);
         free(h);
         free(xd);
     }
@@ -309,8 +362,8 @@ void oracle_expert_rows(int d, int f, int nrows, const int32_t *rows, const uint
  * (expert e = the block r lies in, token t = row_token[r]),
  *   y_perm[r] = E_e(x[t]).
  * Rows whose token has want[t] == 0 are skipped (want may be NULL = all). */
-void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
-                       const uint16_t *x, const uint16_t *W1, const float *b1, const uint16_t *W2,
+static void expert_ffn(int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
+                       const uint16_t *x, const wmat *W1, const float *b1, const wmat *W2,
                        const float *b2, const uint8_t *want, uint16_t *y_perm)
 {
     int R = offsets[N];
@@ -318,7 +371,6 @@ void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const
     for (int e = 0; e < N; ++e)
         for (int r = offsets[e]; r < offsets[e + 1]; ++r)
             row_expert[r] = e;
-    (void)T;
 #pragma omp parallel
     {
         double *xd = (double *)malloc(sizeof(double) * (size_t)d);
@@ -329,8 +381,9 @@ void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const
             if (want && !want[t])
                 continue;
             int e = row_expert[r];
-            ffn_row(d, f, x + (size_t)t * d, W1 + (size_t)e * f * d, b1 + (size_t)e * f,
-                    W2 + (size_t)e * d * f, b2 + (size_t)e * d, xd, h, y_perm + (size_t)r * d);
+            wmat w1 = wexpert(W1, e, (size_t)f, (size_t)d), w2 = wexpert(W2, e, (size_t)d, (size_t)f);
+            ffn_row(d, f, x + (size_t)t * d, &w1, b1 + (size_t)e * f, &w2, b2 + (size_t)e * d, xd, h,
+                    y_perm + (size_t)r * d);
         }
         free(h);
         free(xd);
@@ -338,9 +391,30 @@ void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const
     free(row_expert);
 }
 
+void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
+                       const uint16_t *x, const uint16_t *W1, const float *b1, const uint16_t *W2,
+                       const float *b2, const uint8_t *want, uint16_t *y_perm)
+{
+    const wmat w1 = {W1, NULL, NULL}, w2 = {W2, NULL, NULL};
+    (void)T;
+    expert_ffn(d, f, N, offsets, row_token, x, &w1, b1, &w2, b2, want, y_perm);
+}
+
+/* The same with FP8 E4M3 expert weights: W1q[N][f][d] with scales s1[N][f],
+ * W2q[N][d][f] with scales s2[N][d] (one per output channel). */
+void oracle_expert_ffn_fp8(int T, int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
+                           const uint16_t *x, const uint8_t *W1q, const float *s1, const float *b1,
+                           const uint8_t *W2q, const float *s2, const float *b2, const uint8_t *want,
+                           uint16_t *y_perm)
+{
+    const wmat w1 = {NULL, W1q, s1}, w2 = {NULL, W2q, s2};
+    (void)T;
+    expert_ffn(d, f, N, offsets, row_token, x, &w1, b1, &w2, b2, want, y_perm);
+}
+
 /* [Wiblog] shared expert: the same FFN applied to every token (want may be NULL). */
-void oracle_shared_ffn(int T, int d, int f, const uint16_t *x, const uint16_t *Ws1, const float *bs1,
-                       const uint16_t *Ws2, const float *bs2, const uint8_t *want, uint16_t *z)
+static void shared_ffn(int T, int d, int f, const uint16_t *x, const wmat *Ws1, const float *bs1,
+                       const wmat *Ws2, const float *bs2, const uint8_t *want, uint16_t *z)
 {
 #pragma omp parallel
     {
@@ -355,6 +429,21 @@ void oracle_shared_ffn(int T, int d, int f, const uint16_t *x, const uint16_t *W
         free(h);
         free(xd);
     }
+}
+
+void oracle_shared_ffn(int T, int d, int f, const uint16_t *x, const uint16_t *Ws1, const float *bs1,
+                       const uint16_t *Ws2, const float *bs2, const uint8_t *want, uint16_t *z)
+{
+    const wmat w1 = {Ws1, NULL, NULL}, w2 = {Ws2, NULL, NULL};
+    shared_ffn(T, d, f, x, &w1, bs1, &w2, bs2, want, z);
+}
+
+void oracle_shared_ffn_fp8(int T, int d, int f, const uint16_t *x, const uint8_t *Ws1q, const float *ss1,
+                           const float *bs1, const uint8_t *Ws2q, const float *ss2, const float *bs2,
+                           const uint8_t *want, uint16_t *z)
+{
+    const wmat w1 = {NULL, Ws1q, ss1}, w2 = {NULL, Ws2q, ss2};
+    shared_ffn(T, d, f, x, &w1, bs1, &w2, bs2, want, z);
 }
 
 /* ---------------------------------------------------------------- combine */

@@ -458,10 +458,71 @@ def pin_z_loss(orc):
     assert orc.z_loss(s, 0.0) == 0.0
 
 
+def pin_fp8_decode(orc):
+    """FP8 E4M3 decoding of every code against torch's float8_e4m3fn."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([orc.fp8_value(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert orc.fp8_value(0x7E) == 448.0 and orc.fp8_value(0x01) == 2.0 ** -9
+
+
+def _fp8_exact_weights(rng, shape):
+    """FP8 codes with one power-of-two scale per output row (rows differ), and
+    the same weights as bf16 (code * 2^k has at most 4 significant bits)."""
+    codes = rng.integers(0, 256, size=shape).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3F   # no NaN codes
+    k = rng.integers(-9, -3, size=shape[:-1])
+    scale = np.ldexp(1.0, k).astype(np.float32)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy() * scale[..., None]
+    bf = torch.from_numpy(vals).to(torch.bfloat16)
+    assert np.array_equal(bf.to(torch.float64).numpy(), vals)   # exactly representable
+    return codes, scale, bits(bf)
+
+
+def pin_fp8_experts(orc):
+    """Quantised experts whose dequantised weights are exactly a bf16 weight
+    set give bit-identical outputs to the bf16 experts (routed and shared),
+    so the quantised path inherits the bf16 path's pins; per-row scales differ,
+    so a scale taken from the wrong row or column fails."""
+    rng = np.random.default_rng(17)
+    T, d, f, N, K = 48, 32, 48, 4, 2
+    x = grid_x(rng, T, d)
+    Wg = grid_wg(rng, N, d)
+    W1q, s1, W1 = _fp8_exact_weights(rng, (N, f, d))
+    W2q, s2, W2 = _fp8_exact_weights(rng, (N, d, f))
+    Ws1q, ss1, Ws1 = _fp8_exact_weights(rng, (f, d))
+    Ws2q, ss2, Ws2 = _fp8_exact_weights(rng, (d, f))
+    b1 = (rng.standard_normal((N, f)) * 0.02).astype(np.float32)
+    b2 = (rng.standard_normal((N, d)) * 0.02).astype(np.float32)
+    bs1 = (rng.standard_normal(f) * 0.02).astype(np.float32)
+    bs2 = (rng.standard_normal(d) * 0.02).astype(np.float32)
+    ref = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=0.0, aux_alpha=0.01,
+                      Ws1=Ws1, bs1=bs1, Ws2=Ws2, bs2=bs2)
+
+    class Q:
+        pass
+    q = Q()
+    q.W1q, q.s1, q.W2q, q.s2, q.Ws1q, q.ss1, q.Ws2q, q.ss2 = W1q, s1, W2q, s2, Ws1q, ss1, Ws2q, ss2
+    got = orc.forward(x, Wg, None, b1, None, b2, K=K, capacity_factor=0.0, aux_alpha=0.01,
+                      bs1=bs1, bs2=bs2, quant=q)
+    assert np.array_equal(got.y_perm, ref.y_perm)
+    assert np.array_equal(got.z, ref.z)
+    assert np.array_equal(got.y, ref.y)
+    # and the dense special case through torch: one quantised expert = one Linear/GELU/Linear
+    e_rows = orc.expert_ffn_fp8(x, np.array([0, T], np.int32), np.arange(T, dtype=np.int32),
+                                W1q[:1], s1[:1], b1[:1], W2q[:1], s2[:1], b2[:1])
+    assert_bf16_close(e_rows, to_bf16_bits_f64(torch_expert(x, W1[0], b1[0], W2[0], b2[0])),
+                      what="fp8 dense expert")
+
+
 ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
-    pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts,
+    pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
+    pin_fp8_experts,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
     pin_dispatch_rank_major, pin_aux_kl,
 ]

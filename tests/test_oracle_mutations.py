@@ -10,6 +10,9 @@ import oracle_pins as pins
 
 # (name, [(exact text in moe_oracle.c, replacement)])
 MUTATIONS = [
+    ("fp8_exponent_bias", [("v = ldexp(1.0 + (double)man / 8.0, ex - 7);", "v = ldexp(1.0 + (double)man / 8.0, ex - 8);")]),
+    ("fp8_subnormal_as_normal", [("v = ldexp((double)man, -9);", "v = ldexp(1.0 + (double)man / 8.0, -7);")]),
+    ("fp8_scale_first_row_only", [("* (double)m->scale[row];", "* (double)m->scale[0];")]),
     ("tie_break_flipped", [("return (a->e > b->e) - (a->e < b->e);",
                             "return (a->e < b->e) - (a->e > b->e);")]),
     ("weights_from_biased_logits", [("if (st[buf[k].e] > m)\n                m = st[buf[k].e];",
@@ -24,7 +27,8 @@ MUTATIONS = [
     ("bias2_dropped", [("acc += (double)b2e[c];", "acc += 0.0;")]),
     ("gelu_sign", [("0.5 * v * (1.0 + erf(v / sqrt(2.0)))", "0.5 * v * (1.0 - erf(v / sqrt(2.0)))")]),
     ("hidden_not_rounded", [("h[j] = bf16_val(bf16_round(gelu_erf(acc)));", "h[j] = gelu_erf(acc);")]),
-    ("w2_transposed", [("acc += h[j] * bf16_val(wr[j]);", "acc += h[j] * bf16_val(W2e[(size_t)j * d + c]);")]),
+    ("w2_transposed", [("acc += h[j] * wval(W2e, (size_t)c, (size_t)j, (size_t)f);",
+                        "acc += h[j] * wval(W2e, (size_t)j, (size_t)c, (size_t)d);")]),
     ("combine_weight_index", [("acc += (double)w[(size_t)t * K + k] *",
                                "acc += (double)w[(size_t)t * K + (K - 1 - k)] *")]),
     ("shared_not_added", [("double acc = z ? bf16_val(z[(size_t)t * d + c]) : 0.0;", "double acc = 0.0;")]),

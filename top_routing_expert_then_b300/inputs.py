@@ -52,6 +52,7 @@ class MoEConfig:
     z_beta: float = 1e-3
     rank_major: bool = False   # capacity priority: earlier ranks first instead of earlier tokens
     kl_coef: float = 0.02      # KL-to-uniform balance-loss variant
+    weights: str = "bf16"      # expert weight format: "bf16" or "fp8_e4m3" (per-output-channel scales)
     note: str = ""
 
     def with_(self, **kw) -> "MoEConfig":
@@ -74,6 +75,10 @@ CONFIGS: Dict[str, MoEConfig] = {
                         note="fine-grained 64 experts, Zipf-skewed gate, capacity factor 1.0"),
     "dsv3": MoEConfig("dsv3", 4096, 7168, 2048, 256, 8, 0.0, has_shared=True, sel_bias=True,
                       note="DeepSeek-V3-shaped: 256 routed + 1 shared expert, top-8, selection bias"),
+    "mixtral_decode16_fp8": MoEConfig("mixtral_decode16_fp8", 16, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
+                                      note="Mixtral-shaped decode, 16 tokens, FP8 E4M3 expert weights"),
+    "mixtral_decode64_fp8": MoEConfig("mixtral_decode64_fp8", 64, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
+                                      note="Mixtral-shaped decode, 64 tokens, FP8 E4M3 expert weights"),
 }
 
 
@@ -92,6 +97,7 @@ class MoEInputs:
     Ws2: Optional[torch.Tensor] = None       # [d, f] bf16
     bs2: Optional[torch.Tensor] = None       # [d] fp32
     extra: Dict[str, torch.Tensor] = field(default_factory=dict)
+    quant: Optional["QuantWeights"] = None   # FP8 expert weights (cfg.weights == "fp8_e4m3")
 
     def to(self, device) -> "MoEInputs":
         def mv(t):
@@ -99,7 +105,43 @@ class MoEInputs:
         return MoEInputs(self.cfg, mv(self.x), mv(self.Wg), mv(self.W1), mv(self.b1),
                          mv(self.W2), mv(self.b2), mv(self.sel_bias), mv(self.Ws1),
                          mv(self.bs1), mv(self.Ws2), mv(self.bs2),
-                         {k: mv(v) for k, v in self.extra.items()})
+                         {k: mv(v) for k, v in self.extra.items()},
+                         None if self.quant is None else self.quant.to(device))
+
+
+@dataclass
+class QuantWeights:
+    """FP8 E4M3 expert weights: uint8 codes in nn.Linear layout and one fp32
+    scale per output channel (dequantised weight = code value * scale)."""
+    W1q: torch.Tensor                      # [N, f, d] uint8
+    s1: torch.Tensor                       # [N, f] fp32
+    W2q: torch.Tensor                      # [N, d, f] uint8
+    s2: torch.Tensor                       # [N, d] fp32
+    Ws1q: Optional[torch.Tensor] = None    # [f, d] uint8
+    ss1: Optional[torch.Tensor] = None     # [f] fp32
+    Ws2q: Optional[torch.Tensor] = None    # [d, f] uint8
+    ss2: Optional[torch.Tensor] = None     # [d] fp32
+
+    def to(self, device) -> "QuantWeights":
+        def mv(t):
+            return None if t is None else t.to(device)
+        return QuantWeights(mv(self.W1q), mv(self.s1), mv(self.W2q), mv(self.s2), mv(self.Ws1q),
+                            mv(self.ss1), mv(self.Ws2q), mv(self.ss2))
+
+
+FP8_E4M3_MAX = 448.0
+
+
+def fp8_codes(W: torch.Tensor):
+    """Synthetic FP8 weights for a stack of nn.Linear matrices [..., out, in]:
+    one fp32 scale per output row mapping the row's largest magnitude to 448,
+    codes = torch's float8_e4m3fn cast of W / scale. (Data preparation only:
+    calibrated quantisers need real data and are not part of this package.)"""
+    w = W.to(torch.float32)
+    amax = w.abs().amax(dim=-1).clamp_min(1e-30)
+    scale = (amax / FP8_E4M3_MAX).to(torch.float32)
+    q = (w / scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q.contiguous(), scale.contiguous()
 
 
 ZIPF_AMPLITUDE_64THS = 16
@@ -161,7 +203,18 @@ def make_inputs(cfg: MoEConfig | str, seed: int = 0, device="cpu") -> MoEInputs:
         Ws2 = _randn_bf16((d, f), f ** -0.5, g, device)
         bs2 = torch.randn((d,), generator=g, device=device, dtype=torch.float32) * 0.02
 
-    return MoEInputs(cfg, x, Wg, W1, b1, W2, b2, sel_bias, Ws1, bs1, Ws2, bs2)
+    quant = None
+    if cfg.weights == "fp8_e4m3":
+        W1q, s1 = fp8_codes(W1)
+        W2q, s2 = fp8_codes(W2)
+        quant = QuantWeights(W1q, s1, W2q, s2)
+        if cfg.has_shared:
+            quant.Ws1q, quant.ss1 = fp8_codes(Ws1)
+            quant.Ws2q, quant.ss2 = fp8_codes(Ws2)
+    elif cfg.weights != "bf16":
+        raise ValueError(f"unknown weight format {cfg.weights!r}")
+
+    return MoEInputs(cfg, x, Wg, W1, b1, W2, b2, sel_bias, Ws1, bs1, Ws2, bs2, quant=quant)
 
 
 def make_x(cfg: MoEConfig, seed: int, device="cpu") -> torch.Tensor:
