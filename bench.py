@@ -185,7 +185,8 @@ def whole_job_rate(world: int, tokens_per_rank: int, steps: int, elapsed_ms: flo
 def workload_config(cfg, extra=None):
     c = {"workload": f"{cfg.name}: T={cfg.T} d_model={cfg.d_model} d_ff={cfg.d_ff} N={cfg.N} K={cfg.K} "
                      f"capacity_factor={'dropless' if cfg.capacity_factor <= 0 else cfg.capacity_factor}"
-                     f"{' +shared' if cfg.has_shared else ''}{' +sel_bias' if cfg.sel_bias else ''}",
+                     f"{' +shared' if cfg.has_shared else ''}{' +sel_bias' if cfg.sel_bias else ''}"
+                     f"{' expert_weights=fp8_e4m3 (per-output-channel scales)' if cfg.weights == 'fp8_e4m3' else ''}",
          "tokens_per_step_per_gpu": cfg.T,
          "l2": "inputs larger than L2: the expert weights read every step exceed the 126 MB L2; no flush"}
     if extra:
@@ -279,7 +280,10 @@ def main():
     # algorithmic bytes of the two grouped GEMMs: weights of every expert that
     # received rows (+ shared), x_perm in, H out and back in, y_perm out
     rows_all = R + (T if cfg.has_shared else 0)
-    ffn_bytes = (hit + (1 if cfg.has_shared else 0)) * 2.0 * d * f * 2 + rows_all * (2 * d + 4 * f + 2 * d)
+    fp8 = cfg.weights == "fp8_e4m3"
+    w_elem = 1 if fp8 else 2  # bytes per expert weight (+ one fp32 scale per output channel with FP8)
+    w_bytes = 2.0 * d * f * w_elem + ((d + f) * 4 if fp8 else 0)
+    ffn_bytes = (hit + (1 if cfg.has_shared else 0)) * w_bytes + rows_all * (2 * d + 4 * f + 2 * d)
 
     # ---- timed region: K steps, per-stage marks on the launching stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
@@ -369,7 +373,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"kept_rows": R, "parallelism": f"replicas{world}"}),
-        "roofline": {"kernel": "grouped_gemm_kernel (both expert Linears, tcgen05)",
+        "roofline": {"kernel": ("grouped_gemm_fp8w_kernel (both expert Linears, FP8 weights widened in shared "
+                                "memory, tcgen05)") if fp8 else "grouped_gemm_kernel (both expert Linears, tcgen05)",
                      "bound": "tensor" if tensor_bound else "hbm",
                      "achieved": achieved_tflops if tensor_bound else achieved_gbs,
                      "peak": peak_t if tensor_bound else P["hbm_gbs"],

@@ -99,6 +99,9 @@ typedef struct {
 #define MOE_DROP_TOKEN_ORDER 0
 #define MOE_DROP_RANK_ORDER 1
 
+#define MOE_WEIGHTS_BF16 0
+#define MOE_WEIGHTS_FP8_E4M3 1
+
 /* Layer weights, all DEVICE pointers. */
 typedef struct {
     const moe_bf16 *Wg;   /* [N, d_model]         gate */
@@ -110,6 +113,24 @@ typedef struct {
     const float *bs1;     /* [d_ff] */
     const moe_bf16 *Ws2;  /* [d_model, d_ff] */
     const float *bs2;     /* [d_model] */
+    /* Expert weight format. MOE_WEIGHTS_BF16 (0): W1, W2, Ws1, Ws2 above.
+     * MOE_WEIGHTS_FP8_E4M3: weight-only quantised experts (the 8/4-bit expert
+     * weights of lmnt.cn/news/351908 sec. 4.3 and the one-byte FP8 weights of
+     * the CSDN "MoE逐token路由与活跃参数率实战解析" sec. 3.2): the bf16 expert
+     * matrices are ignored (may be NULL) and each is given as FP8 E4M3 codes
+     * (the "e4m3fn" encoding) in the same nn.Linear layout with one fp32 scale
+     * per output channel; the dequantised weight is code value * scale. The
+     * gate W_g and all biases stay as above. NaN codes (0x7f, 0xff) are not
+     * supported. */
+    int32_t format;
+    const uint8_t *W1q;   /* [N, d_ff, d_model] */
+    const float *s1;      /* [N, d_ff] */
+    const uint8_t *W2q;   /* [N, d_model, d_ff] */
+    const float *s2;      /* [N, d_model] */
+    const uint8_t *Ws1q;  /* [d_ff, d_model] (has_shared) */
+    const float *ss1;     /* [d_ff] */
+    const uint8_t *Ws2q;  /* [d_model, d_ff] */
+    const float *ss2;     /* [d_model] */
 } moe_weights;
 
 /* Optional outputs of moe_forward, all DEVICE pointers; any member may be NULL

@@ -126,7 +126,7 @@ def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages
     if R:
         xp[:R] = inp.x[torch.from_numpy(ref.row_token[:R].astype(np.int64)).cuda()]
     y_perm, z = lib.expert_ffn(shape, xp, torch.from_numpy(ref.offsets).cuda(), inp.W1, inp.b1, inp.W2, inp.b2,
-                               inp.x, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2)
+                               inp.x, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2, quant=inp.quant)
     torch.cuda.synchronize()
     ypb = bits_np(y_perm)[:R]
     if want is None:

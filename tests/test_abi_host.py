@@ -93,6 +93,18 @@ def test_invalid_arguments(L):
     w = lib.MoeWeights(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None)                 # shared missing
     assert L.moe_expert_ffn(ctypes.byref(sh), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, 1 << 40,
                             None) == lib.MOE_ERR_INVALID_ARG
+    # FP8 expert weights: the bf16 matrices may be absent, the codes and scales may not
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, 2)              # unknown format
+    assert L.moe_expert_ffn(ctypes.byref(ok), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, None, FAKE, 1 << 40,
+                            None) == lib.MOE_ERR_INVALID_ARG
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, lib.MOE_WEIGHTS_FP8_E4M3,
+                       FAKE, None, FAKE, FAKE)                                                 # s1 missing
+    assert L.moe_expert_ffn(ctypes.byref(ok), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, None, FAKE, 1 << 40,
+                            None) == lib.MOE_ERR_INVALID_ARG
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, FAKE, None, FAKE, lib.MOE_WEIGHTS_FP8_E4M3,
+                       FAKE, FAKE, FAKE, FAKE)                                                 # shared codes missing
+    assert L.moe_expert_ffn(ctypes.byref(sh), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, 1 << 40,
+                            None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(ok), FAKE, FAKE, None, None, FAKE, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(ok), FAKE, FAKE, FAKE, FAKE + 8, FAKE, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_aux_loss(ctypes.byref(ok), FAKE, None, FAKE, None) == lib.MOE_ERR_INVALID_ARG

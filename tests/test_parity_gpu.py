@@ -46,6 +46,10 @@ SMALL = [
     MoEConfig("multi_wave", 20000, 128, 128, 8, 2, 1.0),
     # general path (N > 256): CUDA-core tiled gate when N % 32 != 0
     MoEConfig("n300_gate_tiled", 257, 64, 64, 300, 3, 2.0),
+    # FP8 E4M3 expert weights (per-output-channel scales): several n-tiles, a
+    # ragged expert, the shared expert, drops
+    MoEConfig("fp8_experts", 700, 256, 640, 8, 2, 1.25, weights="fp8_e4m3"),
+    MoEConfig("fp8_shared_bias", 300, 192, 320, 16, 4, 0.0, has_shared=True, sel_bias=True, weights="fp8_e4m3"),
 ]
 
 
@@ -127,7 +131,8 @@ def test_out_of_range_expert_ids_are_flagged_not_trapped():
 # ---------------------------------------------------------------- full-size workloads
 # Routing and dispatch compared on every token; FFN outputs on a sample of
 # tokens the oracle can evaluate one by one.
-FULL = ["mixtral_prefill", "mixtral_prefill_cf125", "mixtral_decode16", "mixtral_decode64", "skewed", "dsv3"]
+FULL = ["mixtral_prefill", "mixtral_prefill_cf125", "mixtral_decode16", "mixtral_decode64", "skewed", "dsv3",
+        "mixtral_decode16_fp8", "mixtral_decode64_fp8"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -340,9 +340,31 @@ __device__ __forceinline__ void store_drain(int lane) {
 
 // ---------------------------------------------------------------- kernel
 
+// A tile of at most 96 valid rows (an expert's last rows, or every tile of a
+// decode batch) is loaded in 32-row chunks through tmA32, only the chunks that
+// hold rows; the MMA still reads 128 rows, the rest are stale and their
+// results are never stored.
+constexpr int A_CHUNK_ROWS = 32;
+constexpr int A_CHUNK_BYTES = A_CHUNK_ROWS * BK * 2;  // 4 KB: a multiple of the 1024-byte swizzle atom
+
+__device__ __forceinline__ uint32_t a_tile_bytes(int rows) {
+    return rows > 3 * A_CHUNK_ROWS ? (uint32_t)A_BYTES
+                                   : (uint32_t)((rows + A_CHUNK_ROWS - 1) / A_CHUNK_ROWS) * A_CHUNK_BYTES;
+}
+__device__ __forceinline__ void load_a_tile(uint32_t dst, const CUtensorMap *tmA, const CUtensorMap *tmA32,
+                                            uint32_t bar, int x, int row0, int rows) {
+    if (rows > 3 * A_CHUNK_ROWS) {
+        tma_load_2d(dst, tmA, bar, x, row0);
+    } else {
+        for (int c = 0; c * A_CHUNK_ROWS < rows; ++c)
+            tma_load_2d(dst + c * A_CHUNK_BYTES, tmA32, bar, x, row0 + c * A_CHUNK_ROWS);
+    }
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const Params p) {
+                    const __grid_constant__ CUtensorMap tmC, const Params p,
+                    const __grid_constant__ CUtensorMap tmA32) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -410,8 +432,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     const uint32_t fb = smem_u32(&sh->full[stage]);
                     uint8_t *a_s = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d(smem_u32(a_s), &tmA, fb, kb * BK, t.row0);
+                    mbar_arrive_expect_tx(fb, a_tile_bytes(t.rows) + B_BYTES);
+                    load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, kb * BK, t.row0, t.rows);
                     tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
                     issued_phase[stage] = (int)phase;
                     if (++stage == STAGES) {

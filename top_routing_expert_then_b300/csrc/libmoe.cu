@@ -18,6 +18,7 @@
 #include "grouped_gemm.cuh"
 #include "route.cuh"
 #include "route_tc.cuh"
+#include "gemm_fp8w.cuh"
 
 namespace {
 
@@ -267,6 +268,9 @@ moe_status device_state(DeviceState **out) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_mc_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8w_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::Q_SMEM_BYTES);
         const void *routers[] = {
             (const void *)moe::route::router_smallN_kernel<8, 1>, (const void *)moe::route::router_smallN_kernel<8, 2>,
             (const void *)moe::route::router_smallN_kernel<8, 4>, (const void *)moe::route::router_smallN_kernel<8, 8>,
@@ -324,6 +328,21 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, u
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Row-major one-byte [rows, cols] tensor (FP8 codes), no swizzle: box_rows x
+// box_cols bytes land densely, rows box_cols bytes apart.
+bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                  uint32_t box_cols) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -522,7 +541,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
                        cudaStream_t st, float *out_f32, int k_splits) {
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tb, tc, ta32;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
     const bool share_a = !pair && out_f32 == nullptr && k_splits == 1 && use_share_a();
     if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, share_a ? 64 : 128)) return MOE_ERR_CUDA;
@@ -568,8 +587,46 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
-        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p);
+        if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
+        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p, ta32);
     }
+    count_launch();
+    return MOE_OK;
+}
+
+// The grouped GEMM with FP8 expert weights (gemm_fp8w.cuh): A bf16 [a_rows,
+// k_dim], Bq codes [groups * n_out, k_dim], scale [groups * n_out].
+moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, const void *Bq, uint64_t b_rows,
+                           int k_dim, int n_out, int groups, const float *scale, const float *bias, uint16_t *out,
+                           int out_rows, const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows,
+                           bool gelu, cudaStream_t st) {
+    CUtensorMap ta, tb, tc, ta32;
+    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, moe::gg::BM)) return MOE_ERR_CUDA;
+    if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
+    if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::BN, moe::gg::Q_RAW_K)) return MOE_ERR_CUDA;
+    if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
+    moe::gg::Params p;
+    p.mtiles = mtiles;
+    p.num_mtiles = num_mtiles;
+    p.max_mtiles = max_tiles;
+    p.dense_rows = dense_rows;
+    p.n_out = n_out;
+    p.k_dim = k_dim;
+    p.num_groups = groups;
+    p.out_rows = out_rows;
+    p.bias = bias;
+    p.out = out;
+    p.gelu = gelu ? 1 : 0;
+    p.out_f32 = nullptr;
+    p.k_splits = 1;
+    p.raster = kRasterSingle;
+    const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::BM - 1) / moe::gg::BM;
+    const int64_t work = (int64_t)m_upper * ((n_out + moe::gg::BN - 1) / moe::gg::BN);
+    int grid = dev->num_sms;
+    if (work < grid) grid = (int)work;
+    if (grid < 1) grid = 1;
+    moe::gg::grouped_gemm_fp8w_kernel<<<grid, moe::gg::Q_NUM_THREADS, moe::gg::Q_SMEM_BYTES, st>>>(ta, tb, tc, p,
+                                                                                                   scale, ta32);
     count_launch();
     return MOE_OK;
 }
@@ -583,14 +640,36 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     int64_t per_expert = (int64_t)T * K / N;
     const int C = capacity_of(s);
     if (per_expert > C) per_expert = C;
-    const bool pair_routed = use_pair(per_expert);
-    const bool pair_shared = use_pair(T);
+    const bool fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
+    const bool pair_routed = !fp8 && use_pair(per_expert);
+    const bool pair_shared = !fp8 && use_pair(T);
     moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows,
                                                      pair_routed ? moe::gg::PAIR_BM : moe::gg::BM,
                                                      pair_routed ? kRasterPair : kRasterSingle, mt, w.mtiles,
                                                      w.num_mtiles);
     count_launch();
     moe_status r;
+    if (fp8) {
+        // the same four GEMMs with FP8 expert weights and per-channel scales
+        r = launch_gemm_fp8(dev, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->b1, w.H, rows, w.mtiles,
+                            w.num_mtiles, mt, 0, true, st);
+        if (r != MOE_OK) return r;
+        if (s->has_shared) {
+            r = launch_gemm_fp8(dev, x, T, wt->Ws1q, f, d, f, 1, wt->ss1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T,
+                                true, st);
+            if (r != MOE_OK) return r;
+        }
+        if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
+        r = launch_gemm_fp8(dev, w.H, rows, wt->W2q, (uint64_t)N * d, f, d, N, wt->s2, wt->b2, y_perm, rows, w.mtiles,
+                            w.num_mtiles, mt, 0, false, st);
+        if (r != MOE_OK) return r;
+        if (s->has_shared) {
+            r = launch_gemm_fp8(dev, w.Hs, T, wt->Ws2q, d, f, d, 1, wt->ss2, wt->bs2, z, T, nullptr, nullptr, 0, T,
+                                false, st);
+            if (r != MOE_OK) return r;
+        }
+        return launch_status();
+    }
     // routed experts: H = GELU(x_perm W1^T + b1), y_perm = H W2^T + b2
     r = launch_gemm(dev, pair_routed, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
                     w.num_mtiles, mt, 0, true, st);
@@ -640,14 +719,22 @@ moe_status run_aux(const moe_shape *s, const int32_t *demand, const float *prob_
 
 bool weights_ok(const moe_shape *s, const moe_weights *w, bool need_gate) {
     if (w == nullptr) return false;
+    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_FP8_E4M3) return false;
+    const bool q = w->format == MOE_WEIGHTS_FP8_E4M3;
     if (need_gate && (w->Wg == nullptr || !aligned16(w->Wg))) return false;
-    const void *req[] = {w->W1, w->b1, w->W2, w->b2};
-    for (const void *p : req)
-        if (p == nullptr || !aligned16(p)) return false;
+    const void *req_bf[] = {w->W1, w->b1, w->W2, w->b2};
+    const void *req_q[] = {w->W1q, w->s1, w->b1, w->W2q, w->s2, w->b2};
+    for (const void *p : req_bf)
+        if (!q && (p == nullptr || !aligned16(p))) return false;
+    for (const void *p : req_q)
+        if (q && (p == nullptr || !aligned16(p))) return false;
     if (s->has_shared) {
-        const void *sh[] = {w->Ws1, w->bs1, w->Ws2, w->bs2};
-        for (const void *p : sh)
-            if (p == nullptr || !aligned16(p)) return false;
+        const void *sh_bf[] = {w->Ws1, w->bs1, w->Ws2, w->bs2};
+        const void *sh_q[] = {w->Ws1q, w->ss1, w->bs1, w->Ws2q, w->ss2, w->bs2};
+        for (const void *p : sh_bf)
+            if (!q && (p == nullptr || !aligned16(p))) return false;
+        for (const void *p : sh_q)
+            if (q && (p == nullptr || !aligned16(p))) return false;
     }
     return true;
 }

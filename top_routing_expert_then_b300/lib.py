@@ -42,8 +42,13 @@ class MoeShape(ctypes.Structure):
                 ("drop_policy", ctypes.c_int32), ("kl_coef", ctypes.c_float)]
 
 
+MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3 = 0, 1
+
+
 class MoeWeights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("Wg", "W1", "b1", "W2", "b2", "Ws1", "bs1", "Ws2", "bs2")]
+    _fields_ = ([(n, ctypes.c_void_p) for n in ("Wg", "W1", "b1", "W2", "b2", "Ws1", "bs1", "Ws2", "bs2")]
+                + [("format", ctypes.c_int32)]
+                + [(n, ctypes.c_void_p) for n in ("W1q", "s1", "W2q", "s2", "Ws1q", "ss1", "Ws2q", "ss2")])
 
 
 class MoeRouteOut(ctypes.Structure):
@@ -219,34 +224,52 @@ def dispatch(shape: MoeShape, topk_idx, x, ws=None, stream=None):
     return kept, offsets, slot_of, row_token, x_perm
 
 
-def weights_struct(W1, b1, W2, b2, Wg=None, Ws1=None, bs1=None, Ws2=None, bs2=None) -> MoeWeights:
-    bf, f32 = torch.bfloat16, torch.float32
-    return MoeWeights(_ptr(Wg, bf, "Wg"), _ptr(W1, bf, "W1"), _ptr(b1, f32, "b1"), _ptr(W2, bf, "W2"),
-                      _ptr(b2, f32, "b2"), _ptr(Ws1, bf, "Ws1"), _ptr(bs1, f32, "bs1"), _ptr(Ws2, bf, "Ws2"),
-                      _ptr(bs2, f32, "bs2"))
+def weights_struct(W1, b1, W2, b2, Wg=None, Ws1=None, bs1=None, Ws2=None, bs2=None, quant=None) -> MoeWeights:
+    """The C struct; with ``quant`` (FP8 codes and scales: W1q, s1, W2q, s2 and
+    the shared expert's Ws1q, ss1, Ws2q, ss2) the expert matrices are FP8."""
+    bf, f32, u8 = torch.bfloat16, torch.float32, torch.uint8
+    w = MoeWeights(_ptr(Wg, bf, "Wg"), _ptr(W1, bf, "W1"), _ptr(b1, f32, "b1"), _ptr(W2, bf, "W2"),
+                   _ptr(b2, f32, "b2"), _ptr(Ws1, bf, "Ws1"), _ptr(bs1, f32, "bs1"), _ptr(Ws2, bf, "Ws2"),
+                   _ptr(bs2, f32, "bs2"), MOE_WEIGHTS_BF16)
+    if quant is not None:
+        w.format = MOE_WEIGHTS_FP8_E4M3
+        for n, dt in (("W1q", u8), ("s1", f32), ("W2q", u8), ("s2", f32), ("Ws1q", u8), ("ss1", f32),
+                      ("Ws2q", u8), ("ss2", f32)):
+            setattr(w, n, _ptr(getattr(quant, n), dt, n))
+    return w
 
 
-def _check_weights(shape: MoeShape, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None, bs2=None, Wg=None):
+def _check_weights(shape: MoeShape, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None, bs2=None, Wg=None, quant=None):
     N, d, f = shape.N, shape.d_model, shape.d_ff
-    want = {"W1": (W1, (N, f, d)), "b1": (b1, (N, f)), "W2": (W2, (N, d, f)), "b2": (b2, (N, d))}
+    want = {"b1": (b1, (N, f)), "b2": (b2, (N, d))}
+    if quant is None:
+        want.update({"W1": (W1, (N, f, d)), "W2": (W2, (N, d, f))})
+    else:
+        want.update({"W1q": (quant.W1q, (N, f, d)), "s1": (quant.s1, (N, f)), "W2q": (quant.W2q, (N, d, f)),
+                     "s2": (quant.s2, (N, d))})
     if Wg is not None:
         want["Wg"] = (Wg, (N, d))
     if shape.has_shared:
-        want.update({"Ws1": (Ws1, (f, d)), "bs1": (bs1, (f,)), "Ws2": (Ws2, (d, f)), "bs2": (bs2, (d,))})
+        want.update({"bs1": (bs1, (f,)), "bs2": (bs2, (d,))})
+        if quant is None:
+            want.update({"Ws1": (Ws1, (f, d)), "Ws2": (Ws2, (d, f))})
+        else:
+            want.update({"Ws1q": (quant.Ws1q, (f, d)), "ss1": (quant.ss1, (f,)), "Ws2q": (quant.Ws2q, (d, f)),
+                         "ss2": (quant.ss2, (d,))})
     for name, (t, shp) in want.items():
         if t is None or tuple(t.shape) != shp:
             raise ValueError(f"{name} must have shape {shp}, got {None if t is None else tuple(t.shape)}")
 
 
 def expert_ffn(shape: MoeShape, x_perm, expert_offsets, W1, b1, W2, b2, x=None, Ws1=None, bs1=None, Ws2=None,
-               bs2=None, ws=None, stream=None):
-    """-> (y_perm [T*K, d], z [T, d] or None)"""
+               bs2=None, ws=None, stream=None, quant=None):
+    """-> (y_perm [T*K, d], z [T, d] or None); ``quant``: FP8 expert weights."""
     T, K, d = shape.T, shape.K, shape.d_model
-    _check_weights(shape, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2)
+    _check_weights(shape, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2, quant=quant)
     dev = x_perm.device
     y_perm = torch.zeros((T * K, d), dtype=torch.bfloat16, device=dev)
     z = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if shape.has_shared else None
-    wts = weights_struct(W1, b1, W2, b2, None, Ws1, bs1, Ws2, bs2)
+    wts = weights_struct(W1, b1, W2, b2, None, Ws1, bs1, Ws2, bs2, quant=quant)
     ws, wp, wn = _ws(shape, MOE_WS_FFN, ws)
     _check("moe_expert_ffn", load().moe_expert_ffn(
         ctypes.byref(shape), _ptr(x_perm, torch.bfloat16, "x_perm", T * K * d),
@@ -303,18 +326,19 @@ class RouteOutputs:
 class MoELayer:
     """One MoE layer's weights plus a forward workspace, all on one device."""
 
-    def __init__(self, shape: MoeShape, Wg, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None, bs2=None):
-        _check_weights(shape, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2, Wg=Wg)
+    def __init__(self, shape: MoeShape, Wg, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None, bs2=None, quant=None):
+        _check_weights(shape, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2, Wg=Wg, quant=quant)
         self.shape = shape
-        self.tensors = (Wg, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2)  # keep alive
-        self.weights = weights_struct(W1, b1, W2, b2, Wg, Ws1, bs1, Ws2, bs2)
-        self.device = W1.device
+        self.tensors = (Wg, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2, quant)  # keep alive
+        self.weights = weights_struct(W1, b1, W2, b2, Wg, Ws1, bs1, Ws2, bs2, quant=quant)
+        self.device = Wg.device
         self.ws = workspace(shape, MOE_WS_FORWARD, self.device)
 
     @classmethod
     def from_inputs(cls, inp) -> "MoELayer":
         """From an inputs.MoEInputs already on the GPU."""
-        return cls(shape_of(inp.cfg), inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2)
+        return cls(shape_of(inp.cfg), inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
+                   quant=getattr(inp, "quant", None))
 
     def route_outputs(self) -> RouteOutputs:
         T, N, K, dev = self.shape.T, self.shape.N, self.shape.K, self.device
