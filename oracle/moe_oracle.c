@@ -472,6 +472,225 @@ void oracle_combine(int T, int d, int K, const uint16_t *y_perm, const int32_t *
     }
 }
 
+/* ---------------------------------------------------------------- backward */
+
+static double gelu_grad(double v)
+{
+    /* d/dv [v Phi(v)] = Phi(v) + v phi(v) */
+    const double phi = exp(-0.5 * v * v) / sqrt(2.0 * 3.14159265358979323846);
+    return 0.5 * (1.0 + erf(v / sqrt(2.0))) + v * phi;
+}
+
+/* One expert row, forward then backward:
+ *   a = x W1^T + b1, h = bf16(GELU(a)), o = bf16(h W2^T + b2)   (as the forward)
+ *   dw = <dy, o> (returned);  dO = wgt * dy
+ *   dh = dO W2,  da = dh * GELU'(a)
+ *   dW2 += dO^T h,  db2 += dO,  dW1 += da^T x,  db1 += da,  dxrow = da W1
+ * With round_stored, dO and da are rounded to bf16 (the values the GPU keeps
+ * between its GEMMs). wgt = 1 and no dw for the shared expert. */
+static double expert_row_backward(int d, int f, const uint16_t *xrow, const uint16_t *W1e, const float *b1e,
+                                  const uint16_t *W2e, const float *b2e, const uint16_t *dyrow, double wgt,
+                                  int round_stored, double *a, double *h, double *dO, double *dh,
+                                  double *dW1e, double *db1e, double *dW2e, double *db2e, double *dxrow)
+{
+    for (int j = 0; j < f; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i)
+            acc += bf16_val(xrow[i]) * bf16_val(W1e[(size_t)j * d + i]);
+        a[j] = acc + (double)b1e[j];
+        h[j] = bf16_val(bf16_round(gelu_erf(a[j])));
+    }
+    double dw = 0.0;
+    for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int j = 0; j < f; ++j)
+            acc += h[j] * bf16_val(W2e[(size_t)c * f + j]);
+        const double o = bf16_val(bf16_round(acc + (double)b2e[c]));
+        const double g = bf16_val(dyrow[c]);
+        dw += g * o;
+        dO[c] = round_stored ? bf16_val(bf16_round(wgt * g)) : wgt * g;
+    }
+    for (int j = 0; j < f; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += dO[c] * bf16_val(W2e[(size_t)c * f + j]);
+        double da = acc * gelu_grad(a[j]);
+        if (round_stored)
+            da = bf16_val(bf16_round(da));
+        dh[j] = da;
+    }
+    for (int c = 0; c < d; ++c) {
+        db2e[c] += dO[c];
+        for (int j = 0; j < f; ++j)
+            dW2e[(size_t)c * f + j] += dO[c] * h[j];
+    }
+    for (int i = 0; i < d; ++i)
+        dxrow[i] = 0.0;
+    for (int j = 0; j < f; ++j) {
+        db1e[j] += dh[j];
+        for (int i = 0; i < d; ++i) {
+            dW1e[(size_t)j * d + i] += dh[j] * bf16_val(xrow[i]);
+            dxrow[i] += dh[j] * bf16_val(W1e[(size_t)j * d + i]);
+        }
+    }
+    return dw;
+}
+
+/* Gradients of the layer given the upstream gradient dy of y and weights
+ * g_aux, g_z on the balance loss and the router z-loss (the training signal
+ * the pages build around; [Infra] sec. 5). The TopK sets, the capacity drops
+ * and the dispatch are the forward's: piecewise constant, so nothing flows
+ * through the selection, the selection bias, the drops or the KL variant (a
+ * function of the counts). With y_t = z_t + sum_k w_tk o_tk:
+ *   dw_tk = <dy_t, o_tk> (0 when dropped), dO = w_tk dy_t into the expert;
+ *   gate: ds_t[e] = w_te (dw_te - sum_k w_tk dw_tk) for e in the TopK set
+ *         (softmax over the K kept logits, [Infra] sec. 2.1)
+ *       + g_aux alpha N / T * p_te (f_e - sum_e' f_e' p_te')   (aux = alpha N sum f P,
+ *         P_e = mean_t p_te with p_t = softmax over all N, f = demand / (T K) constant)
+ *       + g_z 2 beta / T * lse_t p_te                          (z-loss, [Infra] sec. 5.3)
+ *   dW_g = sum_t ds_t^T x_t,  dx_t += ds_t W_g;  the shared expert gets dO = dy.
+ * s: the forward's logits [T, N]; idx, slot_of [T, K]; offsets [N + 1];
+ * row_token [T K]; demand [N]; dy [T, d] bf16. Outputs (double, written, not
+ * accumulated into): dx [T, d], dWg [N, d], dW1 [N, f, d], db1 [N, f],
+ * dW2 [N, d, f], db2 [N, d], the shared expert's (when Ws1 != NULL) and
+ * dw [T, K]. */
+void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const uint16_t *Wg,
+                     const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
+                     const uint16_t *Ws1, const float *bs1, const uint16_t *Ws2, const float *bs2,
+                     const double *s, const int32_t *idx, const int32_t *slot_of, const int32_t *offsets,
+                     const int32_t *row_token, const int32_t *demand, const uint16_t *dy, double alpha,
+                     double beta, double g_aux, double g_z, int round_stored, double *dx, double *dWg,
+                     double *dW1, double *db1, double *dW2, double *db2, double *dWs1, double *dbs1,
+                     double *dWs2, double *dbs2, double *dw_out)
+{
+    const int R = offsets[N];
+    double *w = (double *)calloc((size_t)T * K, sizeof(double));
+    double *dx_perm = (double *)calloc((size_t)(R > 0 ? R : 1) * d, sizeof(double));
+    double *dx_shared = Ws1 ? (double *)calloc((size_t)T * d, sizeof(double)) : NULL;
+    int *slot_k = (int *)malloc(sizeof(int) * (size_t)(R > 0 ? R : 1));
+
+    /* routing weights in double: softmax over the K selected, unbiased logits */
+    for (int t = 0; t < T; ++t) {
+        double m = -INFINITY, z = 0.0;
+        for (int k = 0; k < K; ++k)
+            m = fmax(m, s[(size_t)t * N + idx[(size_t)t * K + k]]);
+        for (int k = 0; k < K; ++k)
+            z += exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m);
+        for (int k = 0; k < K; ++k)
+            w[(size_t)t * K + k] = exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m) / z;
+        for (int k = 0; k < K; ++k) {
+            int r = slot_of[(size_t)t * K + k];
+            if (r >= 0)
+                slot_k[r] = k;
+        }
+    }
+    memset(dW1, 0, sizeof(double) * (size_t)N * f * d);
+    memset(db1, 0, sizeof(double) * (size_t)N * f);
+    memset(dW2, 0, sizeof(double) * (size_t)N * d * f);
+    memset(db2, 0, sizeof(double) * (size_t)N * d);
+    for (size_t i = 0; i < (size_t)T * K; ++i)
+        dw_out[i] = 0.0;
+
+    /* routed experts: one thread per expert owns its weight gradients */
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)f);
+        double *h = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dO = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e < N; ++e) {
+            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
+                const int t = row_token[r], k = slot_k[r];
+                const double wgt = w[(size_t)t * K + k];
+                dw_out[(size_t)t * K + k] = expert_row_backward(
+                    d, f, x + (size_t)t * d, W1 + (size_t)e * f * d, b1 + (size_t)e * f, W2 + (size_t)e * d * f,
+                    b2 + (size_t)e * d, dy + (size_t)t * d, wgt, round_stored, a, h, dO, dh,
+                    dW1 + (size_t)e * f * d, db1 + (size_t)e * f, dW2 + (size_t)e * d * f, db2 + (size_t)e * d,
+                    dx_perm + (size_t)r * d);
+            }
+        }
+        free(dh);
+        free(dO);
+        free(h);
+        free(a);
+    }
+
+    /* shared expert: weight 1 on every token */
+    if (Ws1) {
+        memset(dWs1, 0, sizeof(double) * (size_t)f * d);
+        memset(dbs1, 0, sizeof(double) * (size_t)f);
+        memset(dWs2, 0, sizeof(double) * (size_t)d * f);
+        memset(dbs2, 0, sizeof(double) * (size_t)d);
+        double *a = (double *)malloc(sizeof(double) * (size_t)f);
+        double *h = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dO = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dh = (double *)malloc(sizeof(double) * (size_t)f);
+        for (int t = 0; t < T; ++t)
+            (void)expert_row_backward(d, f, x + (size_t)t * d, Ws1, bs1, Ws2, bs2, dy + (size_t)t * d, 1.0,
+                                      round_stored, a, h, dO, dh, dWs1, dbs1, dWs2, dbs2,
+                                      dx_shared + (size_t)t * d);
+        free(dh);
+        free(dO);
+        free(h);
+        free(a);
+    }
+
+    /* gate and the token gradient */
+    memset(dWg, 0, sizeof(double) * (size_t)N * d);
+    double *ds = (double *)calloc((size_t)T * N, sizeof(double));
+    const double TK = (double)T * (double)K;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const double *st = s + (size_t)t * N;
+        double *dst = ds + (size_t)t * N;
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < N; ++e)
+            m = fmax(m, st[e]);
+        for (int e = 0; e < N; ++e)
+            z += exp(st[e] - m);
+        const double lse = m + log(z);
+        double fp = 0.0;
+        for (int e = 0; e < N; ++e)
+            fp += ((double)demand[e] / TK) * exp(st[e] - m) / z;
+        for (int e = 0; e < N; ++e) {
+            const double p = exp(st[e] - m) / z;
+            dst[e] = g_aux * alpha * (double)N / (double)T * p * ((double)demand[e] / TK - fp)
+                   + g_z * 2.0 * beta / (double)T * lse * p;
+        }
+        double sdw = 0.0;
+        for (int k = 0; k < K; ++k)
+            sdw += w[(size_t)t * K + k] * dw_out[(size_t)t * K + k];
+        for (int k = 0; k < K; ++k)
+            dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (dw_out[(size_t)t * K + k] - sdw);
+        double *dxt = dx + (size_t)t * d;
+        for (int i = 0; i < d; ++i) {
+            double acc = dx_shared ? dx_shared[(size_t)t * d + i] : 0.0;
+            for (int k = 0; k < K; ++k) {
+                int r = slot_of[(size_t)t * K + k];
+                if (r >= 0)
+                    acc += dx_perm[(size_t)r * d + i];
+            }
+            for (int e = 0; e < N; ++e)
+                acc += dst[e] * bf16_val(Wg[(size_t)e * d + i]);
+            dxt[i] = acc;
+        }
+    }
+    for (int e = 0; e < N; ++e)
+        for (int t = 0; t < T; ++t) {
+            const double g = ds[(size_t)t * N + e];
+            if (g == 0.0)
+                continue;
+            for (int i = 0; i < d; ++i)
+                dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);
+        }
+    free(ds);
+    free(slot_k);
+    free(dx_shared);
+    free(dx_perm);
+    free(w);
+}
+
 /* ---------------------------------------------------------------- KL balance loss */
 
 /* "MoE逐token路由与活跃参数率实战解析" sec. 3.1 and its MoELayer listing: the

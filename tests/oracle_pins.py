@@ -518,11 +518,93 @@ def pin_fp8_experts(orc):
                       what="fp8 dense expert")
 
 
+def _torch_layer_grads(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, shared=None):
+    """torch autograd in float64 of a plain restatement of the layer with the
+    forward's routing decisions held fixed; the bf16 storage points (h, o, y)
+    round the value and pass the gradient through unchanged."""
+    f64 = torch.float64
+
+    def t64(a):
+        return torch.from_numpy(bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)).to(f64)
+
+    def rb(v):  # bf16 rounding with an identity gradient
+        return v + (v.to(torch.bfloat16).to(f64) - v).detach()
+
+    xs, Wgs = t64(x).requires_grad_(), t64(Wg).requires_grad_()
+    W1s, b1s, W2s, b2s = (t64(a).requires_grad_() for a in (W1, b1, W2, b2))
+    T, d = xs.shape
+    N, K = Wgs.shape[0], fwd.topk_idx.shape[1]
+    idx = torch.from_numpy(fwd.topk_idx.astype(np.int64))
+    s = xs @ Wgs.T
+    w = torch.softmax(s.gather(1, idx), dim=1)
+    y = torch.zeros((T, d), dtype=f64)
+    for t in range(T):
+        for k in range(K):
+            if fwd.slot_of[t, k] < 0:
+                continue
+            e = int(idx[t, k])
+            h = rb(torch.nn.functional.gelu(xs[t] @ W1s[e].T + b1s[e]))
+            o = rb(h @ W2s[e].T + b2s[e])
+            y[t] = y[t] + w[t, k] * o
+    extra = []
+    if shared is not None:
+        Ws1s, bs1s, Ws2s, bs2s = (t64(a).requires_grad_() for a in shared)
+        hs = rb(torch.nn.functional.gelu(xs @ Ws1s.T + bs1s))
+        y = y + rb(hs @ Ws2s.T + bs2s)
+        extra = [Ws1s, bs1s, Ws2s, bs2s]
+    p = torch.softmax(s, dim=1)
+    fr = torch.from_numpy(fwd.demand.astype(np.float64)) / (T * K)
+    aux = alpha * N * (fr * p.mean(0)).sum()
+    zl = beta * (torch.logsumexp(s, dim=1) ** 2).mean()
+    L = (rb(y) * t64(dy)).sum() + g_aux * aux + g_z * zl
+    L.backward()
+    g = {"dx": xs.grad, "dWg": Wgs.grad, "dW1": W1s.grad, "db1": b1s.grad, "dW2": W2s.grad, "db2": b2s.grad}
+    if extra:
+        g.update({"dWs1": extra[0].grad, "dbs1": extra[1].grad, "dWs2": extra[2].grad, "dbs2": extra[3].grad})
+    return {k: v.numpy() for k, v in g.items()}
+
+
+def pin_backward_autograd(orc):
+    """The backward against torch autograd in float64 (routing held fixed),
+    with drops (capacity 0.75), a shared expert and non-unit loss weights;
+    dw checked against <dy, o> by its definition through torch as well."""
+    rng = np.random.default_rng(19)
+    T, d, f, N, K = 20, 16, 24, 4, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    Ws1 = randn_bf16(rng, (f, d), d ** -0.5)
+    Ws2 = randn_bf16(rng, (d, f), f ** -0.5)
+    bs1 = (rng.standard_normal(f) * 0.02).astype(np.float32)
+    bs2 = (rng.standard_normal(d) * 0.02).astype(np.float32)
+    dy = bits(torch.from_numpy(rng.standard_normal((T, d))).to(torch.bfloat16))
+    alpha, beta, g_aux, g_z = 0.01, 1e-3, 3.0, 5.0
+    fwd = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=0.75, aux_alpha=alpha, z_beta=beta,
+                      Ws1=Ws1, bs1=bs1, Ws2=Ws2, bs2=bs2)
+    assert (fwd.slot_of < 0).any(), "the case should drop some assignments"
+    got = orc.backward(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, Ws1, bs1, Ws2, bs2,
+                       round_stored=False)
+    ref = _torch_layer_grads(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, (Ws1, bs1, Ws2, bs2))
+    for name, r in ref.items():
+        scale = max(np.abs(r).max(), 1e-30)
+        assert np.abs(got[name] - r).max() <= 1e-10 * scale, name
+    yp = bf16_to_f64(fwd.y_perm)
+    dyv = bf16_to_f64(dy)
+    for t in range(T):
+        for k in range(K):
+            r = fwd.slot_of[t, k]
+            want = 0.0 if r < 0 else float(np.dot(dyv[t], yp[r]))
+            assert abs(got["dw"][t, k] - want) <= 1e-12 * (1 + abs(want))
+    # rounding dO and da to bf16 moves the gradients by about bf16 precision only
+    rnd = orc.backward(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, Ws1, bs1, Ws2, bs2)
+    for name in ("dx", "dW1", "dW2"):
+        rel = np.linalg.norm(rnd[name] - got[name]) / np.linalg.norm(got[name])
+        assert 0 < rel < 1e-2, (name, rel)
+
+
 ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
-    pin_fp8_experts,
+    pin_fp8_experts, pin_backward_autograd,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
     pin_dispatch_rank_major, pin_aux_kl,
 ]

@@ -10,6 +10,12 @@ import oracle_pins as pins
 
 # (name, [(exact text in moe_oracle.c, replacement)])
 MUTATIONS = [
+    ("gelu_grad_no_phi_term", [("return 0.5 * (1.0 + erf(v / sqrt(2.0))) + v * phi;",
+                                "return 0.5 * (1.0 + erf(v / sqrt(2.0)));")]),
+    ("softmax_jacobian_sign", [("dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (dw_out[(size_t)t * K + k] - sdw);",
+                                "dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (sdw - dw_out[(size_t)t * K + k]);")]),
+    ("aux_grad_not_centred", [("((double)demand[e] / TK - fp)", "((double)demand[e] / TK)")]),
+    ("dW2_from_preactivation", [("dW2e[(size_t)c * f + j] += dO[c] * h[j];", "dW2e[(size_t)c * f + j] += dO[c] * a[j];")]),
     ("fp8_exponent_bias", [("v = ldexp(1.0 + (double)man / 8.0, ex - 7);", "v = ldexp(1.0 + (double)man / 8.0, ex - 8);")]),
     ("fp8_subnormal_as_normal", [("v = ldexp((double)man, -9);", "v = ldexp(1.0 + (double)man / 8.0, -7);")]),
     ("fp8_scale_first_row_only", [("* (double)m->scale[row];", "* (double)m->scale[0];")]),
@@ -37,7 +43,8 @@ MUTATIONS = [
     ("round_ties_away", [("nearbyint(ldexp(a, 7 - E))", "round(ldexp(a, 7 - E))")]),
     ("prob_not_normalised", [("P[e] += ex[e] / zn;", "P[e] += ex[e];")]),
     ("z_loss_not_squared", [("acc += lse * lse;", "acc += lse;")]),
-    ("z_loss_no_max_shift", [("double lse = m + log(z);", "double lse = log(z);")]),
+    ("z_loss_no_max_shift", [("double lse = m + log(z);\n        acc += lse * lse;",
+                              "double lse = log(z);\n        acc += lse * lse;")]),
     ("rank_major_ignored", [("const int outer = rank_major ? K : T, inner = rank_major ? T : K;",
                              "const int outer = T, inner = K; (void)rank_major;"),
                             ("const int t = rank_major ? b : a, k = rank_major ? a : b;",
