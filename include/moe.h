@@ -133,6 +133,22 @@ typedef struct {
     const float *ss2;     /* [d_model] */
 } moe_weights;
 
+/* Gradients written by moe_backward, all DEVICE fp32 buffers in the layout
+ * of the corresponding parameter (each is overwritten, not accumulated). */
+typedef struct {
+    float *dx;            /* [T, d_model] */
+    float *dWg;           /* [N, d_model] */
+    float *dW1;           /* [N, d_ff, d_model] */
+    float *db1;           /* [N, d_ff] */
+    float *dW2;           /* [N, d_model, d_ff] */
+    float *db2;           /* [N, d_model] */
+    float *dWs1;          /* [d_ff, d_model] (has_shared) */
+    float *dbs1;          /* [d_ff] */
+    float *dWs2;          /* [d_model, d_ff] */
+    float *dbs2;          /* [d_model] */
+    float *dw;            /* [T, K] gradient of the routing weights (optional, NULL) */
+} moe_grads;
+
 /* Optional outputs of moe_forward, all DEVICE pointers; any member may be NULL
  * (the value is then kept in the workspace only). */
 typedef struct {
@@ -156,7 +172,8 @@ typedef enum {
     MOE_WS_FORWARD = 0,  /* moe_forward and moe_forward_hostio */
     MOE_WS_ROUTE = 1,    /* moe_route */
     MOE_WS_DISPATCH = 2, /* moe_dispatch */
-    MOE_WS_FFN = 3       /* moe_expert_ffn */
+    MOE_WS_FFN = 3,      /* moe_expert_ffn */
+    MOE_WS_BACKWARD = 4  /* moe_backward */
 } moe_ws_kind;
 
 /* capacity = ceil(T / N * capacity_factor), evaluated in double, clamped to
@@ -285,6 +302,29 @@ MOE_API moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights 
 
 /* Reads (and, if clear != 0, resets) the device error word of the current
  * device. Synchronises the device. *code_out receives the MOE_DEVERR_* bits. */
+/* Backward pass of the layer (training; the pages' sec. 5 training signal,
+ * lmnt.cn/news/351908). Recomputes the forward for (x, sel_bias) and writes
+ * the gradients of
+ *     L = <dy, y> + g_aux * aux + g_z * z_loss
+ * with respect to x and every weight and bias, for the forward's routing
+ * decisions (TopK sets, capacity drops and dispatch are piecewise constant:
+ * no gradient flows through them, through sel_bias or the KL variant):
+ *   combine   dw_tk = <dy_t, o_tk> (0 when dropped), dO = bf16(w_tk dy_t)
+ *   experts   dh = dO W2, da = bf16(dh * GELU'(a)) with a = x W1^T + b1,
+ *             dW2 = dO^T h, db2 = sum dO, dW1 = da^T x, db1 = sum da,
+ *             dx += da W1 through the dispatch; shared expert with dO = dy
+ *   gate      ds_t = w (dw - <w, dw>) on the TopK set (softmax over the kept
+ *             logits, sec. 2.1) + g_aux alpha N / T p (f - <f, p>) + g_z 2 beta
+ *             / T lse p (sec. 5.2-5.3), dWg = ds^T x, dx += ds Wg
+ * dO and da are stored in bf16 between the tensor-core GEMMs, every other
+ * intermediate and every gradient in fp32. dy: [T, d_model] bf16 (device).
+ * grads: see moe_grads. BF16 expert weights only (FP8: MOE_ERR_UNSUPPORTED).
+ * workspace >= moe_workspace_bytes(shape, MOE_WS_BACKWARD). Asynchronous on
+ * `stream`. */
+MOE_API moe_status moe_backward(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
+                                const float *sel_bias, const moe_bf16 *dy, float g_aux, float g_z,
+                                const moe_grads *grads, void *workspace, size_t workspace_bytes, void *stream);
+
 MOE_API moe_status moe_get_device_error(int32_t clear, int32_t *code_out);
 
 /* Number of kernels this library has launched in this process (all devices,

@@ -93,6 +93,9 @@ struct Params {
                               // split s written to out_f32 + s * out_rows * n_out
     int k_splits;             // fp32 mode: the K range is cut into this many splits
     int raster;               // m-tiles per raster group (dense mode; the list mode stores groups)
+    const int *k_ranges;      // fp32 mode: non-null = split s covers the reduction columns
+                              // [k_ranges[s], k_ranges[s + 1]) (multiples of 64, device memory);
+                              // an empty range writes zeros (per-expert weight gradients)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -420,8 +423,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int brow = t.group * p.n_out + t.n0;
-                const int kb0 = (w % splits) * kb_per_split;
-                const int kb1 = min(kblocks, kb0 + kb_per_split);
+                const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
+                const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
                 if (PF_DIST > 0)
                     for (int kb = kb0; kb < kb1 && kb < kb0 + PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -463,8 +466,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                const int kb0 = (w % splits) * kb_per_split;
-                const int kb1 = min(kblocks, kb0 + kb_per_split);
+                const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
+                const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true)) {
                         stop = true;
@@ -526,6 +529,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (out32_row != nullptr) {
                     // fp32 mode: n_out is a multiple of 4, columns past it are not stored
                     const int ncols = min(32, p.n_out - col);
+                    if (p.k_ranges && p.k_ranges[w % splits] == p.k_ranges[w % splits + 1]) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;  // nothing accumulated
+                    }
                     if (store) {
                         uint4 *dst = reinterpret_cast<uint4 *>(out32_row + col);
 #pragma unroll

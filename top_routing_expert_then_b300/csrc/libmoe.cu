@@ -19,6 +19,7 @@
 #include "route.cuh"
 #include "route_tc.cuh"
 #include "gemm_fp8w.cuh"
+#include "backward.cuh"
 
 namespace {
 
@@ -202,6 +203,63 @@ ForwardWs carve_forward(Carve &c, const moe_shape *s) {
     return w;
 }
 
+// Backward workspace: the forward's, plus the recomputed pre-activations, the
+// backward intermediates, transposed weights and the transposed, 64-padded
+// activation copies the per-expert weight-gradient GEMMs reduce over.
+struct BackwardWs {
+    ForwardWs fwd;
+    int4 *mtiles;
+    int *num_mtiles;
+    float *A1, *DH, *DXP, *L, *DS, *dw;
+    uint16_t *DA, *dO, *W1t, *W2t, *dOT, *HT, *DAT, *XPT;
+    int32_t *poff;
+    size_t ldp;  // columns of the padded transposed copies
+    // shared expert
+    float *As1, *DHs, *DXs;
+    uint16_t *DAs, *Ws1t, *Ws2t, *dyT, *HsT, *DAsT, *xT;
+    int32_t *soff, *spoff;
+    size_t ldt;
+};
+BackwardWs carve_backward(Carve &c, const moe_shape *s) {
+    BackwardWs w{};
+    const size_t T = s->T, d = s->d_model, f = s->d_ff, N = s->N, R = (size_t)s->T * s->K;
+    w.fwd = carve_forward(c, s);
+    w.mtiles = c.take<int4>((size_t)max_mtiles(s));
+    w.num_mtiles = c.take<int>(4);
+    w.A1 = c.take<float>(R * f);
+    w.DH = c.take<float>(R * f);
+    w.DXP = c.take<float>(R * d);
+    w.L = c.take<float>(T * N);
+    w.DS = c.take<float>(T * N);
+    w.dw = c.take<float>(R);
+    w.DA = c.take<uint16_t>(R * f);
+    w.dO = c.take<uint16_t>(R * d);
+    w.W1t = c.take<uint16_t>(N * d * f);
+    w.W2t = c.take<uint16_t>(N * f * d);
+    w.ldp = (R + 63) / 64 * 64 + 64 * N;  // >= sum of the 64-padded groups; rows 16-byte aligned
+    w.dOT = c.take<uint16_t>(d * w.ldp);
+    w.HT = c.take<uint16_t>(f * w.ldp);
+    w.DAT = c.take<uint16_t>(f * w.ldp);
+    w.XPT = c.take<uint16_t>(d * w.ldp);
+    w.poff = c.take<int32_t>(N + 1);
+    if (s->has_shared) {
+        w.ldt = (T + 63) / 64 * 64;
+        w.As1 = c.take<float>(T * f);
+        w.DHs = c.take<float>(T * f);
+        w.DXs = c.take<float>(T * d);
+        w.DAs = c.take<uint16_t>(T * f);
+        w.Ws1t = c.take<uint16_t>(d * f);
+        w.Ws2t = c.take<uint16_t>(f * d);
+        w.dyT = c.take<uint16_t>(d * w.ldt);
+        w.HsT = c.take<uint16_t>(f * w.ldt);
+        w.DAsT = c.take<uint16_t>(f * w.ldt);
+        w.xT = c.take<uint16_t>(d * w.ldt);
+        w.soff = c.take<int32_t>(2);
+        w.spoff = c.take<int32_t>(2);
+    }
+    return w;
+}
+
 size_t ws_bytes(const moe_shape *s, int kind) {
     Carve c(nullptr);
     switch (kind) {
@@ -209,6 +267,7 @@ size_t ws_bytes(const moe_shape *s, int kind) {
         case MOE_WS_DISPATCH: carve_dispatch(c, s); break;
         case MOE_WS_FFN: carve_ffn(c, s); break;
         case MOE_WS_FORWARD: carve_forward(c, s); break;
+        case MOE_WS_BACKWARD: carve_backward(c, s); break;
         default: return 0;
     }
     return c.bytes();
@@ -352,7 +411,7 @@ bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1);
+                       cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1, const int *k_ranges = nullptr);
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
@@ -540,10 +599,11 @@ bool use_share_a() { return gemm_variant_override() == kShareA; }
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st, float *out_f32, int k_splits) {
+                       cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges) {
     CUtensorMap ta, tb, tc, ta32;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
     const bool share_a = !pair && out_f32 == nullptr && k_splits == 1 && use_share_a();
+    if (out_f32 != nullptr) pair = false;  // the fp32 (raw accumulator) mode is single-SM only
     if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, share_a ? 64 : 128)) return MOE_ERR_CUDA;
     if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
     if (out != nullptr) {
@@ -551,7 +611,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     } else {
         tc = ta;  // fp32 mode: the epilogue stores directly and never reads this map
     }
-    moe::gg::Params p;
+    moe::gg::Params p{};
     p.mtiles = mtiles;
     p.num_mtiles = num_mtiles;
     p.max_mtiles = max_tiles;
@@ -565,6 +625,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     p.gelu = gelu ? 1 : 0;
     p.out_f32 = out_f32;
     p.k_splits = k_splits;
+    p.k_ranges = k_ranges;
     if (pair && (out_f32 != nullptr || k_splits != 1)) return MOE_ERR_UNSUPPORTED;
     const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
     p.raster = pair ? kRasterPair : kRasterSingle;
@@ -605,7 +666,7 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
     if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
     if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::BN, moe::gg::Q_RAW_K)) return MOE_ERR_CUDA;
     if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
-    moe::gg::Params p;
+    moe::gg::Params p{};
     p.mtiles = mtiles;
     p.num_mtiles = num_mtiles;
     p.max_mtiles = max_tiles;
@@ -713,6 +774,146 @@ moe_status run_combine(const moe_shape *s, const uint16_t *y_perm, const int32_t
 moe_status run_aux(const moe_shape *s, const int32_t *demand, const float *prob_sum, float *aux,
                    cudaStream_t st) {
     moe::dispatch::aux_loss_kernel<<<1, 256, 0, st>>>(demand, prob_sum, s->T, s->N, s->K, s->aux_alpha, aux);
+    count_launch();
+    return launch_status();
+}
+
+// Transposes of the grouped rows in[rows(offsets), C] into out[C, ld] (zeroed
+// first: padding columns must read as zeros).
+moe_status transpose_grouped(const uint16_t *in, int R, int C, const int32_t *offsets, const int32_t *poff, int N,
+                             uint16_t *out, size_t ld, cudaStream_t st) {
+    if (cudaMemsetAsync(out, 0, (size_t)C * ld * sizeof(uint16_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (R <= 0) return MOE_OK;
+    dim3 grid((C + 31) / 32, (R + 31) / 32);
+    moe::bwd::transpose_grouped_kernel<<<grid, moe::bwd::kThreads, 0, st>>>(in, R, C, offsets, poff, N, out, ld);
+    count_launch();
+    return launch_status();
+}
+
+moe_status batched_transpose(const uint16_t *in, int G, int A, int B, uint16_t *out, cudaStream_t st) {
+    dim3 grid((B + 31) / 32, (A + 31) / 32, G);
+    moe::bwd::batched_transpose_kernel<<<grid, moe::bwd::kThreads, 0, st>>>(in, A, B, out);
+    count_launch();
+    return launch_status();
+}
+
+moe_status simt_gemm(const float *a, size_t a_ks, size_t a_ms, const uint16_t *b, size_t ldb, int M, int Nn, int Kk,
+                     float *c, size_t ldc, cudaStream_t st) {
+    dim3 grid((Nn + moe::bwd::kSB - 1) / moe::bwd::kSB, (M + moe::bwd::kSB - 1) / moe::bwd::kSB);
+    moe::bwd::simt_gemm_kernel<<<grid, moe::bwd::kThreads, 0, st>>>(a, a_ks, a_ms, b, ldb, M, Nn, Kk, c, ldc);
+    count_launch();
+    return launch_status();
+}
+
+moe_status run_backward(const moe_shape *s, DeviceState *dev, const moe_weights *wt, const uint16_t *x,
+                        const float *sel_bias, const uint16_t *dy, float g_aux, float g_z, const moe_grads *g,
+                        const BackwardWs &w, cudaStream_t st) {
+    const int T = s->T, N = s->N, K = s->K, d = s->d_model, f = s->d_ff;
+    const int rows = T * K;
+    const int mt = max_mtiles(s);
+    const ForwardWs &fw = w.fwd;
+    float *dw = g->dw ? g->dw : w.dw;
+    moe_status r;
+    // ---- forward recompute (routing decisions, H = h, y_perm = o)
+    if ((r = run_route(s, dev, x, wt->Wg, sel_bias, fw.topk_idx, fw.topk_w, fw.demand, fw.prob_sum, nullptr, fw.route,
+                       st)) != MOE_OK)
+        return r;
+    if ((r = run_dispatch(s, fw.topk_idx, x, fw.kept, fw.offsets, fw.slot_of, fw.row_token, fw.x_perm, fw.disp,
+                          st)) != MOE_OK)
+        return r;
+    if ((r = run_ffn(s, dev, fw.x_perm, fw.offsets, wt, x, fw.y_perm, fw.z, fw.ffn, st)) != MOE_OK) return r;
+    // the 128-row tile list for the single-SM fp32 GEMMs below
+    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(fw.offsets, N, rows, moe::gg::BM, kRasterSingle, mt, w.mtiles,
+                                                     w.num_mtiles);
+    count_launch();
+    // pre-activations a = x W1^T (raw fp32; the bias is added where GELU' is taken)
+    if ((r = launch_gemm(dev, false, fw.x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, nullptr, rows,
+                         w.mtiles, w.num_mtiles, mt, 0, false, st, w.A1)) != MOE_OK)
+        return r;
+    // gate logits in fp32 (exact on the input grid, any order)
+    {
+        dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
+        moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, wt->Wg, T, d, N, w.L);
+        count_launch();
+    }
+    // ---- combine backward
+    moe::bwd::combine_backward_kernel<<<T, moe::bwd::kThreads, 0, st>>>(dy, fw.y_perm, fw.slot_of, fw.topk_w, K, d,
+                                                                        dw, w.dO);
+    count_launch();
+    // ---- routed experts
+    if ((r = batched_transpose(wt->W2, N, d, f, w.W2t, st)) != MOE_OK) return r;  // W2t[e] = W2[e]^T: [f, d]
+    if ((r = batched_transpose(wt->W1, N, f, d, w.W1t, st)) != MOE_OK) return r;  // W1t[e] = W1[e]^T: [d, f]
+    if ((r = launch_gemm(dev, false, w.dO, rows, w.W2t, (uint64_t)N * f, d, f, N, wt->b1, nullptr, rows, w.mtiles,
+                         w.num_mtiles, mt, 0, false, st, w.DH)) != MOE_OK)
+        return r;
+    moe::bwd::gelu_backward_kernel<<<rows, moe::bwd::kThreads, 0, st>>>(w.DH, w.A1, wt->b1, fw.offsets, N, f, w.DA);
+    count_launch();
+    if ((r = launch_gemm(dev, false, w.DA, rows, w.W1t, (uint64_t)N * d, f, d, N, wt->b2, nullptr, rows, w.mtiles,
+                         w.num_mtiles, mt, 0, false, st, w.DXP)) != MOE_OK)
+        return r;
+    moe::bwd::expert_colsum_kernel<<<dim3((f + 255) / 256, N), moe::bwd::kThreads, 0, st>>>(w.DA, fw.offsets, f,
+                                                                                           g->db1);
+    moe::bwd::expert_colsum_kernel<<<dim3((d + 255) / 256, N), moe::bwd::kThreads, 0, st>>>(w.dO, fw.offsets, d,
+                                                                                           g->db2);
+    moe::bwd::padded_offsets_kernel<<<1, 32, 0, st>>>(fw.offsets, N, w.poff);
+    count_launch();
+    count_launch();
+    count_launch();
+    if ((r = transpose_grouped(w.dO, rows, d, fw.offsets, w.poff, N, w.dOT, w.ldp, st)) != MOE_OK) return r;
+    if ((r = transpose_grouped(fw.ffn.H, rows, f, fw.offsets, w.poff, N, w.HT, w.ldp, st)) != MOE_OK) return r;
+    if ((r = transpose_grouped(w.DA, rows, f, fw.offsets, w.poff, N, w.DAT, w.ldp, st)) != MOE_OK) return r;
+    if ((r = transpose_grouped(fw.x_perm, rows, d, fw.offsets, w.poff, N, w.XPT, w.ldp, st)) != MOE_OK) return r;
+    // dW2[e] = dO_e^T H_e: [d, f], dW1[e] = DA_e^T X_e: [f, d] -- the expert's rows are the reduction
+    if ((r = launch_gemm(dev, false, w.dOT, d, w.HT, f, (int)w.ldp, f, 1, wt->b1, nullptr, d, nullptr, nullptr, 0, d,
+                         false, st, g->dW2, N, w.poff)) != MOE_OK)
+        return r;
+    if ((r = launch_gemm(dev, false, w.DAT, f, w.XPT, d, (int)w.ldp, d, 1, wt->b1, nullptr, f, nullptr, nullptr, 0, f,
+                         false, st, g->dW1, N, w.poff)) != MOE_OK)
+        return r;
+    // ---- shared expert (weight 1: dO = dy)
+    const float *dxs = nullptr;
+    if (s->has_shared) {
+        moe::bwd::single_group_kernel<<<1, 32, 0, st>>>(T, w.soff, w.spoff);
+        count_launch();
+        if ((r = launch_gemm(dev, false, x, T, wt->Ws1, f, d, f, 1, wt->bs1, nullptr, T, nullptr, nullptr, 0, T, false,
+                             st, w.As1)) != MOE_OK)
+            return r;
+        if ((r = batched_transpose(wt->Ws2, 1, d, f, w.Ws2t, st)) != MOE_OK) return r;
+        if ((r = batched_transpose(wt->Ws1, 1, f, d, w.Ws1t, st)) != MOE_OK) return r;
+        if ((r = launch_gemm(dev, false, dy, T, w.Ws2t, f, d, f, 1, wt->bs1, nullptr, T, nullptr, nullptr, 0, T, false,
+                             st, w.DHs)) != MOE_OK)
+            return r;
+        moe::bwd::gelu_backward_kernel<<<T, moe::bwd::kThreads, 0, st>>>(w.DHs, w.As1, wt->bs1, w.soff, 1, f, w.DAs);
+        count_launch();
+        if ((r = launch_gemm(dev, false, w.DAs, T, w.Ws1t, d, f, d, 1, wt->bs2, nullptr, T, nullptr, nullptr, 0, T,
+                             false, st, w.DXs)) != MOE_OK)
+            return r;
+        moe::bwd::expert_colsum_kernel<<<dim3((f + 255) / 256, 1), moe::bwd::kThreads, 0, st>>>(w.DAs, w.soff, f,
+                                                                                               g->dbs1);
+        moe::bwd::expert_colsum_kernel<<<dim3((d + 255) / 256, 1), moe::bwd::kThreads, 0, st>>>(dy, w.soff, d,
+                                                                                               g->dbs2);
+        count_launch();
+        count_launch();
+        if ((r = transpose_grouped(dy, T, d, w.soff, w.spoff, 1, w.dyT, w.ldt, st)) != MOE_OK) return r;
+        if ((r = transpose_grouped(fw.ffn.Hs, T, f, w.soff, w.spoff, 1, w.HsT, w.ldt, st)) != MOE_OK) return r;
+        if ((r = transpose_grouped(w.DAs, T, f, w.soff, w.spoff, 1, w.DAsT, w.ldt, st)) != MOE_OK) return r;
+        if ((r = transpose_grouped(x, T, d, w.soff, w.spoff, 1, w.xT, w.ldt, st)) != MOE_OK) return r;
+        if ((r = launch_gemm(dev, false, w.dyT, d, w.HsT, f, (int)w.ldt, f, 1, wt->bs1, nullptr, d, nullptr, nullptr, 0,
+                             d, false, st, g->dWs2, 1, w.spoff)) != MOE_OK)
+            return r;
+        if ((r = launch_gemm(dev, false, w.DAsT, f, w.xT, d, (int)w.ldt, d, 1, wt->bs1, nullptr, f, nullptr, nullptr, 0,
+                             f, false, st, g->dWs1, 1, w.spoff)) != MOE_OK)
+            return r;
+        dxs = w.DXs;
+    }
+    // ---- gate
+    moe::bwd::gate_backward_kernel<<<(T + 7) / 8, moe::bwd::kThreads, 0, st>>>(
+        w.L, fw.topk_idx, fw.topk_w, dw, fw.demand, T, N, K, s->aux_alpha, s->z_beta, g_aux, g_z, w.DS);
+    count_launch();
+    // dWg[e, i] = sum_t DS[t, e] x[t, i];  dx[t, i] = sum_e DS[t, e] Wg[e, i]
+    if ((r = simt_gemm(w.DS, (size_t)N, 1, x, (size_t)d, N, d, T, g->dWg, (size_t)d, st)) != MOE_OK) return r;
+    if ((r = simt_gemm(w.DS, 1, (size_t)N, wt->Wg, (size_t)d, T, d, N, g->dx, (size_t)d, st)) != MOE_OK) return r;
+    moe::bwd::dx_gather_kernel<<<T, moe::bwd::kThreads, 0, st>>>(w.DXP, fw.slot_of, dxs, K, d, g->dx);
     count_launch();
     return launch_status();
 }
@@ -978,6 +1179,31 @@ moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights *weights
         return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+moe_status moe_backward(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,
+                        const float *sel_bias, const moe_bf16 *dy, float g_aux, float g_z, const moe_grads *grads,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (!x || !dy || !aligned16(x) || !aligned16(dy) || !grads || !weights_ok(shape, weights, true))
+        return MOE_ERR_INVALID_ARG;
+    if (weights->format != MOE_WEIGHTS_BF16) return MOE_ERR_UNSUPPORTED;
+    if (std::isnan(g_aux) || std::isnan(g_z)) return MOE_ERR_INVALID_ARG;
+    const void *req[] = {grads->dx, grads->dWg, grads->dW1, grads->db1, grads->dW2, grads->db2};
+    for (const void *p : req)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (shape->has_shared) {
+        const void *sh[] = {grads->dWs1, grads->dbs1, grads->dWs2, grads->dbs2};
+        for (const void *p : sh)
+            if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    }
+    if ((r = check_ws(shape, MOE_WS_BACKWARD, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    Carve c(workspace);
+    BackwardWs w = carve_backward(c, shape);
+    return run_backward(shape, dev, weights, x, sel_bias, dy, g_aux, g_z, grads, w, as_stream(stream));
 }
 
 moe_status moe_get_device_error(int32_t clear, int32_t *code_out) {

@@ -222,3 +222,9 @@ def make_x(cfg: MoEConfig, seed: int, device="cpu") -> torch.Tensor:
     g = _gen(torch.device(device), seed)
     return (torch.randint(-128, 129, (cfg.T, cfg.d_model), generator=g, device=device,
                           dtype=torch.int32).to(torch.float32) / 64).to(torch.bfloat16)
+
+
+def make_dy(cfg: MoEConfig, seed: int, device="cpu") -> torch.Tensor:
+    """A seeded upstream gradient for the layer output: N(0, 1) rounded to bf16."""
+    g = _gen(torch.device(device), seed + 1000)
+    return torch.randn((cfg.T, cfg.d_model), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)

@@ -21,7 +21,7 @@ LIBRARY = os.path.join(HERE, "libmoe.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
-MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_FFN = range(4)
+MOE_WS_FORWARD, MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_FFN, MOE_WS_BACKWARD = range(5)
 DEVERR_EXPERT_ID, DEVERR_ROW_INDEX, DEVERR_TIMEOUT, DEVERR_TILE_LIST = 1, 2, 4, 8
 
 
@@ -49,6 +49,11 @@ class MoeWeights(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_void_p) for n in ("Wg", "W1", "b1", "W2", "b2", "Ws1", "bs1", "Ws2", "bs2")]
                 + [("format", ctypes.c_int32)]
                 + [(n, ctypes.c_void_p) for n in ("W1q", "s1", "W2q", "s2", "Ws1q", "ss1", "Ws2q", "ss2")])
+
+
+class MoeGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dx", "dWg", "dW1", "db1", "dW2", "db2", "dWs1", "dbs1", "dWs2",
+                                               "dbs2", "dw")]
 
 
 class MoeRouteOut(ctypes.Structure):
@@ -94,6 +99,8 @@ def load():
                                 ctypes.POINTER(ctypes.c_void_p), P], i32),
         "moe_forward_hostio": ([S, ctypes.POINTER(MoeWeights), P, P, P, P, P, ctypes.POINTER(MoeRouteOut),
                                 P, sz, P], i32),
+        "moe_backward": ([S, ctypes.POINTER(MoeWeights), P, P, P, ctypes.c_float, ctypes.c_float,
+                          ctypes.POINTER(MoeGrads), P, sz, P], i32),
         "moe_get_device_error": ([i32, ctypes.POINTER(i32)], i32),
         "moe_launch_count": ([], ctypes.c_uint64),
     }
@@ -366,6 +373,25 @@ class MoELayer:
             _ptr(sel_bias, torch.float32, "sel_bias", s.N), _ptr(y, torch.bfloat16, "y", s.T * s.d_model),
             self._out_struct(route_out), self.ws.data_ptr(), self.ws.numel(), _stream(stream)))
         return y
+
+    def backward(self, x, dy, sel_bias=None, g_aux: float = 1.0, g_z: float = 1.0, ws=None, stream=None) -> dict:
+        """moe_backward: fp32 gradients {dx, dWg, dW1, db1, dW2, db2, dw (+ dWs1, dbs1, dWs2, dbs2)} of
+        <dy, y> + g_aux * aux + g_z * z_loss for this layer at x."""
+        s = self.shape
+        T, d, f, N, K, dev = s.T, s.d_model, s.d_ff, s.N, s.K, self.device
+        e = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)  # noqa: E731
+        g = {"dx": e(T, d), "dWg": e(N, d), "dW1": e(N, f, d), "db1": e(N, f), "dW2": e(N, d, f), "db2": e(N, d),
+             "dw": e(T, K)}
+        if s.has_shared:
+            g.update({"dWs1": e(f, d), "dbs1": e(f), "dWs2": e(d, f), "dbs2": e(d)})
+        gs = MoeGrads(*(g[n].data_ptr() if n in g else None for n in (
+            "dx", "dWg", "dW1", "db1", "dW2", "db2", "dWs1", "dbs1", "dWs2", "dbs2", "dw")))
+        ws, wp, wn = _ws(s, MOE_WS_BACKWARD, ws)
+        _check("moe_backward", load().moe_backward(
+            ctypes.byref(s), ctypes.byref(self.weights), _ptr(x, torch.bfloat16, "x", T * d),
+            _ptr(sel_bias, torch.float32, "sel_bias", N), _ptr(dy, torch.bfloat16, "dy", T * d), float(g_aux),
+            float(g_z), ctypes.byref(gs), wp, wn, _stream(stream)))
+        return g
 
     def forward_marked(self, x, events, sel_bias=None, y=None, route_out: Optional[RouteOutputs] = None,
                        stream=None):
