@@ -238,6 +238,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=1024, help="tokens in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--backward-steps", type=int, default=10,
+                    help="also time moe_backward (forward recompute + backward) for this many steps; 0 = off")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -249,7 +251,7 @@ def main():
 
     import torch
     from top_routing_expert_then_b300 import lib
-    from top_routing_expert_then_b300.inputs import make_inputs
+    from top_routing_expert_then_b300.inputs import make_dy, make_inputs
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -354,6 +356,26 @@ def main():
     e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
     e2e_value = whole_job_rate(world, T, args.e2e_steps, e2e_ms)
 
+    # ---- training step: moe_backward (recomputes the forward, then every gradient)
+    train = None
+    if args.backward_steps > 0 and cfg.weights == "bf16":
+        dy = make_dy(cfg, args.seed, device=dev)
+        bws = lib.workspace(layer.shape, lib.MOE_WS_BACKWARD, dev)
+        for _ in range(2):
+            layer.backward(inp.x, dy, inp.sel_bias, ws=bws)
+        torch.cuda.synchronize()
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.backward_steps):
+            layer.backward(inp.x, dy, inp.sel_bias, ws=bws)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bwd_ms = max_over_ranks(pg, b0.elapsed_time(b1), dev) / args.backward_steps
+        train = {"ms_per_step": bwd_ms, "tokens_per_s": whole_job_rate(world, T, 1, bwd_ms),
+                 "steps": args.backward_steps, "what": "moe_backward: forward recompute + all gradients (fp32)"}
+        del bws
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -394,6 +416,7 @@ def main():
             "combine": {"bytes": combine_bytes, "gbs": combine_bytes / (stage_ms[4] * 1e-3) / 1e9},
             "peak_gbs": P["hbm_gbs"]},
         "cpu_baseline": cpu,
+        "train_step": train,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
                 "steps": args.e2e_steps},
         "gpu_launches": launches,

@@ -119,7 +119,7 @@ class Oracle:
         lib.oracle_shared_ffn.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
-        lib.oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [P] * 17 + [f64, f64, f64, f64, i32] + [P] * 11
+        lib.oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [P] * 17 + [f64, f64, f64, f64, i32] + [P] * 12
         lib.oracle_fp8_value.restype = f64
         lib.oracle_fp8_value.argtypes = [ctypes.c_uint8]
         lib.oracle_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
@@ -271,11 +271,12 @@ class Oracle:
 
     def backward(self, x, Wg, W1, b1, W2, b2, fwd: "OracleResult", dy, aux_alpha: float, z_beta: float,
                  g_aux: float = 1.0, g_z: float = 1.0, Ws1=None, bs1=None, Ws2=None, bs2=None,
-                 round_stored: bool = True) -> dict:
+                 round_stored: bool = True, want=None) -> dict:
         """Gradients of the layer (see oracle_backward in moe_oracle.c) for the
         routing decisions of ``fwd`` and the upstream gradient ``dy`` [T, d]
         (bf16). Returns float64 arrays dx, dWg, dW1, db1, dW2, db2, dw (and
-        dWs1, dbs1, dWs2, dbs2 with a shared expert)."""
+        dWs1, dbs1, dWs2, dbs2 with a shared expert). ``want`` (bool [T])
+        limits the work to those tokens' dx and dw."""
         x, Wg = _np(x, np.uint16), _np(Wg, np.uint16)
         W1, W2 = _np(W1, np.uint16), _np(W2, np.uint16)
         b1, b2 = _np(b1, np.float32), _np(b2, np.float32)
@@ -287,9 +288,11 @@ class Oracle:
         if shared:
             Ws1, Ws2 = _np(Ws1, np.uint16), _np(Ws2, np.uint16)
             bs1, bs2 = _np(bs1, np.float32), _np(bs2, np.float32)
-        out = {"dx": np.zeros((T, d)), "dWg": np.zeros((N, d)), "dW1": np.zeros((N, f, d)), "db1": np.zeros((N, f)),
-               "dW2": np.zeros((N, d, f)), "db2": np.zeros((N, d)), "dw": np.zeros((T, K))}
-        if shared:
+        out = {"dx": np.zeros((T, d)), "dw": np.zeros((T, K))}
+        if want is None:
+            out.update({"dWg": np.zeros((N, d)), "dW1": np.zeros((N, f, d)), "db1": np.zeros((N, f)),
+                        "dW2": np.zeros((N, d, f)), "db2": np.zeros((N, d))})
+        if shared and want is None:
             out.update({"dWs1": np.zeros((f, d)), "dbs1": np.zeros(f), "dWs2": np.zeros((d, f)),
                         "dbs2": np.zeros(d)})
         s = np.ascontiguousarray(fwd.logits, dtype=np.float64)
@@ -298,8 +301,10 @@ class Oracle:
             _p(s), _p(np.ascontiguousarray(fwd.topk_idx, np.int32)), _p(np.ascontiguousarray(fwd.slot_of, np.int32)),
             _p(np.ascontiguousarray(fwd.offsets, np.int32)), _p(np.ascontiguousarray(fwd.row_token, np.int32)),
             _p(np.ascontiguousarray(fwd.demand, np.int32)), _p(dy), float(aux_alpha), float(z_beta), float(g_aux),
-            float(g_z), 1 if round_stored else 0, _p(out["dx"]), _p(out["dWg"]), _p(out["dW1"]), _p(out["db1"]),
-            _p(out["dW2"]), _p(out["db2"]), _p(out.get("dWs1")), _p(out.get("dbs1")), _p(out.get("dWs2")),
+            float(g_z), 1 if round_stored else 0,
+            _p(None if want is None else np.ascontiguousarray(np.asarray(want).astype(np.uint8))),
+            _p(out["dx"]), _p(out.get("dWg")), _p(out.get("dW1")), _p(out.get("db1")),
+            _p(out.get("dW2")), _p(out.get("db2")), _p(out.get("dWs1")), _p(out.get("dbs1")), _p(out.get("dWs2")),
             _p(out.get("dbs2")), _p(out["dw"]))
         return out
 
@@ -357,12 +362,12 @@ def forward(*args, **kw) -> OracleResult:
 
 
 def backward_inputs(inp, fwd: OracleResult, dy, g_aux: float = 1.0, g_z: float = 1.0,
-                    round_stored: bool = True) -> dict:
+                    round_stored: bool = True, want=None) -> dict:
     """Backward over the fields of the seeded input generator (bf16 experts)."""
     c = inp.cfg
     return default().backward(inp.x, inp.Wg, inp.W1, inp.b1, inp.W2, inp.b2, fwd, dy, c.aux_alpha,
                               getattr(c, "z_beta", 1e-3), g_aux, g_z, inp.Ws1, inp.bs1, inp.Ws2, inp.bs2,
-                              round_stored=round_stored)
+                              round_stored=round_stored, want=want)
 
 
 def forward_inputs(inp, want=None, skip_ffn: bool = False) -> OracleResult:

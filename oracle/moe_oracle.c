@@ -519,17 +519,21 @@ static double expert_row_backward(int d, int f, const uint16_t *xrow, const uint
             da = bf16_val(bf16_round(da));
         dh[j] = da;
     }
-    for (int c = 0; c < d; ++c) {
-        db2e[c] += dO[c];
-        for (int j = 0; j < f; ++j)
-            dW2e[(size_t)c * f + j] += dO[c] * h[j];
+    if (dW2e) {  /* NULL: only dx and dw wanted */
+        for (int c = 0; c < d; ++c) {
+            db2e[c] += dO[c];
+            for (int j = 0; j < f; ++j)
+                dW2e[(size_t)c * f + j] += dO[c] * h[j];
+        }
     }
     for (int i = 0; i < d; ++i)
         dxrow[i] = 0.0;
     for (int j = 0; j < f; ++j) {
-        db1e[j] += dh[j];
+        if (dW1e)
+            db1e[j] += dh[j];
         for (int i = 0; i < d; ++i) {
-            dW1e[(size_t)j * d + i] += dh[j] * bf16_val(xrow[i]);
+            if (dW1e)
+                dW1e[(size_t)j * d + i] += dh[j] * bf16_val(xrow[i]);
             dxrow[i] += dh[j] * bf16_val(W1e[(size_t)j * d + i]);
         }
     }
@@ -553,14 +557,16 @@ static double expert_row_backward(int d, int f, const uint16_t *xrow, const uint
  * row_token [T K]; demand [N]; dy [T, d] bf16. Outputs (double, written, not
  * accumulated into): dx [T, d], dWg [N, d], dW1 [N, f, d], db1 [N, f],
  * dW2 [N, d, f], db2 [N, d], the shared expert's (when Ws1 != NULL) and
- * dw [T, K]. */
+ * dw [T, K]. want (may be NULL = all): only tokens with want[t] != 0 get dx
+ * and dw, and no weight or bias gradient is formed (those outputs may then be
+ * NULL). */
 void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const uint16_t *Wg,
                      const uint16_t *W1, const float *b1, const uint16_t *W2, const float *b2,
                      const uint16_t *Ws1, const float *bs1, const uint16_t *Ws2, const float *bs2,
                      const double *s, const int32_t *idx, const int32_t *slot_of, const int32_t *offsets,
                      const int32_t *row_token, const int32_t *demand, const uint16_t *dy, double alpha,
-                     double beta, double g_aux, double g_z, int round_stored, double *dx, double *dWg,
-                     double *dW1, double *db1, double *dW2, double *db2, double *dWs1, double *dbs1,
+                     double beta, double g_aux, double g_z, int round_stored, const uint8_t *want, double *dx,
+                     double *dWg, double *dW1, double *db1, double *dW2, double *db2, double *dWs1, double *dbs1,
                      double *dWs2, double *dbs2, double *dw_out)
 {
     const int R = offsets[N];
@@ -584,10 +590,13 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
                 slot_k[r] = k;
         }
     }
-    memset(dW1, 0, sizeof(double) * (size_t)N * f * d);
-    memset(db1, 0, sizeof(double) * (size_t)N * f);
-    memset(dW2, 0, sizeof(double) * (size_t)N * d * f);
-    memset(db2, 0, sizeof(double) * (size_t)N * d);
+    const int weights = want == NULL;
+    if (weights) {
+        memset(dW1, 0, sizeof(double) * (size_t)N * f * d);
+        memset(db1, 0, sizeof(double) * (size_t)N * f);
+        memset(dW2, 0, sizeof(double) * (size_t)N * d * f);
+        memset(db2, 0, sizeof(double) * (size_t)N * d);
+    }
     for (size_t i = 0; i < (size_t)T * K; ++i)
         dw_out[i] = 0.0;
 
@@ -602,11 +611,14 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
         for (int e = 0; e < N; ++e) {
             for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
                 const int t = row_token[r], k = slot_k[r];
+                if (want && !want[t])
+                    continue;
                 const double wgt = w[(size_t)t * K + k];
                 dw_out[(size_t)t * K + k] = expert_row_backward(
                     d, f, x + (size_t)t * d, W1 + (size_t)e * f * d, b1 + (size_t)e * f, W2 + (size_t)e * d * f,
                     b2 + (size_t)e * d, dy + (size_t)t * d, wgt, round_stored, a, h, dO, dh,
-                    dW1 + (size_t)e * f * d, db1 + (size_t)e * f, dW2 + (size_t)e * d * f, db2 + (size_t)e * d,
+                    weights ? dW1 + (size_t)e * f * d : NULL, weights ? db1 + (size_t)e * f : NULL,
+                    weights ? dW2 + (size_t)e * d * f : NULL, weights ? db2 + (size_t)e * d : NULL,
                     dx_perm + (size_t)r * d);
             }
         }
@@ -618,18 +630,21 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
 
     /* shared expert: weight 1 on every token */
     if (Ws1) {
-        memset(dWs1, 0, sizeof(double) * (size_t)f * d);
-        memset(dbs1, 0, sizeof(double) * (size_t)f);
-        memset(dWs2, 0, sizeof(double) * (size_t)d * f);
-        memset(dbs2, 0, sizeof(double) * (size_t)d);
+        if (weights) {
+            memset(dWs1, 0, sizeof(double) * (size_t)f * d);
+            memset(dbs1, 0, sizeof(double) * (size_t)f);
+            memset(dWs2, 0, sizeof(double) * (size_t)d * f);
+            memset(dbs2, 0, sizeof(double) * (size_t)d);
+        }
         double *a = (double *)malloc(sizeof(double) * (size_t)f);
         double *h = (double *)malloc(sizeof(double) * (size_t)f);
         double *dO = (double *)malloc(sizeof(double) * (size_t)d);
         double *dh = (double *)malloc(sizeof(double) * (size_t)f);
         for (int t = 0; t < T; ++t)
-            (void)expert_row_backward(d, f, x + (size_t)t * d, Ws1, bs1, Ws2, bs2, dy + (size_t)t * d, 1.0,
-                                      round_stored, a, h, dO, dh, dWs1, dbs1, dWs2, dbs2,
-                                      dx_shared + (size_t)t * d);
+            if (!want || want[t])
+                (void)expert_row_backward(d, f, x + (size_t)t * d, Ws1, bs1, Ws2, bs2, dy + (size_t)t * d, 1.0,
+                                          round_stored, a, h, dO, dh, weights ? dWs1 : NULL, weights ? dbs1 : NULL,
+                                          weights ? dWs2 : NULL, weights ? dbs2 : NULL, dx_shared + (size_t)t * d);
         free(dh);
         free(dO);
         free(h);
@@ -637,11 +652,14 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
     }
 
     /* gate and the token gradient */
-    memset(dWg, 0, sizeof(double) * (size_t)N * d);
+    if (weights)
+        memset(dWg, 0, sizeof(double) * (size_t)N * d);
     double *ds = (double *)calloc((size_t)T * N, sizeof(double));
     const double TK = (double)T * (double)K;
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
+        if (want && !want[t])
+            continue;
         const double *st = s + (size_t)t * N;
         double *dst = ds + (size_t)t * N;
         double m = -INFINITY, z = 0.0;
@@ -676,7 +694,7 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
             dxt[i] = acc;
         }
     }
-    for (int e = 0; e < N; ++e)
+    for (int e = 0; e < N && weights; ++e)
         for (int t = 0; t < T; ++t) {
             const double g = ds[(size_t)t * N + e];
             if (g == 0.0)

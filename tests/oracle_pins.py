@@ -600,11 +600,27 @@ def pin_backward_autograd(orc):
         assert 0 < rel < 1e-2, (name, rel)
 
 
+def pin_backward_token_mask(orc):
+    """The token-masked backward (used on full-size workloads) gives the same
+    dx and dw on the wanted tokens as the full backward."""
+    rng = np.random.default_rng(23)
+    T, d, f, N, K = 30, 16, 32, 4, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    dy = bits(torch.from_numpy(rng.standard_normal((T, d))).to(torch.bfloat16))
+    fwd = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=1.0, aux_alpha=0.01)
+    full = orc.backward(x, Wg, W1, b1, W2, b2, fwd, dy, 0.01, 1e-3)
+    want = np.zeros(T, dtype=bool)
+    want[[0, 7, 29]] = True
+    part = orc.backward(x, Wg, W1, b1, W2, b2, fwd, dy, 0.01, 1e-3, want=want)
+    assert np.array_equal(part["dx"][want], full["dx"][want])
+    assert np.array_equal(part["dw"][want], full["dw"][want])
+
+
 ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
-    pin_fp8_experts, pin_backward_autograd,
+    pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
     pin_dispatch_rank_major, pin_aux_kl,
 ]
