@@ -93,6 +93,8 @@ class OracleResult:
     aux: float
     z_loss: float
     aux_kl: float = 0.0
+    health: Optional[np.ndarray] = None      # util_std, drop_rate, mean entropy, max |logit|
+    mean_weight: Optional[np.ndarray] = None  # [N]
 
 
 class Oracle:
@@ -120,6 +122,7 @@ class Oracle:
         lib.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [P] * 17 + [f64, f64, f64, f64, i32] + [P] * 12
+        lib.oracle_health.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_fp8_value.restype = f64
         lib.oracle_fp8_value.argtypes = [ctypes.c_uint8]
         lib.oracle_combine.argtypes = [i32, i32, i32, P, P, P, P, P, P]
@@ -203,6 +206,18 @@ class Oracle:
         self.lib.oracle_expert_ffn(T, d, f, N, _p(offsets), _p(row_token), _p(x), _p(W1), _p(b1),
                                    _p(W2), _p(b2), _p(want), _p(y_perm))
         return y_perm
+
+    def health(self, s, demand, kept, idx, w):
+        """-> (h [4]: util_std, drop_rate, mean entropy, max |logit|; mean_w [N])."""
+        s = np.ascontiguousarray(s, dtype=np.float64)
+        T, N = s.shape
+        idx = _np(idx, np.int32)
+        K = idx.shape[1]
+        h = np.zeros(4)
+        mw = np.zeros(N)
+        self.lib.oracle_health(T, N, K, _p(s), _p(_np(demand, np.int32)), _p(_np(kept, np.int32)), _p(idx),
+                               _p(_np(w, np.float32)), _p(h), _p(mw))
+        return h, mw
 
     def fp8_value(self, code: int) -> float:
         return float(self.lib.oracle_fp8_value(int(code)))
@@ -342,7 +357,9 @@ class Oracle:
                 if bs1 is not None:
                     z = self.shared_ffn_fp8(x, q.Ws1q, q.ss1, bs1, q.Ws2q, q.ss2, bs2, want_u8)
             y = self.combine(y_perm, slot_of, w, d, z, want_u8)
-        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl, akl)
+        hl, mw = self.health(s, demand, kept, idx, w)
+        return OracleResult(s, idx, w, demand, P, C, kept, offsets, slot_of, row_token, y_perm, z, y, aux, zl, akl,
+                            hl, mw)
 
 
 _default: Optional[Oracle] = None

@@ -472,6 +472,59 @@ void oracle_combine(int T, int d, int K, const uint16_t *y_perm, const int32_t *
     }
 }
 
+/* ---------------------------------------------------------------- router health */
+
+/* Router health statistics the pages monitor (lmnt.cn/news/351908 sec. 8.2
+ * and 9.3: tokens per expert, mean routing weight per expert, token drop
+ * rate, gate logit range; the CSDN page's sec. 3.3 expert_util_std):
+ *   h[0] util_std     population std over experts of f_e = demand_e / (T K)
+ *   h[1] drop_rate    fraction of the T K assignments dropped by capacity
+ *   h[2] entropy      mean over tokens of the entropy (nats) of softmax_N(s_t)
+ *   h[3] max |s|      largest gate logit magnitude
+ *   mean_w[e]         mean routing weight of the assignments to e (0 if none) */
+void oracle_health(int T, int N, int K, const double *s, const int32_t *demand, const int32_t *kept,
+                   const int32_t *idx, const float *w, double *h, double *mean_w)
+{
+    const double TK = (double)T * (double)K;
+    double mean = 0.0, var = 0.0;
+    for (int e = 0; e < N; ++e)
+        mean += (double)demand[e] / TK;
+    mean /= (double)N;
+    for (int e = 0; e < N; ++e) {
+        const double df = (double)demand[e] / TK - mean;
+        var += df * df;
+    }
+    h[0] = sqrt(var / (double)N);
+    double kept_all = 0.0;
+    for (int e = 0; e < N; ++e)
+        kept_all += (double)kept[e];
+    h[1] = 1.0 - kept_all / TK;
+    double ent = 0.0, amax = 0.0;
+    for (int t = 0; t < T; ++t) {
+        const double *st = s + (size_t)t * N;
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < N; ++e)
+            m = fmax(m, st[e]);
+        for (int e = 0; e < N; ++e)
+            z += exp(st[e] - m);
+        for (int e = 0; e < N; ++e) {
+            const double p = exp(st[e] - m) / z;
+            if (p > 0.0)
+                ent -= p * log(p);
+            amax = fmax(amax, fabs(st[e]));
+        }
+    }
+    h[2] = ent / (double)T;
+    h[3] = amax;
+    for (int e = 0; e < N; ++e)
+        mean_w[e] = 0.0;
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k)
+            mean_w[idx[(size_t)t * K + k]] += (double)w[(size_t)t * K + k];
+    for (int e = 0; e < N; ++e)
+        mean_w[e] = demand[e] > 0 ? mean_w[e] / (double)demand[e] : 0.0;
+}
+
 /* ---------------------------------------------------------------- backward */
 
 static double gelu_grad(double v)

@@ -616,11 +616,42 @@ def pin_backward_token_mask(orc):
     assert np.array_equal(part["dw"][want], full["dw"][want])
 
 
+def pin_health(orc):
+    """Router health statistics: entropy vs scipy.stats.entropy per token;
+    equal logits give log N and a spread of 0 over equal loads; a closed-form
+    two-level load; drop rate from the dispatch counts; mean weights vs
+    numpy.bincount; max |logit| vs numpy."""
+    import scipy.stats
+    rng = np.random.default_rng(29)
+    T, N, K = 40, 6, 2
+    s = rng.standard_normal((T, N)) * 3
+    idx, w, demand, _ = orc.route(s, K)
+    C = 9
+    kept = orc.dispatch(idx, N, C)[0]
+    h, mw = orc.health(s, demand, kept, idx, w)
+    p = scipy.special.softmax(s, axis=1)
+    assert abs(h[2] - np.mean(scipy.stats.entropy(p, axis=1))) < 1e-12
+    f = demand / (T * K)
+    assert abs(h[0] - np.std(f)) < 1e-15
+    assert abs(h[1] - (1 - kept.sum() / (T * K))) < 1e-15 and h[1] > 0
+    assert abs(h[3] - np.abs(s).max()) == 0
+    ref_mw = np.bincount(idx.ravel(), weights=w.ravel().astype(np.float64), minlength=N)
+    ref_mw = np.where(demand > 0, ref_mw / np.maximum(demand, 1), 0.0)
+    assert np.allclose(mw, ref_mw, rtol=1e-15, atol=1e-15)
+    # equal logits: entropy log N, every token on experts 0..K-1
+    s0 = np.full((8, 4), 1.5)
+    idx0, w0, d0, _ = orc.route(s0, 2)
+    h0, _ = orc.health(s0, d0, d0, idx0, w0)
+    assert abs(h0[2] - math.log(4)) < 1e-14 and h0[1] == 0.0
+    # loads (1/2, 1/2, 0, 0) -> std 1/4
+    assert abs(h0[0] - 0.25) < 1e-15
+
+
 ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
-    pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask,
+    pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask, pin_health,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
     pin_dispatch_rank_major, pin_aux_kl,
 ]

@@ -10,6 +10,8 @@ import oracle_pins as pins
 
 # (name, [(exact text in moe_oracle.c, replacement)])
 MUTATIONS = [
+    ("health_std_sample", [("h[0] = sqrt(var / (double)N);", "h[0] = sqrt(var / (double)(N - 1));")]),
+    ("health_entropy_sign", [("ent -= p * log(p);", "ent += p * log(p);")]),
     ("gelu_grad_no_phi_term", [("return 0.5 * (1.0 + erf(v / sqrt(2.0))) + v * phi;",
                                 "return 0.5 * (1.0 + erf(v / sqrt(2.0)));")]),
     ("softmax_jacobian_sign", [("dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (dw_out[(size_t)t * K + k] - sdw);",
