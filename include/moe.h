@@ -165,6 +165,14 @@ typedef struct {
     float *aux_kl;           /* [1] kl_coef * sum_e (1/N) (log(1/N) - log f_e), f_e = demand_e/(T K)
                                 (KL-to-uniform balance loss of the CSDN MoELayer listing);
                                 +inf when an expert receives nothing */
+    float *health;           /* [4] router health statistics (lmnt.cn/news/351908 sec. 8.2 and
+                                9.3 monitors; the CSDN page's sec. 3.3 expert_util_std):
+                                [0] population std over experts of f_e = demand_e / (T K),
+                                [1] fraction of the T K assignments dropped by capacity,
+                                [2] mean routing entropy (nats) of the full softmax,
+                                [3] max |gate logit| */
+    float *mean_weight;      /* [N] mean routing weight of the assignments to each expert
+                                (0 for an idle expert) */
 } moe_route_out;
 
 /* Workspace sizes. */

@@ -97,6 +97,13 @@ def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages
     else:
         assert kl == ref.aux_kl, ("aux_kl", kl, ref.aux_kl)
 
+    hl = ro.health.cpu().numpy().astype(np.float64)
+    assert abs(hl[0] - ref.health[0]) <= 1e-5 * ref.health[0] + 1e-7, ("util_std", hl[0], ref.health[0])
+    assert abs(hl[1] - ref.health[1]) <= 1e-6, ("drop_rate", hl[1], ref.health[1])
+    assert abs(hl[2] - ref.health[2]) <= 1e-5 * abs(ref.health[2]) + 1e-6, ("entropy", hl[2], ref.health[2])
+    assert hl[3] == np.float32(ref.health[3]), ("max|logit|", hl[3], ref.health[3])
+    assert np.allclose(ro.mean_weight.cpu().numpy(), ref.mean_weight, rtol=0, atol=W_ATOL), "mean_weight"
+
     yb = bits_np(y)
     rows = slice(None) if want is None else want.astype(bool)
     assert_bf16_tol(yb[rows], ref.y[rows], "forward y")

@@ -59,10 +59,12 @@ count_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int32_t *__re
 }
 
 // One block. base[c][e] = sum_{c' < c} hist[c'][e]; kept[e] = min(total, C);
-// offsets = exclusive prefix of kept (offsets[N] = kept rows R).
+// offsets = exclusive prefix of kept (offsets[N] = kept rows R). drop_rate
+// (optional): the fraction of the `total` assignments past capacity (the
+// token drop rate the lmnt.cn/news/351908 sec. 8.2 / 9.3 monitors watch).
 __global__ void __launch_bounds__(1024)
 scan_kernel(const int32_t *__restrict__ hist, int chunks, int N, int C, int32_t *__restrict__ base,
-            int32_t *__restrict__ kept, int32_t *__restrict__ offsets) {
+            int32_t *__restrict__ kept, int32_t *__restrict__ offsets, float *__restrict__ drop_rate, int total) {
     extern __shared__ int sh[];  // [N] kept, then scan buffer [N]
     int *kv = sh;
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
@@ -89,6 +91,7 @@ scan_kernel(const int32_t *__restrict__ hist, int chunks, int N, int C, int32_t 
     }
     if (e < N) offsets[e + 1] = v;
     if (e == 0) offsets[0] = 0;
+    if (drop_rate != nullptr && e == N - 1) drop_rate[0] = (float)((double)(total - v) / (double)total);
 }
 
 // slot_of[t, k] = offsets[e] + p if p < C else -1; row_token[slot] = t.

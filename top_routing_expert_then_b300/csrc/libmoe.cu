@@ -92,14 +92,15 @@ struct RouteWs {
     float *lse_partial;            // per-block sums of logsumexp^2
     unsigned long long *acc;       // fused path: fixed-point probability sums  } zeroed
     int32_t *dem;                  // fused path: assignments per expert         } by one
-    unsigned int *done;            // finished-block ticket                      } memset
+    unsigned long long *wacc;      // fixed-point routing-weight sums            } memset
+    unsigned int *done;            // finished-block ticket                      } (fused path)
 };
 
 // Routing for N <= 256 runs as one fused kernel (tensor-core gate, TopK,
-// softmax, statistics and losses). MOE_ROUTE_VARIANT=legacy (environment,
-// read once) selects the general path instead: CUDA-core router for N <= 16,
-// otherwise gate GEMM + TopK kernel + finalize kernel. N > 256 always takes
-// the general path.
+// softmax, statistics and losses). N > 256 takes the general path: gate GEMM
+// (tensor cores when N % 32 == 0, else CUDA-core tiles) + TopK kernel +
+// finalize kernel; MOE_ROUTE_VARIANT=legacy (environment, read once) selects
+// the general path for every N.
 bool legacy_route() {
     static const bool v = []() {
         const char *e = std::getenv("MOE_ROUTE_VARIANT");
@@ -140,9 +141,10 @@ RouteWs carve_route(Carve &c, const moe_shape *s) {
         w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
         w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
     }
-    w.lse_partial = c.take<float>(rows);
+    w.lse_partial = c.take<float>(rows * moe::route::kPartialStride);
     w.acc = c.take<unsigned long long>(s->N);
     w.dem = c.take<int32_t>(s->N);
+    w.wacc = c.take<unsigned long long>(s->N);
     w.done = c.take<unsigned int>(4);
     return w;
 }
@@ -307,7 +309,6 @@ const void *fused_route_kernel(int lpl, int S) {
     return fused_route_kernel_s<8>(S);
 }
 
-constexpr int kSmallGateMaxN = 16;
 
 moe_status device_state(DeviceState **out) {
     int dev = 0;
@@ -330,15 +331,6 @@ moe_status device_state(DeviceState **out) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8w_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::Q_SMEM_BYTES);
-        const void *routers[] = {
-            (const void *)moe::route::router_smallN_kernel<8, 1>, (const void *)moe::route::router_smallN_kernel<8, 2>,
-            (const void *)moe::route::router_smallN_kernel<8, 4>, (const void *)moe::route::router_smallN_kernel<8, 8>,
-            (const void *)moe::route::router_smallN_kernel<16, 1>, (const void *)moe::route::router_smallN_kernel<16, 2>,
-            (const void *)moe::route::router_smallN_kernel<16, 4>, (const void *)moe::route::router_smallN_kernel<16, 8>};
-        for (const void *k : routers)
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)moe::route::kRouterSmemBudget + 1024);
         for (int lpl = 1; lpl <= 8; lpl <<= 1)
             for (int sp = 1; sp <= moe::rtc::kMaxSplits; sp <<= 1)
                 if (e == cudaSuccess)
@@ -416,7 +408,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
                      float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr,
-                     float *aux_kl = nullptr) {
+                     float *aux_kl = nullptr, float *health = nullptr, float *mean_weight = nullptr) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
     if (fused_route(s)) {
         const size_t zero_bytes = (size_t)(reinterpret_cast<char *>(w.done + 4) - reinterpret_cast<char *>(w.acc));
@@ -440,6 +432,9 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         p.topk_w = topk_w;
         p.prob_acc = w.acc;
         p.dem_acc = w.dem;
+        p.w_acc = w.wacc;
+        p.health = health;
+        p.mean_weight = mean_weight;
         p.done = w.done;
         p.lse_partial = w.lse_partial;
         p.demand = demand;
@@ -475,73 +470,46 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
     }
     const int splits = gate_splits(s);
     if (cudaMemsetAsync(demand, 0, sizeof(int32_t) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
-    int rows;
-    if (N <= kSmallGateMaxN) {
-        // gate + TopK + softmax + statistics in one kernel
-        rows = moe::route::small_router_grid(T);
-        const int thr = moe::route::kRouterWarps * 32;
-        const int stages = moe::route::small_router_stages(d);
-        const size_t smem = moe::route::small_router_smem(d);
-        const int cpw_needed = ((d / 8) + moe::route::kRouterWarps - 1) / moe::route::kRouterWarps;
-        const int jmax = cpw_needed <= 32 ? 1 : (cpw_needed <= 64 ? 2 : (cpw_needed <= 128 ? 4 : 8));
-#define MOE_ROUTER(NM, JM)                                                                                    \
-    moe::route::router_smallN_kernel<NM, JM><<<rows, thr, smem, st>>>(x, Wg, sel_bias, T, d, N, K, stages, \
-                                                                      topk_idx, topk_w, demand, w.partial, \
-                                                                      w.lse_partial)
-        if (N <= 8) {
-            if (jmax == 1) MOE_ROUTER(8, 1);
-            else if (jmax == 2) MOE_ROUTER(8, 2);
-            else if (jmax == 4) MOE_ROUTER(8, 4);
-            else MOE_ROUTER(8, 8);
-        } else {
-            if (jmax == 1) MOE_ROUTER(16, 1);
-            else if (jmax == 2) MOE_ROUTER(16, 2);
-            else if (jmax == 4) MOE_ROUTER(16, 4);
-            else MOE_ROUTER(16, 8);
-        }
-#undef MOE_ROUTER
-        count_launch();
+    if (cudaMemsetAsync(w.wacc, 0, sizeof(unsigned long long) * N, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tensor_gate(s)) {
+        // logits = x Wg^T on the tensor cores, raw fp32 K-split partials
+        moe_status g = launch_gemm(dev, false, x, (uint64_t)T, Wg, (uint64_t)N, d, N, 1, nullptr, nullptr, T,
+                                   nullptr, nullptr, 0, T, false, st, w.logits, splits);
+        if (g != MOE_OK) return g;
     } else {
-        if (tensor_gate(s)) {
-            // logits = x Wg^T on the tensor cores, raw fp32 K-split partials
-            moe_status g = launch_gemm(dev, false, x, (uint64_t)T, Wg, (uint64_t)N, d, N, 1, nullptr, nullptr, T,
-                                       nullptr, nullptr, 0, T, false, st, w.logits, splits);
-            if (g != MOE_OK) return g;
-        } else {
-            dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
-            moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N,
-                                                                                            w.logits);
-            count_launch();
-        }
-        rows = moe::route::topk_grid(T);
-        const size_t smem = (size_t)moe::route::kTopkWarps * N * sizeof(float) + (size_t)N * sizeof(int);
-        const int lpl = (N + 31) / 32;
-        const int thr = moe::route::kTopkWarps * 32;
-#define MOE_TOPK(L)                                                                                     \
-    moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, splits, sel_bias, T, N, K, topk_idx, \
-                                                                topk_w, demand, w.partial, w.lse_partial)
-        if (lpl <= 1) MOE_TOPK(1);
-        else if (lpl <= 2) MOE_TOPK(2);
-        else if (lpl <= 4) MOE_TOPK(4);
-        else if (lpl <= 8) MOE_TOPK(8);
-        else if (lpl <= 16) MOE_TOPK(16);
-        else MOE_TOPK(32);
-#undef MOE_TOPK
+        dim3 grid((T + moe::route::kGBM - 1) / moe::route::kGBM, (N + moe::route::kGBN - 1) / moe::route::kGBN);
+        moe::route::gate_logits_tiled_kernel<<<grid, moe::route::kGateThreads, 0, st>>>(x, Wg, T, d, N, w.logits);
         count_launch();
     }
-    if ((aux != nullptr || z_loss != nullptr || aux_kl != nullptr) &&
+    const int rows = moe::route::topk_grid(T);
+    const size_t smem = (size_t)N * sizeof(unsigned long long) + (size_t)moe::route::kTopkWarps * N * sizeof(float) +
+                        (size_t)N * sizeof(int);
+    const int lpl = (N + 31) / 32;
+    const int thr = moe::route::kTopkWarps * 32;
+#define MOE_TOPK(L)                                                                                     \
+    moe::route::topk_softmax_kernel<L><<<rows, thr, smem, st>>>(w.logits, splits, sel_bias, T, N, K, topk_idx, \
+                                                                topk_w, demand, w.partial, w.lse_partial, w.wacc)
+    if (lpl <= 1) MOE_TOPK(1);
+    else if (lpl <= 2) MOE_TOPK(2);
+    else if (lpl <= 4) MOE_TOPK(4);
+    else if (lpl <= 8) MOE_TOPK(8);
+    else if (lpl <= 16) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
+    count_launch();
+    if ((aux != nullptr || z_loss != nullptr || aux_kl != nullptr || health != nullptr || mean_weight != nullptr) &&
         cudaMemsetAsync(w.done, 0, sizeof(unsigned int), st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(w.partial, w.lse_partial, rows, N, T, K,
-                                                                      s->aux_alpha, s->z_beta, s->kl_coef, demand,
-                                                                      prob_sum, aux, z_loss, aux_kl, w.done);
+    moe::route::route_finalize_kernel<<<(N + 31) / 32, 1024, 0, st>>>(
+        w.partial, w.lse_partial, rows, N, T, K, s->aux_alpha, s->z_beta, s->kl_coef, demand, prob_sum, aux, z_loss,
+        aux_kl, w.wacc, health, mean_weight, w.done);
     count_launch();
     return launch_status();
 }
 
 moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint16_t *x, int32_t *kept,
                         int32_t *offsets, int32_t *slot_of, int32_t *row_token, uint16_t *x_perm,
-                        const DispatchWs &w, cudaStream_t st) {
+                        const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model;
     const int C = capacity_of(s);
     const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
@@ -551,7 +519,8 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
         return MOE_ERR_CUDA;
     moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, order, N, w.hist);
     count_launch();
-    moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets);
+    moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets,
+                                                                 drop_rate, T * K);
     count_launch();
     moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
         topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
@@ -1121,6 +1090,8 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     float *aux = o.aux ? o.aux : w.aux;
     float *z_loss = o.z_loss ? o.z_loss : w.aux + 1;
     float *aux_kl = o.aux_kl ? o.aux_kl : w.aux + 2;
+    float *health = o.health;
+    float *mean_weight = o.mean_weight;
 
     auto mark = [&](int i) -> bool {
         return events == nullptr || events[i] == nullptr ||
@@ -1128,10 +1099,11 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     };
     if (!mark(0)) return MOE_ERR_CUDA;
     if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
-                       st, z_loss, aux_kl)) != MOE_OK)
+                       st, z_loss, aux_kl, health, mean_weight)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
-    if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st)) != MOE_OK)
+    if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st,
+                          health ? health + 1 : nullptr)) != MOE_OK)
         return r;
     if (!mark(2)) return MOE_ERR_CUDA;
     cudaEvent_t mid = events ? reinterpret_cast<cudaEvent_t>(events[3]) : nullptr;

@@ -54,7 +54,7 @@ constexpr int kMaxN = 256;
 constexpr int kRefSMs = 148;               // the split choice assumes one wave on 148 SMs
 constexpr float kProbScale = 2147483648.0f;          // 2^31
 constexpr float kProbUnit = 1.0f / 2147483648.0f;    // 2^-31
-constexpr size_t kMaxSmem = 220 * 1024;
+constexpr size_t kMaxSmem = 214 * 1024;  // + the static block below stays within 227 KB
 
 // Partial-logit buffer [expert][token]: with one split the routing reads it
 // directly (odd stride: conflict-free across experts); with several, rows are
@@ -78,11 +78,12 @@ struct Params {
     // zeroed by the caller before the launch, contiguous
     unsigned long long *prob_acc;  // [N] sum_t softmax_N(s_t)[e] in 2^-31 units
     int32_t *dem_acc;              // [N] assignments per expert
+    unsigned long long *w_acc;     // [N] sum of the routing weights given to e, 2^-31 units
     unsigned int *done;            // finished-block ticket
-    float *lse_partial;            // [gridDim.x] per-block sum of logsumexp^2
+    float *lse_partial;            // [gridDim.x][4] per-block sums of logsumexp^2 and entropy, max |logit|
     // written by the last block (demand and prob_sum required)
     int32_t *demand;
-    float *prob_sum, *aux, *z_loss, *aux_kl;
+    float *prob_sum, *aux, *z_loss, *aux_kl, *health, *mean_weight;
     float alpha, beta, kl_coef;
 };
 
@@ -94,11 +95,13 @@ struct Shared {
     uint32_t tmem_base;
     volatile int abort_flag;
     int last;
-    float lsq_w[kWarps];
+    float lsq_w[kWarps], ent_w[kWarps], amax_w[kWarps];
     float bias[kMaxN];
-    route::KSum red[96];
+    route::KSum red[5 * 32];
+    float mred[32];
     int dcount[kMaxN];
     unsigned long long pacc[kMaxN];
+    unsigned long long wacc[kMaxN];
 };
 
 // Tiles, splits and shared memory of a launch: functions of (T, d, N) only.
@@ -242,6 +245,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     for (int e = threadIdx.x; e < N; e += kThreads) {
         sh.dcount[e] = 0;
         sh.pacc[e] = 0ull;
+        sh.wacc[e] = 0ull;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -399,7 +403,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int col0 = S == 1 ? r0 : 0;
         for (int e = threadIdx.x; e < N; e += kThreads) sh.bias[e] = p.sel_bias != nullptr ? p.sel_bias[e] : 0.f;
         __syncthreads();
-        float lsq = 0.f;
+        float lsq = 0.f, ent = 0.f, amax = 0.f;
         for (int i = threadIdx.x / G; i < RT && !sh.abort_flag; i += TPP) {
             // the loop bound is warp-uniform (RT is a multiple of the groups per
             // warp); tokens past T run along with zero logits and write nothing,
@@ -427,9 +431,24 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
             for (int o = G / 2; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
             const float inv_z = 1.f / z;
+            // routing entropy lse - sum_e p_e s_e and the logit range (health statistics)
+            float ps = 0.f, am = 0.f;
+#pragma unroll
+            for (int j = 0; j < EPT; ++j)
+                if (gl + G * j < N) {
+                    ps += ex[j] * sv[j];
+                    am = fmaxf(am, fabsf(sv[j]));
+                }
+#pragma unroll
+            for (int o = G / 2; o > 0; o >>= 1) {
+                ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            }
             if (gl == 0 && live) {
                 const float lse = m + logf(z);
                 lsq += lse * lse;
+                ent += lse - ps * inv_z;
+                amax = fmaxf(amax, am);
             }
             // this token's softmax probabilities replace its logits in the column
 #pragma unroll
@@ -492,17 +511,26 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         const bool ok = (unsigned)sel_e[k] < (unsigned)N;
                         p.topk_idx[(size_t)t * K + k] = ok ? sel_e[k] : -1;
                         p.topk_w[(size_t)t * K + k] = nu[k] / den;
-                        if (ok)
+                        if (ok) {
                             atomicAdd(&sh.dcount[sel_e[k]], 1);
-                        else
+                            atomicAdd(&sh.wacc[sel_e[k]], (unsigned long long)__float2uint_rn(nu[k] / den * kProbScale));
+                        } else
                             flag_error(MOE_DEVERR_EXPERT_ID);  // no orderable logit (NaN input)
                     }
                 }
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lsq += __shfl_xor_sync(0xffffffffu, lsq, o);
-        if (lane == 0) sh.lsq_w[warp] = lsq;
+        for (int o = 16; o > 0; o >>= 1) {
+            lsq += __shfl_xor_sync(0xffffffffu, lsq, o);
+            ent += __shfl_xor_sync(0xffffffffu, ent, o);
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        }
+        if (lane == 0) {
+            sh.lsq_w[warp] = lsq;
+            sh.ent_w[warp] = ent;
+            sh.amax_w[warp] = amax;
+        }
         __syncthreads();
         // per-expert sums of this block's probabilities, in fixed point
         const int nlive = sh.abort_flag ? 0 : max(0, min(RT, p.T - (m0 + r0)));
@@ -517,11 +545,18 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     for (int e = threadIdx.x; e < N; e += kThreads) {
         if (sh.pacc[e] != 0ull) atomicAdd(p.prob_acc + e, sh.pacc[e]);
         if (sh.dcount[e] != 0) atomicAdd(p.dem_acc + e, sh.dcount[e]);
+        if (sh.wacc[e] != 0ull) atomicAdd(p.w_acc + e, sh.wacc[e]);
     }
     if (threadIdx.x == 0) {
-        float a = 0.f;
-        for (int w = 0; w < kWarps; ++w) a += sh.lsq_w[w];
-        p.lse_partial[blockIdx.x] = a;
+        float a = 0.f, b = 0.f, c = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+            a += sh.lsq_w[w];
+            b += sh.ent_w[w];
+            c = fmaxf(c, sh.amax_w[w]);
+        }
+        p.lse_partial[(size_t)blockIdx.x * route::kPartialStride] = a;
+        p.lse_partial[(size_t)blockIdx.x * route::kPartialStride + 1] = b;
+        p.lse_partial[(size_t)blockIdx.x * route::kPartialStride + 2] = c;
     }
 
     // -------------------------------------------------------- last block: totals and losses
@@ -533,24 +568,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     __syncthreads();
     if (!sh.last) return;
     __threadfence();
-    const long long TK = (long long)p.T * K;
-    const float TKf = (float)TK, Tf = (float)p.T;
-    route::KSum a_aux, a_kl, a_z;
     for (int e = threadIdx.x; e < N; e += kThreads) {
-        const float ps = __ull2float_rn(__ldcg(p.prob_acc + e)) * kProbUnit;
-        const int de = __ldcg(p.dem_acc + e);
-        p.prob_sum[e] = ps;
-        p.demand[e] = de;
-        a_aux.add(route::aux_term(de, ps, TKf, Tf));
-        a_kl.add(route::kl_summand(de, TK, N));
+        p.prob_sum[e] = __ull2float_rn(__ldcg(p.prob_acc + e)) * kProbUnit;
+        p.demand[e] = __ldcg(p.dem_acc + e);
     }
-    for (int r = threadIdx.x; r < (int)gridDim.x; r += kThreads) a_z.add(__ldcg(p.lse_partial + r));
-    route::block_sum3(a_aux, a_kl, a_z, sh.red);
-    if (threadIdx.x == 0) {
-        if (p.aux != nullptr) p.aux[0] = p.alpha * (float)N * a_aux.value();
-        if (p.z_loss != nullptr) p.z_loss[0] = p.beta * (a_z.value() / (float)p.T);
-        if (p.aux_kl != nullptr) p.aux_kl[0] = p.kl_coef * a_kl.value();
-    }
+    __threadfence();
+    __syncthreads();
+    route::block_losses(N, p.T, K, p.demand, p.prob_sum, p.lse_partial, (int)gridDim.x, p.w_acc, p.alpha, p.beta,
+                        p.kl_coef, p.aux, p.z_loss, p.aux_kl, p.health, p.mean_weight, sh.red, sh.mred);
 }
 
 }  // namespace rtc

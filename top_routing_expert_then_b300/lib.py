@@ -58,7 +58,8 @@ class MoeGrads(ctypes.Structure):
 
 class MoeRouteOut(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "demand", "prob_sum", "kept",
-                                               "expert_offsets", "slot_of", "aux", "z_loss", "aux_kl")]
+                                               "expert_offsets", "slot_of", "aux", "z_loss", "aux_kl",
+                                               "health", "mean_weight")]
 
 
 _lib = None
@@ -328,6 +329,8 @@ class RouteOutputs:
     aux: torch.Tensor
     z_loss: torch.Tensor
     aux_kl: torch.Tensor
+    health: torch.Tensor
+    mean_weight: torch.Tensor
 
 
 class MoELayer:
@@ -354,7 +357,8 @@ class MoELayer:
                             torch.empty((N,), dtype=i32, device=dev), torch.empty((N,), dtype=f32, device=dev),
                             torch.empty((N,), dtype=i32, device=dev), torch.empty((N + 1,), dtype=i32, device=dev),
                             torch.empty((T, K), dtype=i32, device=dev), torch.empty((1,), dtype=f32, device=dev),
-                            torch.empty((1,), dtype=f32, device=dev), torch.empty((1,), dtype=f32, device=dev))
+                            torch.empty((1,), dtype=f32, device=dev), torch.empty((1,), dtype=f32, device=dev),
+                            torch.empty((4,), dtype=f32, device=dev), torch.empty((N,), dtype=f32, device=dev))
 
     @staticmethod
     def _out_struct(ro: Optional[RouteOutputs]):
@@ -362,7 +366,7 @@ class MoELayer:
             return None
         return ctypes.byref(MoeRouteOut(*(getattr(ro, n).data_ptr() for n in (
             "topk_idx", "topk_w", "demand", "prob_sum", "kept", "expert_offsets", "slot_of", "aux", "z_loss",
-            "aux_kl"))))
+            "aux_kl", "health", "mean_weight"))))
 
     def forward(self, x, sel_bias=None, y=None, route_out: Optional[RouteOutputs] = None, stream=None):
         s = self.shape
