@@ -138,6 +138,39 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same with an L2 eviction-priority policy (createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+#ifndef MOE_TMA_L2_HINTS
+#define MOE_TMA_L2_HINTS 0
+#endif
+// L2 policies for the operand loads: activations (A, re-read by every n-tile)
+// and weights (B, read by the m-tiles of one raster group at about the same
+// time, then dead). 0 = none; 1 = A evict_last, B evict_first; 2 = A
+// evict_last; 3 = B evict_first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Ask the TMA unit to pull a tile into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -355,12 +388,15 @@ __device__ __forceinline__ uint32_t a_tile_bytes(int rows) {
                                    : (uint32_t)((rows + A_CHUNK_ROWS - 1) / A_CHUNK_ROWS) * A_CHUNK_BYTES;
 }
 __device__ __forceinline__ void load_a_tile(uint32_t dst, const CUtensorMap *tmA, const CUtensorMap *tmA32,
-                                            uint32_t bar, int x, int row0, int rows) {
+                                            uint32_t bar, int x, int row0, int rows, uint64_t policy = 0) {
     if (rows > 3 * A_CHUNK_ROWS) {
-        tma_load_2d(dst, tmA, bar, x, row0);
+        if (policy) tma_load_2d_hint(dst, tmA, bar, x, row0, policy);
+        else tma_load_2d(dst, tmA, bar, x, row0);
     } else {
-        for (int c = 0; c * A_CHUNK_ROWS < rows; ++c)
-            tma_load_2d(dst + c * A_CHUNK_BYTES, tmA32, bar, x, row0 + c * A_CHUNK_ROWS);
+        for (int c = 0; c * A_CHUNK_ROWS < rows; ++c) {
+            if (policy) tma_load_2d_hint(dst + c * A_CHUNK_BYTES, tmA32, bar, x, row0 + c * A_CHUNK_ROWS, policy);
+            else tma_load_2d(dst + c * A_CHUNK_BYTES, tmA32, bar, x, row0 + c * A_CHUNK_ROWS);
+        }
     }
 }
 
@@ -415,6 +451,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
+            const uint64_t pol_a = (MOE_TMA_L2_HINTS == 1 || MOE_TMA_L2_HINTS == 2) ? l2_policy_evict_last() : 0;
+            const uint64_t pol_b = (MOE_TMA_L2_HINTS == 1 || MOE_TMA_L2_HINTS == 3) ? l2_policy_evict_first() : 0;
             uint32_t stage = 0, phase = 0;
             int issued_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
@@ -436,8 +474,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t fb = smem_u32(&sh->full[stage]);
                     uint8_t *a_s = smem + stage * STAGE_BYTES;
                     mbar_arrive_expect_tx(fb, a_tile_bytes(t.rows) + B_BYTES);
-                    load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, kb * BK, t.row0, t.rows);
-                    tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
+                    load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, kb * BK, t.row0, t.rows, pol_a);
+                    if (pol_b) tma_load_2d_hint(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow, pol_b);
+                    else tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
                     issued_phase[stage] = (int)phase;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -1143,7 +1182,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
 // The m-tile list of the routed experts, from the expert offsets:
 // expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / tile_rows)
-// tiles, cut into raster groups of at most `raster` tiles (see tile_of).
+// tiles, grouped for rasterisation (see tile_of).
 // One block of 1024 threads; N <= 1024; at most 65535 tiles.
 __global__ void __launch_bounds__(1024)
 build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int tile_rows, int raster,
@@ -1172,14 +1211,19 @@ build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, 
         __syncthreads();
     }
     const int start = v - cnt;
+    // raster groups stay inside expert e: all of its tiles in one group when
+    // there are at most 2 * raster of them (so an expert whose rows spill a
+    // few rows into one more tile does not stream its weights a second time),
+    // else ceil(cnt / raster) groups of balanced size
+    const int ng = cnt <= 2 * raster ? 1 : (cnt + raster - 1) / raster;
     for (int i = 0; i < cnt; ++i) {
         int m = start + i;
         if (m < max_tiles) {
             int rr = r0 + i * tile_rows;
             int rows = r1 - rr < tile_rows ? r1 - rr : tile_rows;
-            const int gfirst = start + (i / raster) * raster;   // raster groups stay inside expert e
-            const int gsize = min(raster, cnt - (i / raster) * raster);
-            mtiles[m] = make_int4(rr, rows, e, (gfirst << 16) | gsize);
+            const int g = ((i + 1) * ng - 1) / cnt;           // group of tile i
+            const int lo = (g * cnt) / ng, hi = ((g + 1) * cnt) / ng;
+            mtiles[m] = make_int4(rr, rows, e, ((start + lo) << 16) | (hi - lo));
         }
     }
     if (e == 1023) *num_mtiles = v < max_tiles ? v : max_tiles;
