@@ -310,6 +310,21 @@ MOE_API moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights 
 
 /* Reads (and, if clear != 0, resets) the device error word of the current
  * device. Synchronises the device. *code_out receives the MOE_DEVERR_* bits. */
+/* Host-to-host forward over a sequence of nbatch batches of T tokens with the
+ * transfers overlapped: batch i is read from x_host + i * host_stride and
+ * written to y_host + i * host_stride (host_stride in elements; 0 = the same
+ * host buffers for every batch); host buffers should be pinned. x_dev and
+ * y_dev each hold TWO device buffers of [T, d_model] bf16 (double buffering).
+ * The copies run on two copy streams owned by the library and are ordered
+ * against the forwards on `stream` with events, so batch i+1's input copy and
+ * batch i-1's output copy overlap batch i's forward. Asynchronous: every copy
+ * and forward has finished once `stream` has. One call at a time per device
+ * (a mutex serialises callers). workspace as for moe_forward. */
+MOE_API moe_status moe_forward_hostio_batches(const moe_shape *shape, const moe_weights *weights, int32_t nbatch,
+                                              const moe_bf16 *x_host, moe_bf16 *y_host, size_t host_stride,
+                                              const float *sel_bias, moe_bf16 *x_dev, moe_bf16 *y_dev,
+                                              void *workspace, size_t workspace_bytes, void *stream);
+
 /* Backward pass of the layer (training; the pages' sec. 5 training signal,
  * lmnt.cn/news/351908). Recomputes the forward for (x, sel_bias) and writes
  * the gradients of

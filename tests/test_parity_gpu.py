@@ -145,3 +145,25 @@ def test_full_size_parity(name):
         mean = cfg.T * cfg.K / cfg.N
         assert ref.demand[0] > 4 * mean and ref.demand[1] > 2 * mean
         assert (ref.slot_of < 0).sum() >= 8192
+
+
+def test_hostio_batches_match_forward():
+    """moe_forward_hostio_batches (overlapped copies, double-buffered device
+    buffers) gives, for every batch, the bytes moe_forward gives."""
+    cfg = MoEConfig("hostio_batches", 300, 128, 256, 8, 2, 1.25, has_shared=True)
+    inp = gpu_inputs(cfg, 4)
+    layer = lib.MoELayer.from_inputs(inp)
+    nb = 5
+    xs = torch.stack([(torch.randint(-128, 129, (cfg.T, cfg.d_model), device="cuda").float() / 64).to(torch.bfloat16)
+                      for _ in range(nb)])
+    x_host = xs.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    xd = torch.empty((2, cfg.T, cfg.d_model), dtype=torch.bfloat16, device="cuda")
+    yd = torch.empty_like(xd)
+    layer.forward_hostio_batches(x_host, y_host, nb, xd, yd)
+    torch.cuda.synchronize()
+    for i in range(nb):
+        ref = layer.forward(xs[i])
+        torch.cuda.synchronize()
+        assert torch.equal(y_host[i], ref.cpu()), i
+    assert lib.device_error() == 0

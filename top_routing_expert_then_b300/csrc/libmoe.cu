@@ -289,6 +289,12 @@ struct DeviceState {
     std::once_flag once;
     int num_sms = 0;
     cudaError_t init_err = cudaSuccess;
+    // batched host I/O: two copy streams and per-buffer events, created on first use
+    std::once_flag io_once;
+    cudaError_t io_err = cudaSuccess;
+    std::mutex io_mutex;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_fwd[2] = {}, ev_out[2] = {};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -1151,6 +1157,72 @@ moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights *weights
         return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+moe_status moe_forward_hostio_batches(const moe_shape *shape, const moe_weights *weights, int32_t nbatch,
+                                      const moe_bf16 *x_host, moe_bf16 *y_host, size_t host_stride,
+                                      const float *sel_bias, moe_bf16 *x_dev, moe_bf16 *y_dev, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+    moe_status r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (nbatch < 1 || !x_host || !y_host || !x_dev || !y_dev || !aligned16(x_dev) || !aligned16(y_dev))
+        return MOE_ERR_INVALID_ARG;
+    if (!weights_ok(shape, weights, true)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(shape, MOE_WS_FORWARD, workspace, workspace_bytes)) != MOE_OK) return r;
+    DeviceState *dev;
+    if ((r = device_state(&dev)) != MOE_OK) return r;
+    std::call_once(dev->io_once, [dev]() {
+        cudaError_t e = cudaStreamCreateWithFlags(&dev->h2d, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&dev->d2h, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dev->ev_start, cudaEventDisableTiming);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = cudaEventCreateWithFlags(&dev->ev_in[b], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dev->ev_fwd[b], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&dev->ev_out[b], cudaEventDisableTiming);
+        }
+        dev->io_err = e;
+    });
+    if (dev->io_err != cudaSuccess) return MOE_ERR_CUDA;
+    // one caller at a time per device: the copy streams and events are shared
+    std::lock_guard<std::mutex> lock(dev->io_mutex);
+    cudaStream_t st = as_stream(stream);
+    const size_t elems = (size_t)shape->T * shape->d_model, bytes = elems * sizeof(moe_bf16);
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // earlier work on `stream` may still use the device buffers
+    if (!ok(cudaEventRecord(dev->ev_start, st)) || !ok(cudaStreamWaitEvent(dev->h2d, dev->ev_start, 0)) ||
+        !ok(cudaStreamWaitEvent(dev->d2h, dev->ev_start, 0))) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+    }
+    for (int32_t i = 0; i < nbatch; ++i) {
+        const int b = i & 1;
+        moe_bf16 *xb = x_dev + (size_t)b * elems, *yb = y_dev + (size_t)b * elems;
+        // input copy into buffer b once batch i-2's forward has consumed it
+        if (i >= 2 && !ok(cudaStreamWaitEvent(dev->h2d, dev->ev_fwd[b], 0))) break;
+        if (!ok(cudaMemcpyAsync(xb, x_host + (size_t)i * host_stride, bytes, cudaMemcpyHostToDevice, dev->h2d)) ||
+            !ok(cudaEventRecord(dev->ev_in[b], dev->h2d)))
+            break;
+        // forward once the input has landed and batch i-2's output copy has left buffer b
+        if (!ok(cudaStreamWaitEvent(st, dev->ev_in[b], 0))) break;
+        if (i >= 2 && !ok(cudaStreamWaitEvent(st, dev->ev_out[b], 0))) break;
+        if ((r = moe_forward(shape, weights, xb, sel_bias, yb, nullptr, workspace, workspace_bytes, stream)) !=
+            MOE_OK)
+            return r;
+        if (!ok(cudaEventRecord(dev->ev_fwd[b], st))) break;
+        // output copy after the forward
+        if (!ok(cudaStreamWaitEvent(dev->d2h, dev->ev_fwd[b], 0)) ||
+            !ok(cudaMemcpyAsync(y_host + (size_t)i * host_stride, yb, bytes, cudaMemcpyDeviceToHost, dev->d2h)) ||
+            !ok(cudaEventRecord(dev->ev_out[b], dev->d2h)))
+            break;
+        if (i + 1 == nbatch) {
+            // `stream` completes after every copy
+            if (!ok(cudaStreamWaitEvent(st, dev->ev_out[b], 0))) break;
+            if (nbatch > 1 && !ok(cudaStreamWaitEvent(st, dev->ev_out[b ^ 1], 0))) break;
+            return launch_status();
+        }
+    }
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
 }
 
 moe_status moe_backward(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,

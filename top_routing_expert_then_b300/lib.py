@@ -100,6 +100,7 @@ def load():
                                 ctypes.POINTER(ctypes.c_void_p), P], i32),
         "moe_forward_hostio": ([S, ctypes.POINTER(MoeWeights), P, P, P, P, P, ctypes.POINTER(MoeRouteOut),
                                 P, sz, P], i32),
+        "moe_forward_hostio_batches": ([S, ctypes.POINTER(MoeWeights), i32, P, P, sz, P, P, P, P, sz, P], i32),
         "moe_backward": ([S, ctypes.POINTER(MoeWeights), P, P, P, ctypes.c_float, ctypes.c_float,
                           ctypes.POINTER(MoeGrads), P, sz, P], i32),
         "moe_get_device_error": ([i32, ctypes.POINTER(i32)], i32),
@@ -377,6 +378,25 @@ class MoELayer:
             _ptr(sel_bias, torch.float32, "sel_bias", s.N), _ptr(y, torch.bfloat16, "y", s.T * s.d_model),
             self._out_struct(route_out), self.ws.data_ptr(), self.ws.numel(), _stream(stream)))
         return y
+
+    def forward_hostio_batches(self, x_host, y_host, nbatch: int, x_dev, y_dev, sel_bias=None, same_host=False,
+                               stream=None):
+        """moe_forward_hostio_batches: nbatch host-to-host forwards with the copies
+        overlapped. x_host / y_host: pinned CPU bf16 tensors [nbatch, T, d] (or
+        [T, d] with same_host=True: every batch reuses them); x_dev / y_dev:
+        device bf16 tensors [2, T, d]."""
+        s = self.shape
+        td = s.T * s.d_model
+        for name, t in (("x_host", x_host), ("y_host", y_host)):
+            if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU bf16 tensor")
+            if t.numel() != (td if same_host else nbatch * td):
+                raise ValueError(f"{name} has {t.numel()} elements")
+        _check("moe_forward_hostio_batches", load().moe_forward_hostio_batches(
+            ctypes.byref(s), ctypes.byref(self.weights), int(nbatch), x_host.data_ptr(), y_host.data_ptr(),
+            0 if same_host else td, _ptr(sel_bias, torch.float32, "sel_bias", s.N),
+            _ptr(x_dev, torch.bfloat16, "x_dev", 2 * td), _ptr(y_dev, torch.bfloat16, "y_dev", 2 * td),
+            self.ws.data_ptr(), self.ws.numel(), _stream(stream)))
 
     def backward(self, x, dy, sel_bias=None, g_aux: float = 1.0, g_z: float = 1.0, ws=None, stream=None) -> dict:
         """moe_backward: fp32 gradients {dx, dWg, dW1, db1, dW2, db2, dw (+ dWs1, dbs1, dWs2, dbs2)} of
