@@ -50,6 +50,11 @@ SMALL = [
     # ragged expert, the shared expert, drops
     MoEConfig("fp8_experts", 700, 256, 640, 8, 2, 1.25, weights="fp8_e4m3"),
     MoEConfig("fp8_shared_bias", 300, 192, 320, 16, 4, 0.0, has_shared=True, sel_bias=True, weights="fp8_e4m3"),
+    # a few rows per expert (decode: MMA N = 16), three channel tiles
+    MoEConfig("fp8_decode_small", 24, 256, 384, 8, 2, 0.0, weights="fp8_e4m3"),
+    # several 128-row tiles per expert with a ragged last one, a half channel
+    # tile (192 = 128 + 64), an odd k-block count, the dense shared expert
+    MoEConfig("fp8_many_rows", 700, 128, 192, 2, 1, 0.0, has_shared=True, weights="fp8_e4m3"),
 ]
 
 

@@ -1,0 +1,462 @@
+// gemm_fp8t.cuh -- the grouped expert GEMM with weight-only FP8 expert
+// weights (E4M3 codes, one fp32 scale per output channel; the weight
+// quantisation of the lmnt.cn/news/351908 sec. 4.3 remark and the CSDN page's
+// sec. 3.2 one-byte FP8 weights), computed transposed so that the weights,
+// not the tokens, fill the 128 rows of the MMA:
+//
+//   out[r, n] = epilogue( scale[g(r), n] * sum_k code(B[g(r) * n_out + n, k]) * A[r, k] + bias[g(r), n] )
+//
+// A decode batch gives each expert a handful of rows, so a token-major tile
+// (128 token rows) would spend almost all of its MMA work on padding. Here one
+// tile is 128 output channels of one expert x up to 64 of its rows: the MMA
+// is D[channel, row] = sum_k W[channel, k] * A[row, k] with M = 128 channels
+// and N = the tile's row count rounded up to 16, so the tensor-core work
+// scales with the real rows and the kernel is left to stream the codes.
+//
+// The codes cross HBM as one byte per element and are widened to bf16 in
+// registers (exact: every E4M3 value is a bf16 value) and written straight
+// into tensor memory, which the MMA reads as its A operand (tcgen05.mma with
+// A in TMEM); only the raw codes and the token tiles pass through shared
+// memory. bf16 x bf16 products are exact in the fp32 accumulator; the
+// per-channel scale is applied in the epilogue, where it factors out of the
+// sum over k.
+//
+// The unit of the pipeline is a k-pair (128 reduction columns): one raw
+// stage of codes, one TMEM A stage, one token stage, 8 MMAs and one commit.
+// A narrow MMA is cheap, so the issuing thread's own instruction stream sets
+// the pace: few barrier operations per 8 MMAs keep it short, and waiting
+// warps sleep on their barrier instead of spinning for issue slots.
+//
+// Block = 15 warps, one block per SM, persistent over the tile list:
+//   warp 0     raw producer (one lane): TMA of 128 channels x 128 codes
+//              (128-byte swizzle) into a 7-deep ring
+//   warp 1     TMEM allocator + MMA issuer (one lane)
+//   warp 2     token producer (one lane): TMA of the tile's rows (16-row
+//              boxes, only the boxes that hold rows) x 64 bf16, two per stage
+//   warps 3-6  epilogue: accumulator lane = channel, column = row; scale,
+//              bias, GELU, bf16, stores (one 64-byte segment per row and warp)
+//   warps 7-14 converters: warp w owns TMEM lanes 32 (w % 4) .. +31 (the
+//              lanes its warp may address) and one k-block of each pair;
+//              lane = channel, 64 codes -> 32 TMEM columns per stage
+// TMEM: 6 A stages x 64 columns, then two 64-column accumulators.
+// Every wait is bounded (globaltimer); on a timeout the block sets
+// MOE_DEVERR_TIMEOUT, stops, drains its own copies and MMAs and frees TMEM.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "grouped_gemm.cuh"
+
+namespace moe {
+namespace gg {
+
+constexpr int QT_CH = 128;                      // output channels per tile (MMA M)
+constexpr int QT_ROWS = 64;                     // rows per tile at most (MMA N <= 64)
+constexpr int QT_RAW_K = 2 * BK;                // codes per raw row: 128 bytes
+constexpr int QT_RAW_BYTES = QT_CH * QT_RAW_K;  // 16 KB
+constexpr int QT_RSTAGES = 7;                   // raw ring: 7 k-pairs of codes in flight
+constexpr int QT_TBOX = 16;                     // token rows per TMA box
+constexpr int QT_TBOX_BYTES = QT_TBOX * BK * 2;       // 2 KB (two 1024-byte swizzle atoms)
+constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a full token tile
+constexpr int QT_TOK_BYTES = 2 * QT_TOK_HALF;         // a k-pair
+constexpr int QT_STAGES = 6;                    // A (TMEM) + token (shared) stages
+constexpr int QT_A_COLS = BK;                   // 128 bf16 per lane = 64 columns
+constexpr int QT_ACC_COL0 = QT_STAGES * QT_A_COLS;    // 384
+constexpr int QT_ACC_COLS = QT_ROWS;            // fp32 accumulator columns per buffer
+constexpr int QT_TMEM_COLS = 512;
+static_assert(QT_ACC_COL0 + 2 * QT_ACC_COLS <= QT_TMEM_COLS, "TMEM budget");
+constexpr int QT_CONVERTERS = 256;              // warps 7-14
+constexpr int QT_NUM_THREADS = 7 * 32 + QT_CONVERTERS;
+constexpr int QT_BAR_BYTES = 512;
+constexpr int QT_SMEM_BYTES = QT_RSTAGES * QT_RAW_BYTES + QT_STAGES * QT_TOK_BYTES + QT_BAR_BYTES + 1024;
+static_assert(QT_SMEM_BYTES <= 227 * 1024, "shared memory");
+
+struct QTShared {
+    uint64_t raw_full[QT_RSTAGES];
+    uint64_t raw_empty[QT_RSTAGES];
+    uint64_t a_full[QT_STAGES];    // the 8 converter warps wrote the stage's A columns
+    uint64_t tok_full[QT_STAGES];  // the stage's token boxes have landed
+    uint64_t empty[QT_STAGES];     // the MMAs reading the stage have completed
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(QTShared) <= QT_BAR_BYTES, "barrier block too large");
+
+// try_wait that lets the thread sleep up to `ns` while the phase is pending
+// (a waiting warp then takes no issue slots from the working ones)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __noinline__ bool qt_wait_slow(QTShared *sh, uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                          bool raise) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+        if ((it & 15u) == 15u) {
+            if (raise && sh->abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                if (raise) {
+                    sh->abort_flag = 1;
+                    flag_error(MOE_DEVERR_TIMEOUT);
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait with an inline fast path for a phase that has already completed.
+__device__ __forceinline__ bool qt_wait(QTShared *sh, uint32_t bar, uint32_t parity, uint64_t limit_ns, bool raise) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return qt_wait_slow(sh, bar, parity, limit_ns, raise);
+}
+
+// Two E4M3 codes -> two bf16, exactly. `sel` picks the two code bytes of w
+// into bits 0-7 and 16-23 and fills bits 8-15 and 24-31 with copies of each
+// code's sign bit (prmt's sign-replicating byte select). Shifted left by 4
+// and masked, each half is the bf16 pattern sign | (7 magnitude bits << 4):
+// 2^(E-127) (1 + M/8) for E >= 1 and the subnormal (M/8) 2^-126 for E = 0,
+// i.e. the E4M3 value times 2^-120 in every case; one packed bf16 multiply by
+// 2^120 (exact: at most 4 significant bits, no overflow, subnormals kept)
+// gives the E4M3 value with its sign. (E4M3 NaN, codes 0x7f / 0xff, come out
+// as +-480.)
+__device__ __forceinline__ uint32_t e4m3x2_bf16x2(uint32_t w, uint32_t sel) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "r"(sel));
+    uint32_t pat = (t << 4) & 0x87F087F0u;
+    const __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&pat);
+    const __nv_bfloat162 k120 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x7B80u),
+                                                   __ushort_as_bfloat16((unsigned short)0x7B80u));  // 2^120
+    const __nv_bfloat162 v = __hmul2(m, k120);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// 16 codes (one 16-byte chunk, memory order) -> 8 packed bf16 pairs.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &in, uint32_t *o) {
+    o[0] = e4m3x2_bf16x2(in.x, 0x9180u);
+    o[1] = e4m3x2_bf16x2(in.x, 0xB3A2u);
+    o[2] = e4m3x2_bf16x2(in.y, 0x9180u);
+    o[3] = e4m3x2_bf16x2(in.y, 0xB3A2u);
+    o[4] = e4m3x2_bf16x2(in.z, 0x9180u);
+    o[5] = e4m3x2_bf16x2(in.z, 0xB3A2u);
+    o[6] = e4m3x2_bf16x2(in.w, 0x9180u);
+    o[7] = e4m3x2_bf16x2(in.w, 0xB3A2u);
+}
+
+// This thread's lane of 32 consecutive TMEM columns.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// This thread's lane of 16 consecutive TMEM columns, read.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// D (TMEM) [+]= A (TMEM, 128 lanes x 16 bf16) * B (shared memory descriptor)^T.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(QT_NUM_THREADS, 1)
+grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmBq,
+                         const Params p, const float *__restrict__ wscale) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *rawbuf = smem;
+    uint8_t *tokbuf = rawbuf + QT_RSTAGES * QT_RAW_BYTES;
+    QTShared *sh = reinterpret_cast<QTShared *>(tokbuf + QT_STAGES * QT_TOK_BYTES);
+
+    const int warp = warp_id();
+    const int lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QT_RSTAGES; ++s) {
+            mbar_init(smem_u32(&sh->raw_full[s]), 1);
+            mbar_init(smem_u32(&sh->raw_empty[s]), QT_CONVERTERS / 32);
+        }
+        for (int s = 0; s < QT_STAGES; ++s) {
+            mbar_init(smem_u32(&sh->a_full[s]), QT_CONVERTERS / 32);
+            mbar_init(smem_u32(&sh->tok_full[s]), 1);
+            mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&sh->tfull[a]), 1);
+            mbar_init(smem_u32(&sh->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmT);
+        prefetch_tmap(&tmBq);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sh->tmem_base)),
+                     "r"(QT_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sh->tmem_base;
+
+    const int num_m = num_m_tiles<QT_ROWS>(p);
+    const int num_n = (p.n_out + QT_CH - 1) / QT_CH;
+    const int total = num_m * num_n;
+    const int kblocks = p.k_dim / BK;
+    const int kpairs = (kblocks + 1) / 2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ raw producer (codes)
+            int j = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                const int brow = t.group * p.n_out + t.n0;
+                for (int kp = 0; kp < kpairs; ++kp, ++j) {
+                    const int r = j % QT_RSTAGES;
+                    if (!qt_wait(sh, smem_u32(&sh->raw_empty[r]), ((uint32_t)(j / QT_RSTAGES) & 1u) ^ 1u,
+                                 WAIT_LIMIT_NS, true)) {
+                        stop = true;
+                        break;
+                    }
+                    // the second half of an odd k count's last pair reads zeros past k_dim;
+                    // channels past the tensor's last row read zeros too
+                    mbar_arrive_expect_tx(smem_u32(&sh->raw_full[r]), QT_RAW_BYTES);
+                    tma_load_2d(smem_u32(rawbuf + r * QT_RAW_BYTES), &tmBq, smem_u32(&sh->raw_full[r]),
+                                kp * QT_RAW_K, brow);
+                }
+            }
+            if (stop) {
+                for (int jj = max(0, j - QT_RSTAGES); jj < j; ++jj)
+                    qt_wait(sh, smem_u32(&sh->raw_full[jj % QT_RSTAGES]), (uint32_t)(jj / QT_RSTAGES) & 1u,
+                            DRAIN_LIMIT_NS, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ------------------------------------------------ token producer
+            int i = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                const int boxes = (t.rows + QT_TBOX - 1) / QT_TBOX;
+                for (int kp = 0; kp < kpairs; ++kp, ++i) {
+                    const int s = i % QT_STAGES;
+                    if (!qt_wait(sh, smem_u32(&sh->empty[s]), ((uint32_t)(i / QT_STAGES) & 1u) ^ 1u,
+                                 WAIT_LIMIT_NS, true)) {
+                        stop = true;
+                        break;
+                    }
+                    const int halves = (2 * kp + 1 < kblocks) ? 2 : 1;
+                    mbar_arrive_expect_tx(smem_u32(&sh->tok_full[s]), (uint32_t)(halves * boxes * QT_TBOX_BYTES));
+                    for (int h = 0; h < halves; ++h)
+                        for (int b = 0; b < boxes; ++b)
+                            tma_load_2d(smem_u32(tokbuf + s * QT_TOK_BYTES + h * QT_TOK_HALF + b * QT_TBOX_BYTES),
+                                        &tmT, smem_u32(&sh->tok_full[s]), (2 * kp + h) * BK, t.row0 + b * QT_TBOX);
+                }
+            }
+            if (stop) {
+                for (int ii = max(0, i - QT_STAGES); ii < i; ++ii)
+                    qt_wait(sh, smem_u32(&sh->tok_full[ii % QT_STAGES]), (uint32_t)(ii / QT_STAGES) & 1u,
+                            DRAIN_LIMIT_NS, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int i = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool stop = false;
+            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                if (!t.ok) continue;
+                const uint32_t ncols = (uint32_t)((t.rows + 15) & ~15);  // MMA N: 16 .. 64
+                const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((ncols >> 3) << 17) |
+                                       ((uint32_t)(QT_CH >> 4) << 24);
+                if (!qt_wait(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + QT_ACC_COL0 + acc * QT_ACC_COLS;
+                for (int kp = 0; kp < kpairs; ++kp, ++i) {
+                    const int s = i % QT_STAGES;
+                    const uint32_t ph = (uint32_t)(i / QT_STAGES) & 1u;
+                    if (!qt_wait(sh, smem_u32(&sh->a_full[s]), ph, WAIT_LIMIT_NS, true) ||
+                        !qt_wait(sh, smem_u32(&sh->tok_full[s]), ph, WAIT_LIMIT_NS, true)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem_base + s * QT_A_COLS;
+                    const uint32_t b_addr = smem_u32(tokbuf + s * QT_TOK_BYTES);
+                    if (2 * kp + 1 < kblocks) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2),
+                                        sdesc(b_addr + (kk >> 2) * QT_TOK_HALF + (kk & 3) * UMMA_K * 2), idesc,
+                                        (kp != 0 || kk != 0) ? 1u : 0u);
+                    } else {  // an odd k count's last pair: its first k-block only
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2), sdesc(b_addr + kk * UMMA_K * 2), idesc,
+                                        (kp != 0 || kk != 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&sh->empty[s]));
+                }
+                if (stop) break;
+                mma_commit(smem_u32(&sh->tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            mma_commit(smem_u32(&sh->drain));
+            qt_wait(sh, smem_u32(&sh->drain), 0, DRAIN_LIMIT_NS, false);
+        }
+        __syncwarp();
+    } else if (warp < 7) {
+        // ---------------------------------------------------- epilogue (warps 3-6)
+        const int q = warp & 3;
+        const int ch = q * 32 + lane;  // channel within the tile = accumulator lane
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+            if (!t.ok) {
+                if (threadIdx.x == 96) flag_error(MOE_DEVERR_TILE_LIST);
+                continue;
+            }
+            if (!qt_wait(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
+            tc_fence_after();
+            const int n = t.n0 + ch;
+            const bool live = n < p.n_out;
+            float scl = 0.f, b = 0.f;
+            if (live) {
+                scl = __ldg(wscale + (size_t)t.group * p.n_out + n);
+                b = __ldg(p.bias + (size_t)t.group * p.n_out + n);
+            }
+            uint16_t *outc = p.out + (size_t)t.row0 * p.n_out + n;
+            const uint32_t tbase = tmem_base + QT_ACC_COL0 + acc * QT_ACC_COLS + ((uint32_t)(q * 32) << 16);
+            for (int c0 = 0; c0 < t.rows; c0 += 16) {  // t.rows is warp-uniform
+                uint32_t r[16];
+                tmem_ld16(tbase + c0, r);
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j < t.rows) {
+                            float v = fmaf(__uint_as_float(r[j]), scl, b);
+                            if (p.gelu) v = gelu_erf(v);
+                            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                            outc[(size_t)(c0 + j) * p.n_out] = *reinterpret_cast<const uint16_t *>(&h);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // ---------------------------------------------------- converters (warps 7-14)
+        const int q = warp & 3;            // TMEM lane quarter this warp may address
+        const int half = (warp - 7) >> 2;  // which k-block of each pair
+        const int ch = q * 32 + lane;      // channel = raw row = TMEM lane
+        const uint8_t *rrow = rawbuf + ch * QT_RAW_K;
+        const int sw = ch & 7;             // the 128-byte swizzle of the raw tile
+        const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + half * (BK / 2);
+        int i = 0;  // k-pairs converted (= raw stages consumed)
+        bool stop = false;
+        for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+            const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+            if (!t.ok) continue;
+            for (int kp = 0; kp < kpairs; ++kp, ++i) {
+                const int r = i % QT_RSTAGES, s = i % QT_STAGES;
+                if (!qt_wait(sh, smem_u32(&sh->raw_full[r]), (uint32_t)(i / QT_RSTAGES) & 1u, WAIT_LIMIT_NS,
+                             true)) {
+                    stop = true;
+                    break;
+                }
+                const uint8_t *src = rrow + r * QT_RAW_BYTES;
+                uint32_t v[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = half * 4 + c;  // 16-byte chunks of this k-block in the raw row
+                    const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
+                    e4m3x16_to_bf16(in, v + 8 * c);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh->raw_empty[r]));
+                if (!qt_wait(sh, smem_u32(&sh->empty[s]), ((uint32_t)(i / QT_STAGES) & 1u) ^ 1u, WAIT_LIMIT_NS,
+                             true)) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                tmem_st32(tlane + s * QT_A_COLS, v);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh->a_full[s]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(QT_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+}  // namespace gg
+}  // namespace moe

@@ -19,6 +19,7 @@
 #include "route.cuh"
 #include "route_tc.cuh"
 #include "gemm_fp8w.cuh"
+#include "gemm_fp8t.cuh"
 #include "backward.cuh"
 
 namespace {
@@ -80,8 +81,10 @@ int capacity_of(const moe_shape *s) {
     return (int)c;
 }
 
+// Capacity of the device tile list: m-tiles of 64 rows (the FP8 kernel's
+// height; the bf16 kernels' 128- and 256-row tiles need fewer).
 int max_mtiles(const moe_shape *s) {
-    return (int)(((int64_t)s->T * s->K + BM - 1) / BM) + s->N;
+    return (int)(((int64_t)s->T * s->K + 63) / 64) + s->N;
 }
 
 // ------------------------------------------------------------------ workspace layouts
@@ -337,6 +340,9 @@ moe_status device_state(DeviceState **out) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8w_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::Q_SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8t_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::QT_SMEM_BYTES);
         for (int lpl = 1; lpl <= 8; lpl <<= 1)
             for (int sp = 1; sp <= moe::rtc::kMaxSplits; sp <<= 1)
                 if (e == cudaSuccess)
@@ -389,17 +395,19 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, u
     return r == CUDA_SUCCESS;
 }
 
-// Row-major one-byte [rows, cols] tensor (FP8 codes), no swizzle: box_rows x
-// box_cols bytes land densely, rows box_cols bytes apart.
+// Row-major one-byte [rows, cols] tensor (FP8 codes): box_rows x box_cols
+// bytes land densely, rows box_cols bytes apart; with swizzle128 (box_cols =
+// 128) the 16-byte chunks of row r are permuted by r % 8 as for bf16 tiles.
 bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                  uint32_t box_cols) {
+                  uint32_t box_cols, bool swizzle128 = false) {
     if (!get_encoder()) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -630,17 +638,20 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     return MOE_OK;
 }
 
-// The grouped GEMM with FP8 expert weights (gemm_fp8w.cuh): A bf16 [a_rows,
-// k_dim], Bq codes [groups * n_out, k_dim], scale [groups * n_out].
-moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, const void *Bq, uint64_t b_rows,
-                           int k_dim, int n_out, int groups, const float *scale, const float *bias, uint16_t *out,
-                           int out_rows, const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows,
-                           bool gelu, cudaStream_t st) {
-    CUtensorMap ta, tb, tc, ta32;
-    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, moe::gg::BM)) return MOE_ERR_CUDA;
-    if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
-    if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::BN, moe::gg::Q_RAW_K)) return MOE_ERR_CUDA;
-    if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
+// FP8 expert GEMM variant: the channel-major kernel (gemm_fp8t.cuh, weights
+// widened into tensor memory, default) or the token-major one (gemm_fp8w.cuh,
+// weights widened into shared memory), MOE_FP8_GEMM=token_major
+// (environment, read once).
+bool fp8_token_major() {
+    static const bool v = []() {
+        const char *e = std::getenv("MOE_FP8_GEMM");
+        return e != nullptr && std::strcmp(e, "token_major") == 0;
+    }();
+    return v;
+}
+
+moe::gg::Params fp8_params(int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
+                           const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu) {
     moe::gg::Params p{};
     p.mtiles = mtiles;
     p.num_mtiles = num_mtiles;
@@ -656,6 +667,39 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
     p.out_f32 = nullptr;
     p.k_splits = 1;
     p.raster = kRasterSingle;
+    return p;
+}
+
+// The grouped GEMM with FP8 expert weights: A bf16 [a_rows, k_dim], Bq codes
+// [groups * n_out, k_dim], scale [groups * n_out].
+moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, const void *Bq, uint64_t b_rows,
+                           int k_dim, int n_out, int groups, const float *scale, const float *bias, uint16_t *out,
+                           int out_rows, const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows,
+                           bool gelu, cudaStream_t st) {
+    if (!fp8_token_major()) {
+        CUtensorMap tt, tb;
+        if (!make_tmap(&tt, A, a_rows, (uint64_t)k_dim, moe::gg::QT_TBOX)) return MOE_ERR_CUDA;
+        if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::QT_CH, moe::gg::QT_RAW_K, true))
+            return MOE_ERR_CUDA;
+        const moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles,
+                                             max_tiles, dense_rows, gelu);
+        const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::QT_ROWS - 1) / moe::gg::QT_ROWS;
+        const int64_t work = (int64_t)m_upper * ((n_out + moe::gg::QT_CH - 1) / moe::gg::QT_CH);
+        int grid = dev->num_sms;
+        if (work < grid) grid = (int)work;
+        if (grid < 1) grid = 1;
+        moe::gg::grouped_gemm_fp8t_kernel<<<grid, moe::gg::QT_NUM_THREADS, moe::gg::QT_SMEM_BYTES, st>>>(tt, tb, p,
+                                                                                                     scale);
+        count_launch();
+        return MOE_OK;
+    }
+    CUtensorMap ta, tb, tc, ta32;
+    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, moe::gg::BM)) return MOE_ERR_CUDA;
+    if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
+    if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::BN, moe::gg::Q_RAW_K)) return MOE_ERR_CUDA;
+    if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
+    const moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles, max_tiles,
+                                         dense_rows, gelu);
     const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::BM - 1) / moe::gg::BM;
     const int64_t work = (int64_t)m_upper * ((n_out + moe::gg::BN - 1) / moe::gg::BN);
     int grid = dev->num_sms;
@@ -679,8 +723,9 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     const bool fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
     const bool pair_routed = !fp8 && use_pair(per_expert);
     const bool pair_shared = !fp8 && use_pair(T);
-    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows,
-                                                     pair_routed ? moe::gg::PAIR_BM : moe::gg::BM,
+    const int tile_rows = fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
+                              : (pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
+    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, tile_rows,
                                                      pair_routed ? kRasterPair : kRasterSingle, mt, w.mtiles,
                                                      w.num_mtiles);
     count_launch();
