@@ -27,10 +27,11 @@
 // the pace: few barrier operations per 8 MMAs keep it short, and waiting
 // warps sleep on their barrier instead of spinning for issue slots.
 //
-// Block = 15 warps, one block per SM, persistent over the tile list:
+// Block = 16 warps, one block per SM, persistent over the tile list:
 //   warp 0     raw producer (one lane): TMA of 128 channels x 128 codes
 //              (128-byte swizzle) into a 7-deep ring
-//   warp 1     TMEM allocator + MMA issuer (one lane)
+//   warps 1,15 TMEM allocator (warp 1) + two MMA issuers (one lane each):
+//              even k-pairs into one accumulator, odd into another
 //   warp 2     token producer (one lane): TMA of the tile's rows (16-row
 //              boxes, only the boxes that hold rows) x 64 bf16, two per stage
 //   warps 3-6  epilogue: accumulator lane = channel, column = row; scale,
@@ -38,7 +39,8 @@
 //   warps 7-14 converters: warp w owns TMEM lanes 32 (w % 4) .. +31 (the
 //              lanes its warp may address) and one k-block of each pair;
 //              lane = channel, 64 codes -> 32 TMEM columns per stage
-// TMEM: 6 A stages x 64 columns, then two 64-column accumulators.
+// TMEM: 4 A stages x 64 columns, then two buffers of two 64-column
+// accumulators (one per issuer), summed in the epilogue.
 // Every wait is bounded (globaltimer); on a timeout the block sets
 // MOE_DEVERR_TIMEOUT, stops, drains its own copies and MMAs and frees TMEM.
 #pragma once
@@ -60,14 +62,15 @@ constexpr int QT_TBOX = 16;                     // token rows per TMA box
 constexpr int QT_TBOX_BYTES = QT_TBOX * BK * 2;       // 2 KB (two 1024-byte swizzle atoms)
 constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a full token tile
 constexpr int QT_TOK_BYTES = 2 * QT_TOK_HALF;         // a k-pair
-constexpr int QT_STAGES = 6;                    // A (TMEM) + token (shared) stages
+constexpr int QT_STAGES = 4;                    // A (TMEM) + token (shared) stages
 constexpr int QT_A_COLS = BK;                   // 128 bf16 per lane = 64 columns
-constexpr int QT_ACC_COL0 = QT_STAGES * QT_A_COLS;    // 384
-constexpr int QT_ACC_COLS = QT_ROWS;            // fp32 accumulator columns per buffer
+constexpr int QT_ACC_COL0 = QT_STAGES * QT_A_COLS;    // 256
+constexpr int QT_ACC_COLS = QT_ROWS;            // fp32 columns of one issuer's accumulator
 constexpr int QT_TMEM_COLS = 512;
-static_assert(QT_ACC_COL0 + 2 * QT_ACC_COLS <= QT_TMEM_COLS, "TMEM budget");
+static_assert(QT_ACC_COL0 + 4 * QT_ACC_COLS <= QT_TMEM_COLS, "TMEM budget");
 constexpr int QT_CONVERTERS = 256;              // warps 7-14
-constexpr int QT_NUM_THREADS = 7 * 32 + QT_CONVERTERS;
+constexpr int QT_ISSUER2 = 15;                  // the second MMA issuer warp
+constexpr int QT_NUM_THREADS = 16 * 32;
 constexpr int QT_BAR_BYTES = 512;
 constexpr int QT_SMEM_BYTES = QT_RSTAGES * QT_RAW_BYTES + QT_STAGES * QT_TOK_BYTES + QT_BAR_BYTES + 1024;
 static_assert(QT_SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -78,9 +81,9 @@ struct QTShared {
     uint64_t a_full[QT_STAGES];    // the 8 converter warps wrote the stage's A columns
     uint64_t tok_full[QT_STAGES];  // the stage's token boxes have landed
     uint64_t empty[QT_STAGES];     // the MMAs reading the stage have completed
-    uint64_t tfull[2];
+    uint64_t tfull[2][2];          // [accumulator buffer][issuer]
     uint64_t tempty[2];
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -219,10 +222,11 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             mbar_init(smem_u32(&sh->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(smem_u32(&sh->tfull[a]), 1);
+            mbar_init(smem_u32(&sh->tfull[a][0]), 1);
+            mbar_init(smem_u32(&sh->tfull[a][1]), 1);
             mbar_init(smem_u32(&sh->tempty[a]), 4);
+            mbar_init(smem_u32(&sh->drain[a]), 1);
         }
-        mbar_init(smem_u32(&sh->drain), 1);
         sh->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -308,9 +312,13 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == QT_ISSUER2) {
         if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+            // ------------------------------------------------ MMA issuers
+            // Issuer e takes the k-pairs kp = e, e + 2, ... of every tile into
+            // its own accumulator: a narrow MMA costs its issuing thread more
+            // time than the tensor core, and two issuers overlap.
+            const int e = warp == 1 ? 0 : 1;
             int i = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
@@ -322,8 +330,9 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                                        ((uint32_t)(QT_CH >> 4) << 24);
                 if (!qt_wait(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + QT_ACC_COL0 + acc * QT_ACC_COLS;
+                const uint32_t d_tmem = tmem_base + QT_ACC_COL0 + (2 * acc + e) * QT_ACC_COLS;
                 for (int kp = 0; kp < kpairs; ++kp, ++i) {
+                    if ((kp & 1) != e) continue;
                     const int s = i % QT_STAGES;
                     const uint32_t ph = (uint32_t)(i / QT_STAGES) & 1u;
                     if (!qt_wait(sh, smem_u32(&sh->a_full[s]), ph, WAIT_LIMIT_NS, true) ||
@@ -339,24 +348,25 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                         for (int kk = 0; kk < 8; ++kk)
                             mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2),
                                         sdesc(b_addr + (kk >> 2) * QT_TOK_HALF + (kk & 3) * UMMA_K * 2), idesc,
-                                        (kp != 0 || kk != 0) ? 1u : 0u);
+                                        (kp != e || kk != 0) ? 1u : 0u);
                     } else {  // an odd k count's last pair: its first k-block only
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2), sdesc(b_addr + kk * UMMA_K * 2), idesc,
-                                        (kp != 0 || kk != 0) ? 1u : 0u);
+                                        (kp != e || kk != 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&sh->empty[s]));
                 }
                 if (stop) break;
-                mma_commit(smem_u32(&sh->tfull[acc]));
+                // (an issuer without pairs in this tile commits nothing new: the arrival is immediate)
+                mma_commit(smem_u32(&sh->tfull[acc][e]));
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
-            mma_commit(smem_u32(&sh->drain));
-            qt_wait(sh, smem_u32(&sh->drain), 0, DRAIN_LIMIT_NS, false);
+            mma_commit(smem_u32(&sh->drain[e]));
+            qt_wait(sh, smem_u32(&sh->drain[e]), 0, DRAIN_LIMIT_NS, false);
         }
         __syncwarp();
     } else if (warp < 7) {
@@ -370,7 +380,9 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 if (threadIdx.x == 96) flag_error(MOE_DEVERR_TILE_LIST);
                 continue;
             }
-            if (!qt_wait(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
+            if (!qt_wait(sh, smem_u32(&sh->tfull[acc][0]), acc_phase, WAIT_LIMIT_NS, true) ||
+                !qt_wait(sh, smem_u32(&sh->tfull[acc][1]), acc_phase, WAIT_LIMIT_NS, true))
+                break;
             tc_fence_after();
             const int n = t.n0 + ch;
             const bool live = n < p.n_out;
@@ -380,15 +392,23 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 b = __ldg(p.bias + (size_t)t.group * p.n_out + n);
             }
             uint16_t *outc = p.out + (size_t)t.row0 * p.n_out + n;
-            const uint32_t tbase = tmem_base + QT_ACC_COL0 + acc * QT_ACC_COLS + ((uint32_t)(q * 32) << 16);
+            const uint32_t tbase = tmem_base + QT_ACC_COL0 + 2 * acc * QT_ACC_COLS + ((uint32_t)(q * 32) << 16);
             for (int c0 = 0; c0 < t.rows; c0 += 16) {  // t.rows is warp-uniform
                 uint32_t r[16];
+                float sum[16];
                 tmem_ld16(tbase + c0, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sum[j] = __uint_as_float(r[j]);
+                if (kpairs > 1) {  // the second issuer's accumulator (odd k-pairs)
+                    tmem_ld16(tbase + QT_ACC_COLS + c0, r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sum[j] += __uint_as_float(r[j]);
+                }
                 if (live) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < t.rows) {
-                            float v = fmaf(__uint_as_float(r[j]), scl, b);
+                            float v = fmaf(sum[j], scl, b);
                             if (p.gelu) v = gelu_erf(v);
                             const __nv_bfloat16 h = __float2bfloat16_rn(v);
                             outc[(size_t)(c0 + j) * p.n_out] = *reinterpret_cast<const uint16_t *>(&h);
@@ -404,7 +424,7 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 acc_phase ^= 1u;
             }
         }
-    } else {
+    } else if (warp < 7 + QT_CONVERTERS / 32) {
         // ---------------------------------------------------- converters (warps 7-14)
         const int q = warp & 3;            // TMEM lane quarter this warp may address
         const int half = (warp - 7) >> 2;  // which k-block of each pair
