@@ -397,8 +397,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(cfg, {"kept_rows": R, "parallelism": f"replicas{world}"}),
-        "roofline": {"kernel": ("grouped_gemm_fp8w_kernel (both expert Linears, FP8 weights widened in shared "
-                                "memory, tcgen05)") if fp8 else "grouped_gemm_kernel (both expert Linears, tcgen05)",
+        "roofline": {"kernel": ("grouped_gemm_fp8t_kernel (both expert Linears, FP8 weights widened into tensor "
+                                "memory, channel-major tcgen05)") if fp8 else
+                               "grouped_gemm_kernel (both expert Linears, tcgen05)",
                      "bound": "tensor" if tensor_bound else "hbm",
                      "achieved": achieved_tflops if tensor_bound else achieved_gbs,
                      "peak": peak_t if tensor_bound else P["hbm_gbs"],

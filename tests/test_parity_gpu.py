@@ -55,6 +55,9 @@ SMALL = [
     # several 128-row tiles per expert with a ragged last one, a half channel
     # tile (192 = 128 + 64), an odd k-block count, the dense shared expert
     MoEConfig("fp8_many_rows", 700, 128, 192, 2, 1, 0.0, has_shared=True, weights="fp8_e4m3"),
+    # decode-sized batch: split-K over the k-pairs with an odd k-block count
+    # (192 = 3 x 64, 320 = 5 x 64), the shared expert split too
+    MoEConfig("fp8_split_k", 40, 192, 320, 4, 2, 0.0, has_shared=True, sel_bias=True, weights="fp8_e4m3"),
 ]
 
 

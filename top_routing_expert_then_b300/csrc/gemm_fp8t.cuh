@@ -29,7 +29,7 @@
 //
 // Block = 16 warps, one block per SM, persistent over the tile list:
 //   warp 0     raw producer (one lane): TMA of 128 channels x 128 codes
-//              (128-byte swizzle) into a 7-deep ring
+//              (128-byte swizzle) into a 10-deep ring
 //   warps 1,15 TMEM allocator (warp 1) + two MMA issuers (one lane each):
 //              even k-pairs into one accumulator, odd into another
 //   warp 2     token producer (one lane): TMA of the tile's rows (16-row
@@ -41,6 +41,10 @@
 //              lane = channel, 64 codes -> 32 TMEM columns per stage
 // TMEM: 4 A stages x 64 columns, then two buffers of two 64-column
 // accumulators (one per issuer), summed in the epilogue.
+// Split-K (few rows, so that 148 SMs get equal shares): work item = (tile,
+// range of k-pairs); each split writes its raw fp32 sums to its own plane and
+// fp8_split_finalize_kernel adds the planes in a fixed order and applies the
+// scale, bias and GELU.
 // Every wait is bounded (globaltimer); on a timeout the block sets
 // MOE_DEVERR_TIMEOUT, stops, drains its own copies and MMAs and frees TMEM.
 #pragma once
@@ -57,7 +61,7 @@ constexpr int QT_CH = 128;                      // output channels per tile (MMA
 constexpr int QT_ROWS = 64;                     // rows per tile at most (MMA N <= 64)
 constexpr int QT_RAW_K = 2 * BK;                // codes per raw row: 128 bytes
 constexpr int QT_RAW_BYTES = QT_CH * QT_RAW_K;  // 16 KB
-constexpr int QT_RSTAGES = 7;                   // raw ring: 7 k-pairs of codes in flight
+constexpr int QT_RSTAGES = 10;                  // raw ring: 10 k-pairs of codes in flight
 constexpr int QT_TBOX = 16;                     // token rows per TMA box
 constexpr int QT_TBOX_BYTES = QT_TBOX * BK * 2;       // 2 KB (two 1024-byte swizzle atoms)
 constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a full token tile
@@ -198,6 +202,14 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Work item -> tile: the bf16 kernels' raster order with 128-channel n-tiles
+// (tile_of numbers n-tiles in units of its own 256-column width).
+__device__ __forceinline__ Tile qt_tile(const Params &p, int w, int num_m, int num_n) {
+    Tile t = tile_of<QT_ROWS>(p, w, num_m, num_n);
+    t.n0 = (t.n0 / BN) * QT_CH;
+    return t;
+}
+
 __global__ void __launch_bounds__(QT_NUM_THREADS, 1)
 grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmBq,
                          const Params p, const float *__restrict__ wscale) {
@@ -247,9 +259,14 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
 
     const int num_m = num_m_tiles<QT_ROWS>(p);
     const int num_n = (p.n_out + QT_CH - 1) / QT_CH;
-    const int total = num_m * num_n;
+    const int splits = p.out_f32 != nullptr && p.k_splits > 1 ? p.k_splits : 1;
+    const int total = num_m * num_n * splits;
     const int kblocks = p.k_dim / BK;
     const int kpairs = (kblocks + 1) / 2;
+    // work item w: tile w / splits, k-pairs [split_k0(w), split_k0(w + 1)) of it
+    // (the last split of a tile ends at kpairs); kpairs * splits < 2^31
+    auto split_k0 = [&](int w) { return (w % splits) * kpairs / splits; };
+    auto split_k1 = [&](int w) { return (w % splits + 1) * kpairs / splits; };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -257,10 +274,11 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             int j = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                const Tile t = qt_tile(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int brow = t.group * p.n_out + t.n0;
-                for (int kp = 0; kp < kpairs; ++kp, ++j) {
+                const int k1 = split_k1(w);
+                for (int kp = split_k0(w); kp < k1; ++kp, ++j) {
                     const int r = j % QT_RSTAGES;
                     if (!qt_wait(sh, smem_u32(&sh->raw_empty[r]), ((uint32_t)(j / QT_RSTAGES) & 1u) ^ 1u,
                                  WAIT_LIMIT_NS, true)) {
@@ -287,10 +305,11 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             int i = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                const Tile t = qt_tile(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int boxes = (t.rows + QT_TBOX - 1) / QT_TBOX;
-                for (int kp = 0; kp < kpairs; ++kp, ++i) {
+                const int k1 = split_k1(w);
+                for (int kp = split_k0(w); kp < k1; ++kp, ++i) {
                     const int s = i % QT_STAGES;
                     if (!qt_wait(sh, smem_u32(&sh->empty[s]), ((uint32_t)(i / QT_STAGES) & 1u) ^ 1u,
                                  WAIT_LIMIT_NS, true)) {
@@ -323,7 +342,7 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-                const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+                const Tile t = qt_tile(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const uint32_t ncols = (uint32_t)((t.rows + 15) & ~15);  // MMA N: 16 .. 64
                 const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((ncols >> 3) << 17) |
@@ -331,8 +350,9 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 if (!qt_wait(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + QT_ACC_COL0 + (2 * acc + e) * QT_ACC_COLS;
-                for (int kp = 0; kp < kpairs; ++kp, ++i) {
-                    if ((kp & 1) != e) continue;
+                const int k0 = split_k0(w), k1 = split_k1(w);
+                for (int kp = k0; kp < k1; ++kp, ++i) {
+                    if (((kp - k0) & 1) != e) continue;
                     const int s = i % QT_STAGES;
                     const uint32_t ph = (uint32_t)(i / QT_STAGES) & 1u;
                     if (!qt_wait(sh, smem_u32(&sh->a_full[s]), ph, WAIT_LIMIT_NS, true) ||
@@ -348,12 +368,12 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                         for (int kk = 0; kk < 8; ++kk)
                             mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2),
                                         sdesc(b_addr + (kk >> 2) * QT_TOK_HALF + (kk & 3) * UMMA_K * 2), idesc,
-                                        (kp != e || kk != 0) ? 1u : 0u);
+                                        (kp != k0 + e || kk != 0) ? 1u : 0u);
                     } else {  // an odd k count's last pair: its first k-block only
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2), sdesc(b_addr + kk * UMMA_K * 2), idesc,
-                                        (kp != e || kk != 0) ? 1u : 0u);
+                                        (kp != k0 + e || kk != 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&sh->empty[s]));
                 }
@@ -375,7 +395,7 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
         const int ch = q * 32 + lane;  // channel within the tile = accumulator lane
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+            const Tile t = qt_tile(p, w / splits, num_m, num_n);
             if (!t.ok) {
                 if (threadIdx.x == 96) flag_error(MOE_DEVERR_TILE_LIST);
                 continue;
@@ -385,6 +405,7 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 break;
             tc_fence_after();
             const int n = t.n0 + ch;
+            const int k0 = split_k0(w), k1 = split_k1(w);
             const bool live = n < p.n_out;
             float scl = 0.f, b = 0.f;
             if (live) {
@@ -397,21 +418,30 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 uint32_t r[16];
                 float sum[16];
                 tmem_ld16(tbase + c0, r);
+                const bool none = k1 == k0;  // an empty split (not launched so; zeros if it were)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) sum[j] = __uint_as_float(r[j]);
-                if (kpairs > 1) {  // the second issuer's accumulator (odd k-pairs)
+                for (int j = 0; j < 16; ++j) sum[j] = none ? 0.f : __uint_as_float(r[j]);
+                if (k1 - k0 > 1) {  // the second issuer's accumulator (odd k-pairs)
                     tmem_ld16(tbase + QT_ACC_COLS + c0, r);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) sum[j] += __uint_as_float(r[j]);
                 }
                 if (live) {
+                    // split mode: raw partial sums of this split (scale, bias, GELU come after)
+                    float *part = splits > 1 ? p.out_f32 + ((size_t)(w % splits) * p.out_rows + t.row0) * p.n_out + n
+                                             : nullptr;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         if (c0 + j < t.rows) {
-                            float v = fmaf(sum[j], scl, b);
-                            if (p.gelu) v = gelu_erf(v);
-                            const __nv_bfloat16 h = __float2bfloat16_rn(v);
-                            outc[(size_t)(c0 + j) * p.n_out] = *reinterpret_cast<const uint16_t *>(&h);
+                            const size_t off = (size_t)(c0 + j) * p.n_out;
+                            if (part != nullptr) {
+                                part[off] = sum[j];
+                            } else {
+                                float v = fmaf(sum[j], scl, b);
+                                if (p.gelu) v = gelu_erf(v);
+                                const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                                outc[off] = *reinterpret_cast<const uint16_t *>(&h);
+                            }
                         }
                     }
                 }
@@ -435,9 +465,10 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
         int i = 0;  // k-pairs converted (= raw stages consumed)
         bool stop = false;
         for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
-            const Tile t = tile_of<QT_ROWS, QT_CH>(p, w, num_m, num_n);
+            const Tile t = qt_tile(p, w / splits, num_m, num_n);
             if (!t.ok) continue;
-            for (int kp = 0; kp < kpairs; ++kp, ++i) {
+            const int k1 = split_k1(w);
+            for (int kp = split_k0(w); kp < k1; ++kp, ++i) {
                 const int r = i % QT_RSTAGES, s = i % QT_STAGES;
                 if (!qt_wait(sh, smem_u32(&sh->raw_full[r]), (uint32_t)(i / QT_RSTAGES) & 1u, WAIT_LIMIT_NS,
                              true)) {
@@ -475,6 +506,57 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(QT_TMEM_COLS)
                      : "memory");
+    }
+}
+
+// Split-K finalize: out[r, n] = epilogue( scale[g(r), n] * sum_s part[s, r, n] + bias[g(r), n] ),
+// the splits added in order. Block (x, y) = row x, columns
+// [1024 y, 1024 y + 1024); g(r) from the expert offsets (offsets = nullptr:
+// one group); rows past the last expert's block were not computed and are
+// skipped.
+__global__ void __launch_bounds__(256)
+fp8_split_finalize_kernel(const float *__restrict__ part, int splits, int rows, int n_out,
+                          const int32_t *__restrict__ offsets, int groups, const float *__restrict__ scale,
+                          const float *__restrict__ bias, int gelu, uint16_t *__restrict__ out) {
+    const int r = blockIdx.x;
+    if (r >= rows) return;
+    int g = 0;
+    if (offsets != nullptr) {
+        if (r >= offsets[groups]) return;
+        int lo = 0, hi = groups;  // largest g with offsets[g] <= r
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (offsets[mid] <= r) lo = mid;
+            else hi = mid;
+        }
+        g = lo;
+    }
+    const size_t plane = (size_t)rows * n_out;
+    const float *pr = part + (size_t)r * n_out;
+    const float *sc = scale + (size_t)g * n_out;
+    const float *bi = bias + (size_t)g * n_out;
+    uint16_t *o = out + (size_t)r * n_out;
+    const int n = blockIdx.y * 1024 + threadIdx.x * 4;
+    if (n < n_out) {  // n_out is a multiple of 64
+        float4 acc = *reinterpret_cast<const float4 *>(pr + n);
+        for (int s = 1; s < splits; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(pr + s * plane + n);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const float4 c = *reinterpret_cast<const float4 *>(sc + n);
+        const float4 b = *reinterpret_cast<const float4 *>(bi + n);
+        float y0 = fmaf(acc.x, c.x, b.x), y1 = fmaf(acc.y, c.y, b.y);
+        float y2 = fmaf(acc.z, c.z, b.z), y3 = fmaf(acc.w, c.w, b.w);
+        if (gelu) {
+            y0 = gelu_erf(y0);
+            y1 = gelu_erf(y1);
+            y2 = gelu_erf(y2);
+            y3 = gelu_erf(y3);
+        }
+        *reinterpret_cast<uint2 *>(o + n) = make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
     }
 }
 

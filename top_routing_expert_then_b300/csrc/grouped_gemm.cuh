@@ -289,7 +289,7 @@ __device__ __forceinline__ int num_m_tiles(const Params &p) {
 // work on a few experts' n-tiles at once and share their B (weight) tiles.
 // Each m-tile entry carries its group as (m_j << 16) | g_j in .w; the dense
 // mode (one group of rows) computes the same grouping arithmetically.
-template <int TM, int TN = BN>
+template <int TM>
 __device__ __forceinline__ Tile tile_of(const Params &p, int w, int num_m, int num_n) {
     const int q = w / num_n;  // an m-tile of the group that owns item w
     int mj, gj;
@@ -321,7 +321,7 @@ __device__ __forceinline__ Tile tile_of(const Params &p, int w, int num_m, int n
         t.rows = v.y;
         t.group = v.z;
     }
-    t.n0 = n * TN;
+    t.n0 = n * BN;
     t.ok = t.rows > 0 && t.rows <= TM && t.row0 >= 0 && t.row0 + t.rows <= p.out_rows &&
            t.group >= 0 && t.group < p.num_groups && n < num_n;
     return t;

@@ -164,11 +164,17 @@ DispatchWs carve_dispatch(Carve &c, const moe_shape *s) {
     return w;
 }
 
+// FP8 split-K partial sums: batches of at most kSplitRows routed rows (decode)
+// get kMaxFp8Splits fp32 planes of [rows, max(d_ff, d_model)].
+constexpr int kSplitRows = 128;
+constexpr int kMaxFp8Splits = 4;
+
 struct FfnWs {
     int4 *mtiles;
     int *num_mtiles;
     uint16_t *H;
     uint16_t *Hs;
+    float *part;  // nullptr: no split-K
 };
 FfnWs carve_ffn(Carve &c, const moe_shape *s) {
     FfnWs w;
@@ -176,6 +182,10 @@ FfnWs carve_ffn(Carve &c, const moe_shape *s) {
     w.num_mtiles = c.take<int>(4);
     w.H = c.take<uint16_t>((size_t)s->T * s->K * s->d_ff);
     w.Hs = s->has_shared ? c.take<uint16_t>((size_t)s->T * s->d_ff) : nullptr;
+    const int64_t rows = (int64_t)s->T * s->K;
+    w.part = rows <= kSplitRows
+                 ? c.take<float>((size_t)kMaxFp8Splits * rows * (size_t)std::max(s->d_ff, s->d_model))
+                 : nullptr;
     return w;
 }
 
@@ -672,25 +682,65 @@ moe::gg::Params fp8_params(int k_dim, int n_out, int groups, const float *bias, 
 
 // The grouped GEMM with FP8 expert weights: A bf16 [a_rows, k_dim], Bq codes
 // [groups * n_out, k_dim], scale [groups * n_out].
+// Split count for the channel-major FP8 GEMM: the S (<= kMaxFp8Splits, each
+// split at least one k-pair) that minimises the busiest SM's time,
+// ceil(units / SMs) * (ceil(pairs / S) + kFp8ItemOverhead), for the expected
+// m-tile count; the smaller S on ties. The per-item overhead (about four
+// k-pairs' time) is measured: Mixtral-shaped decode with 4 splits took 6%
+// longer on the first GEMM (32 k-pairs per tile) and 3% less on the second
+// (112 k-pairs per tile) than without.
+constexpr int kFp8ItemOverhead = 4;
+int fp8_splits(int m_est, int n_tiles, int kpairs, int num_sms) {
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int S = 1; S <= kMaxFp8Splits && S <= kpairs; ++S) {
+        const int64_t units = (int64_t)m_est * n_tiles * S;
+        const int64_t cost = ((units + num_sms - 1) / num_sms) * ((kpairs + S - 1) / S + kFp8ItemOverhead);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
 moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, const void *Bq, uint64_t b_rows,
                            int k_dim, int n_out, int groups, const float *scale, const float *bias, uint16_t *out,
                            int out_rows, const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows,
-                           bool gelu, cudaStream_t st) {
+                           bool gelu, cudaStream_t st, float *part = nullptr, const int32_t *offsets = nullptr) {
     if (!fp8_token_major()) {
         CUtensorMap tt, tb;
         if (!make_tmap(&tt, A, a_rows, (uint64_t)k_dim, moe::gg::QT_TBOX)) return MOE_ERR_CUDA;
         if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::QT_CH, moe::gg::QT_RAW_K, true))
             return MOE_ERR_CUDA;
-        const moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles,
-                                             max_tiles, dense_rows, gelu);
+        moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles, max_tiles,
+                                       dense_rows, gelu);
+        const int n_tiles = (n_out + moe::gg::QT_CH - 1) / moe::gg::QT_CH;
+        const int kpairs = (k_dim / moe::gg::BK + 1) / 2;
         const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::QT_ROWS - 1) / moe::gg::QT_ROWS;
-        const int64_t work = (int64_t)m_upper * ((n_out + moe::gg::QT_CH - 1) / moe::gg::QT_CH);
+        int splits = 1;
+        if (part != nullptr && out_rows <= kSplitRows) {
+            // routed rows: about one m-tile per expert that receives rows
+            const int m_est = mtiles ? std::min(groups, out_rows) : m_upper;
+            splits = fp8_splits(m_est, n_tiles, kpairs, dev->num_sms);
+        }
+        if (splits > 1) {
+            p.out_f32 = part;
+            p.k_splits = splits;
+        }
+        const int64_t work = (int64_t)m_upper * n_tiles * splits;
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
         moe::gg::grouped_gemm_fp8t_kernel<<<grid, moe::gg::QT_NUM_THREADS, moe::gg::QT_SMEM_BYTES, st>>>(tt, tb, p,
                                                                                                      scale);
         count_launch();
+        if (splits > 1) {
+            const dim3 fgrid((unsigned)out_rows, (unsigned)((n_out + 1023) / 1024));
+            moe::gg::fp8_split_finalize_kernel<<<fgrid, 256, 0, st>>>(part, splits, out_rows, n_out, offsets,
+                                                                         groups, scale, bias, gelu ? 1 : 0, out);
+            count_launch();
+        }
         return MOE_OK;
     }
     CUtensorMap ta, tb, tc, ta32;
@@ -733,20 +783,20 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     if (fp8) {
         // the same four GEMMs with FP8 expert weights and per-channel scales
         r = launch_gemm_fp8(dev, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->b1, w.H, rows, w.mtiles,
-                            w.num_mtiles, mt, 0, true, st);
+                            w.num_mtiles, mt, 0, true, st, w.part, offsets);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
             r = launch_gemm_fp8(dev, x, T, wt->Ws1q, f, d, f, 1, wt->ss1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T,
-                                true, st);
+                                true, st, w.part);
             if (r != MOE_OK) return r;
         }
         if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
         r = launch_gemm_fp8(dev, w.H, rows, wt->W2q, (uint64_t)N * d, f, d, N, wt->s2, wt->b2, y_perm, rows, w.mtiles,
-                            w.num_mtiles, mt, 0, false, st);
+                            w.num_mtiles, mt, 0, false, st, w.part, offsets);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
             r = launch_gemm_fp8(dev, w.Hs, T, wt->Ws2q, d, f, d, 1, wt->ss2, wt->bs2, z, T, nullptr, nullptr, 0, T,
-                                false, st);
+                                false, st, w.part);
             if (r != MOE_OK) return r;
         }
         return launch_status();
