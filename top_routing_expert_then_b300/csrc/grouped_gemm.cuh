@@ -552,12 +552,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             if (!wait_bounded(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
             tc_fence_after();
-            const bool store = row < t.rows;
             const int rows_valid = max(0, min(32, t.rows - q * 32));
             uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
-            float *out32_row = p.out_f32 == nullptr
-                                   ? nullptr
-                                   : p.out_f32 + ((size_t)(w % splits) * p.out_rows + (t.row0 + row)) * p.n_out;
             const float *bias = p.bias + (size_t)t.group * p.n_out;
             const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -565,19 +561,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (col >= p.n_out) break;  // warp-uniform
                 uint32_t r[32];
                 tmem_ld32(tbase + c0, r);
-                if (out32_row != nullptr) {
-                    // fp32 mode: n_out is a multiple of 4, columns past it are not stored
-                    const int ncols = min(32, p.n_out - col);
-                    if (p.k_ranges && p.k_ranges[w % splits] == p.k_ranges[w % splits + 1]) {
+                if (p.out_f32 != nullptr) {
+                    // fp32 mode: the warp's 32 x 32 block is turned in its shared-memory
+                    // buffer (element (i, j) at word 32 i + (j ^ i): conflict-free both
+                    // ways) so that each store instruction writes 128 contiguous bytes
+                    // of one row; columns past n_out (a multiple of 4) are not stored
+                    const bool empty = p.k_ranges && p.k_ranges[w % splits] == p.k_ranges[w % splits + 1];
+                    uint32_t *tb = reinterpret_cast<uint32_t *>(ebuf);  // 4 KB: both of the warp's buffers
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = 0u;  // nothing accumulated
-                    }
-                    if (store) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(out32_row + col);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (4 * j < ncols) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    }
+                    for (int j = 0; j < 32; ++j) tb[lane * 32 + (j ^ lane)] = empty ? 0u : r[j];  // nothing accumulated
+                    __syncwarp();
+                    float *base = p.out_f32 + ((size_t)(w % splits) * p.out_rows + (t.row0 + q * 32)) * p.n_out + col;
+                    const bool colok = lane < p.n_out - col;
+                    for (int i = 0; i < rows_valid; ++i)
+                        if (colok) base[(size_t)i * p.n_out + lane] = __uint_as_float(tb[i * 32 + (lane ^ i)]);
+                    __syncwarp();
                     continue;
                 }
                 uint32_t packed[16];

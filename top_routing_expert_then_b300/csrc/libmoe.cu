@@ -861,8 +861,9 @@ moe_status transpose_grouped(const uint16_t *in, int R, int C, const int32_t *of
 }
 
 moe_status batched_transpose(const uint16_t *in, int G, int A, int B, uint16_t *out, cudaStream_t st) {
-    dim3 grid((B + 31) / 32, (A + 31) / 32, G);
-    moe::bwd::batched_transpose_kernel<<<grid, moe::bwd::kThreads, 0, st>>>(in, A, B, out);
+    if (A % moe::bwd::kTT != 0 || B % moe::bwd::kTT != 0) return MOE_ERR_UNSUPPORTED;  // d, d_ff: multiples of 64
+    dim3 grid(B / moe::bwd::kTT, A / moe::bwd::kTT, G);
+    moe::bwd::batched_transpose_kernel<<<grid, 256, 0, st>>>(in, A, B, out);
     count_launch();
     return launch_status();
 }
