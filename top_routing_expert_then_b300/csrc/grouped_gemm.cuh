@@ -562,20 +562,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 uint32_t r[32];
                 tmem_ld32(tbase + c0, r);
                 if (p.out_f32 != nullptr) {
-                    // fp32 mode: the warp's 32 x 32 block is turned in its shared-memory
-                    // buffer (element (i, j) at word 32 i + (j ^ i): conflict-free both
-                    // ways) so that each store instruction writes 128 contiguous bytes
-                    // of one row; columns past n_out (a multiple of 4) are not stored
+                    // fp32 mode (raw accumulators of split w % splits). A full 32-row
+                    // block goes row-major into the warp's 4 KB buffer with the
+                    // 128-byte swizzle (conflict-free) and out with one TMA store
+                    // (tmC is then the fp32 map of all split planes); an expert's
+                    // last partial block is turned in the buffer (element (i, j) at
+                    // word 32 i + (j ^ i)) and stored row by row, 128 contiguous
+                    // bytes per instruction. Columns past n_out are not stored.
                     const bool empty = p.k_ranges && p.k_ranges[w % splits] == p.k_ranges[w % splits + 1];
-                    uint32_t *tb = reinterpret_cast<uint32_t *>(ebuf);  // 4 KB: both of the warp's buffers
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();  // the previous store has finished reading the buffer
+                    if (rows_valid == 32) {
+                        uint8_t *rowp = ebuf + lane * 128;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) tb[lane * 32 + (j ^ lane)] = empty ? 0u : r[j];  // nothing accumulated
-                    __syncwarp();
-                    float *base = p.out_f32 + ((size_t)(w % splits) * p.out_rows + (t.row0 + q * 32)) * p.n_out + col;
-                    const bool colok = lane < p.n_out - col;
-                    for (int i = 0; i < rows_valid; ++i)
-                        if (colok) base[(size_t)i * p.n_out + lane] = __uint_as_float(tb[i * 32 + (lane ^ i)]);
-                    __syncwarp();
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(rowp + ((c ^ (lane & 7)) << 4)) =
+                                empty ? make_uint4(0u, 0u, 0u, 0u)  // nothing accumulated
+                                      : make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, smem_u32(ebuf), col, (w % splits) * p.out_rows + t.row0 + q * 32);
+                            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                        }
+                    } else {
+                        uint32_t *tb = reinterpret_cast<uint32_t *>(ebuf);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) tb[lane * 32 + (j ^ lane)] = empty ? 0u : r[j];
+                        __syncwarp();
+                        float *base =
+                            p.out_f32 + ((size_t)(w % splits) * p.out_rows + (t.row0 + q * 32)) * p.n_out + col;
+                        const bool colok = lane < p.n_out - col;
+                        for (int i = 0; i < rows_valid; ++i)
+                            if (colok) base[(size_t)i * p.n_out + lane] = __uint_as_float(tb[i * 32 + (lane ^ i)]);
+                        __syncwarp();
+                    }
                     continue;
                 }
                 uint32_t packed[16];

@@ -405,6 +405,21 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, u
     return r == CUDA_SUCCESS;
 }
 
+// Row-major fp32 [rows, cols] tensor (cols a multiple of 4): the raw
+// accumulator planes the fp32 GEMM mode stores, 32 x 32 boxes with the
+// 128-byte swizzle its epilogue buffers use.
+bool make_tmap_f32(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Row-major one-byte [rows, cols] tensor (FP8 codes): box_rows x box_cols
 // bytes land densely, rows box_cols bytes apart; with swizzle128 (box_cols =
 // 128) the 16-byte chunks of row r are permuted by r % 8 as for bf16 tiles.
@@ -601,8 +616,12 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
     if (out != nullptr) {
         if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
+    } else if (out_f32 != nullptr) {
+        // fp32 mode: every split's plane, [k_splits * out_rows, n_out]
+        if (!make_tmap_f32(&tc, out_f32, (uint64_t)k_splits * (uint64_t)out_rows, (uint64_t)n_out))
+            return MOE_ERR_CUDA;
     } else {
-        tc = ta;  // fp32 mode: the epilogue stores directly and never reads this map
+        return MOE_ERR_INVALID_ARG;
     }
     moe::gg::Params p{};
     p.mtiles = mtiles;
