@@ -44,6 +44,15 @@
  *    trap: the offending element is skipped and a bit is set in a device error
  *    word that moe_get_device_error reads.
  *  - Inputs must be finite. Results on NaN or Inf inputs are unspecified.
+ *  - Kernel variants (environment variables read once per process; every
+ *    variant computes the same function and passes the same parity tests,
+ *    the defaults are the measured fastest): MOE_GEMM_VARIANT=pair (bf16
+ *    expert GEMM on SM pairs, cta_group::2, 256-row tiles) or share_a (2-CTA
+ *    clusters sharing the token tile by TMA multicast); MOE_ROUTE_VARIANT=
+ *    legacy (gate GEMM + TopK + finalize kernels for every N instead of the
+ *    fused router for N <= 256); MOE_FP8_GEMM=token_major (FP8 expert GEMM
+ *    with token rows as the MMA's M and the weights widened in shared memory
+ *    instead of the channel-major kernel).
  */
 #ifndef MOE_H
 #define MOE_H
