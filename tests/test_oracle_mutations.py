@@ -18,6 +18,14 @@ MUTATIONS = [
                                 "dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (sdw - dw_out[(size_t)t * K + k]);")]),
     ("aux_grad_not_centred", [("((double)demand[e] / TK - fp)", "((double)demand[e] / TK)")]),
     ("dW2_from_preactivation", [("dW2e[(size_t)c * f + j] += dO[c] * h[j];", "dW2e[(size_t)c * f + j] += dO[c] * a[j];")]),
+    ("dx_without_shared_expert", [("double acc = dx_shared ? dx_shared[(size_t)t * d + i] : 0.0;", "double acc = 0.0;")]),
+    ("dx_without_gate_term", [("acc += dst[e] * bf16_val(Wg[(size_t)e * d + i]);", "acc += 0.0 * dst[e];")]),
+    ("z_grad_without_lse", [("+ g_z * 2.0 * beta / (double)T * lse * p;", "+ g_z * 2.0 * beta / (double)T * p;")]),
+    ("dWg_from_gate_weights", [("dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);",
+                                "dWg[(size_t)e * d + i] += g * bf16_val(Wg[(size_t)e * d + i]);")]),
+    ("health_drop_rate_inverted", [("h[1] = 1.0 - kept_all / TK;", "h[1] = kept_all / TK;")]),
+    ("health_mean_weight_over_kept", [("mean_w[e] = demand[e] > 0 ? mean_w[e] / (double)demand[e] : 0.0;",
+                                       "mean_w[e] = kept[e] > 0 ? mean_w[e] / (double)kept[e] : 0.0;")]),
     ("fp8_exponent_bias", [("v = ldexp(1.0 + (double)man / 8.0, ex - 7);", "v = ldexp(1.0 + (double)man / 8.0, ex - 8);")]),
     ("fp8_subnormal_as_normal", [("v = ldexp((double)man, -9);", "v = ldexp(1.0 + (double)man / 8.0, -7);")]),
     ("fp8_scale_first_row_only", [("* (double)m->scale[row];", "* (double)m->scale[0];")]),
