@@ -37,6 +37,8 @@ SMALL = [
     MoEConfig("rank_major_drops", 1000, 256, 512, 16, 4, 1.0, rank_major=True),
     MoEConfig("rank_major_skewed", 2048, 256, 192, 64, 2, 1.0, zipf=True, rank_major=True),
     MoEConfig("rank_major_ties", 300, 128, 128, 8, 3, 0.5, rank_major=True),
+    # one dispatch chunk (the single-block dispatch kernel), rank order with drops
+    MoEConfig("rank_major_small", 40, 128, 128, 8, 3, 0.5, rank_major=True),
     # fused tensor-core router: N padded to 16 (37 -> 48, 200 -> 208), several
     # lanes per warp (N = 128, 200), more tiles than one wave (T = 20000: one
     # split, two blocks per SM)

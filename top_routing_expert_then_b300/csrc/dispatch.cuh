@@ -129,6 +129,81 @@ assign_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int C, const
     }
 }
 
+// The count, scan and assign kernels in one launch, for a dispatch of at most
+// kChunk virtual tokens (decode batches): one block of kChunk threads, with
+// the same counts, the same exclusive scan of the kept counts (one warp,
+// ceil(N / 32) experts per lane) and the same positions
+// p = popc of the earlier warps' and lanes' bits, so every output is the one
+// the three kernels write; row_token is filled with -1 first.
+__global__ void __launch_bounds__(kChunk)
+dispatch_small_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int C, int32_t *__restrict__ kept,
+                      int32_t *__restrict__ offsets, int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token,
+                      float *__restrict__ drop_rate, int total) {
+    extern __shared__ int sh[];  // cnt[N], off[N + 1], bits[4][N]
+    int *cnt = sh;
+    int *off = sh + N;
+    unsigned *bits = reinterpret_cast<unsigned *>(sh + 2 * N + 1);
+    for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = 0;
+    for (int i = threadIdx.x; i < 4 * N; i += blockDim.x) bits[i] = 0u;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) row_token[i] = -1;
+    __syncthreads();
+    const int w = warp_id(), lane = lane_id();
+    const int v = threadIdx.x;
+    if (v < o.tv()) {
+        for (int j = 0; j < o.kv(); ++j) {
+            const int e = topk_idx[o.entry(v, j)];
+            if (e >= 0 && e < N) {
+                atomicAdd(&cnt[e], 1);
+                atomicOr(&bits[w * N + e], 1u << lane);
+            } else {
+                flag_error(MOE_DEVERR_EXPERT_ID);
+            }
+        }
+    }
+    __syncthreads();
+    if (w == 0) {
+        const int per = (N + 31) / 32, e0 = min(N, lane * per), e1 = min(N, e0 + per);
+        int sum = 0;
+        for (int e = e0; e < e1; ++e) sum += min(cnt[e], C);
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += t;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < e1; ++e) {
+            const int k = min(cnt[e], C);
+            kept[e] = k;
+            off[e] = run;
+            offsets[e] = run;
+            run += k;
+        }
+        if (lane == 31) {
+            offsets[N] = incl;
+            if (drop_rate != nullptr) drop_rate[0] = (float)((double)(total - incl) / (double)total);
+        }
+    }
+    __syncthreads();
+    if (v >= o.tv()) return;
+    const unsigned below = (1u << lane) - 1u;
+    for (int j = 0; j < o.kv(); ++j) {
+        const int ent = o.entry(v, j);
+        const int e = topk_idx[ent];
+        int slot = -1;
+        if (e >= 0 && e < N) {
+            int p = 0;
+            for (int w2 = 0; w2 < w; ++w2) p += __popc(bits[w2 * N + e]);
+            p += __popc(bits[w * N + e] & below);
+            if (p < C) {
+                slot = off[e] + p;
+                row_token[slot] = o.token(v);
+            }
+        }
+        slot_of[ent] = slot;
+    }
+}
+
 // Tokens per block in the permute and combine kernels: a thread owns one
 // 16-byte column chunk of kRowTok consecutive tokens, so one block issues all
 // of its loads after a single round trip for the dispatch table.

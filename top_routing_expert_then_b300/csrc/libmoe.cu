@@ -554,16 +554,24 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
     const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
     const int chunks = moe::dispatch::num_chunks(order.rank_major ? T * K : T);
     const int rows = T * K;
-    if (cudaMemsetAsync(row_token, 0xFF, sizeof(int32_t) * (size_t)rows, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, order, N, w.hist);
-    count_launch();
-    moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets,
-                                                                 drop_rate, T * K);
-    count_launch();
-    moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
-        topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
-    count_launch();
+    if (chunks == 1) {
+        // a decode-sized batch: count, scan and assign in one block
+        moe::dispatch::dispatch_small_kernel<<<1, moe::dispatch::kChunk, (6 * (size_t)N + 1) * sizeof(int), st>>>(
+            topk_idx, order, N, C, kept, offsets, slot_of, row_token, drop_rate, rows);
+        count_launch();
+    } else {
+        if (cudaMemsetAsync(row_token, 0xFF, sizeof(int32_t) * (size_t)rows, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, order, N,
+                                                                                            w.hist);
+        count_launch();
+        moe::dispatch::scan_kernel<<<1, 1024, N * sizeof(int), st>>>(w.hist, chunks, N, C, w.base, kept, offsets,
+                                                                     drop_rate, rows);
+        count_launch();
+        moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
+            topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
+        count_launch();
+    }
     {
         const int vec = d / 8;
         const int thr = vec < 256 ? 64 : 256;
