@@ -400,28 +400,44 @@ __device__ __forceinline__ float block_max(float v, float *scratch /* 32 */) {
 //   health[3] = max |logit|  (lmnt sec. 8.2 / 9.3 routing monitors;
 //               health[1], the drop rate, is written by the dispatch)
 //   mean_weight[e] = mean routing weight of the assignments to e (0 if none)
-__device__ void block_losses(int N, int T, int K, const int32_t *demand, const float *prob_sum,
-                             const float *partials, int rows, const unsigned long long *w_acc, float alpha,
-                             float beta, float kl_coef, float *aux, float *z_loss, float *aux_kl, float *health,
-                             float *mean_weight, KSum *scratch /* 5 x 32 */, float *mscratch /* 32 */) {
+// With prob_acc / dem_acc given (the fused router's fixed-point totals),
+// prob_sum[e] = prob_acc[e] * prob_unit and demand[e] = dem_acc[e] are
+// computed here and written out; otherwise demand and prob_sum are read.
+// The per-block partial rows are loaded first, so that their loads and the
+// per-expert ones are in flight together.
+__device__ void block_losses(int N, int T, int K, int32_t *demand, float *prob_sum, const float *partials,
+                             int rows, const unsigned long long *w_acc, float alpha, float beta, float kl_coef,
+                             float *aux, float *z_loss, float *aux_kl, float *health, float *mean_weight,
+                             KSum *scratch /* 5 x 32 */, float *mscratch /* 32 */,
+                             const unsigned long long *prob_acc = nullptr, const int32_t *dem_acc = nullptr,
+                             float prob_unit = 0.f) {
     const long long TK = (long long)T * K;
     const float TKf = (float)TK, Tf = (float)T, inv_n = 1.0f / (float)N;
     KSum v[5];  // aux, kl, z, entropy, load variance
+    float amax = 0.f;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        v[2].add(__ldcg(partials + (size_t)r * kPartialStride));
+        v[3].add(__ldcg(partials + (size_t)r * kPartialStride + 1));
+        amax = fmaxf(amax, __ldcg(partials + (size_t)r * kPartialStride + 2));
+    }
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
-        const int de = __ldcg(demand + e);
-        const float pe = __ldcg(prob_sum + e);
+        int de;
+        float pe;
+        if (prob_acc != nullptr) {
+            pe = __ull2float_rn(__ldcg(prob_acc + e)) * prob_unit;
+            de = __ldcg(dem_acc + e);
+            prob_sum[e] = pe;
+            demand[e] = de;
+        } else {
+            de = __ldcg(demand + e);
+            pe = __ldcg(prob_sum + e);
+        }
         v[0].add(aux_term(de, pe, TKf, Tf));
         if (aux_kl != nullptr) v[1].add(kl_summand(de, TK, N));
         const float df = (float)de / TKf - inv_n;
         v[4].add(df * df);
         if (mean_weight != nullptr)
             mean_weight[e] = de > 0 ? __ull2float_rn(__ldcg(w_acc + e)) * kFixUnit / (float)de : 0.f;
-    }
-    float amax = 0.f;
-    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-        v[2].add(__ldcg(partials + (size_t)r * kPartialStride));
-        v[3].add(__ldcg(partials + (size_t)r * kPartialStride + 1));
-        amax = fmaxf(amax, __ldcg(partials + (size_t)r * kPartialStride + 2));
     }
     block_sums<5>(v, scratch);
     amax = block_max(amax, mscratch);
@@ -481,7 +497,7 @@ route_finalize_kernel(const float *__restrict__ prob_partial, const float *__res
     __threadfence();
     __shared__ KSum scratch[5 * 32];
     __shared__ float mscratch[32];
-    block_losses(N, T, K, demand, prob_sum, lse_partial, rows, w_acc, alpha, beta, kl_coef, aux, z_loss, aux_kl,
+    block_losses(N, T, K, const_cast<int32_t *>(demand), prob_sum, lse_partial, rows, w_acc, alpha, beta, kl_coef, aux, z_loss, aux_kl,
                  health, mean_weight, scratch, mscratch);
 }
 

@@ -568,14 +568,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     __syncthreads();
     if (!sh.last) return;
     __threadfence();
-    for (int e = threadIdx.x; e < N; e += kThreads) {
-        p.prob_sum[e] = __ull2float_rn(__ldcg(p.prob_acc + e)) * kProbUnit;
-        p.demand[e] = __ldcg(p.dem_acc + e);
-    }
-    __threadfence();
-    __syncthreads();
     route::block_losses(N, p.T, K, p.demand, p.prob_sum, p.lse_partial, (int)gridDim.x, p.w_acc, p.alpha, p.beta,
-                        p.kl_coef, p.aux, p.z_loss, p.aux_kl, p.health, p.mean_weight, sh.red, sh.mred);
+                        p.kl_coef, p.aux, p.z_loss, p.aux_kl, p.health, p.mean_weight, sh.red, sh.mred, p.prob_acc,
+                        p.dem_acc, kProbUnit);
 }
 
 }  // namespace rtc
