@@ -3,12 +3,17 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-One step = one moe_forward over a resident batch of the Mixtral-shaped
-prefill layer (T=4096 tokens, d_model=4096, d_ff=14336, 8 experts, top-2,
-dropless): gate, TopK-then-softmax routing, dispatch, both grouped expert
-GEMMs, combine and the balance loss. Synthetic inputs on the 1/64 grid, random
-bf16 expert weights. The expert weights alone (1.88 GB) exceed L2, so every
-step streams them from HBM; no explicit flush is added.
+One step = one moe_forward over a resident batch of the DeepSeek-V3-shaped
+layer (T=4096 tokens, d_model=7168, d_ff=2048, 256 routed experts + 1 shared,
+top-8, per-expert selection bias, dropless), the largest of the pages'
+workloads that fits one GPU: gate, TopK-then-softmax routing, dispatch, the
+grouped expert GEMMs, combine and the balance loss. Synthetic inputs on the
+1/64 grid, random bf16 expert weights. The expert weights read every step
+(15 GB) exceed L2, so every step streams them from HBM; no explicit flush is
+added. The same run times further workloads (the Mixtral-shaped prefill layer,
+the tensor-core target, and the 16-token decode layer with bf16 and FP8
+expert weights, the weight-streaming targets) and reports them under
+"workloads".
 
 Prints ONE JSON line on rank 0. Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU and batch (no collective on the data path;
@@ -39,16 +44,18 @@ METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
 
 
-def gemm_traffic(kernel_source: str):
-    """DRAM bytes per step of the grouped GEMM from the committed ncu summary,
-    or None when the kernel source changed since those counters were taken."""
+def gemm_traffic(workload: str):
+    """DRAM bytes per step of the grouped GEMM launches of `workload` from the
+    committed ncu summary (profiles/grouped_gemm_<workload>.json), or None
+    when there is none or the kernel source changed since the counters were
+    taken (the summary records the source's sha256)."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "grouped_gemm_mixtral_prefill.json")) as fh:
+        with open(os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}.json")) as fh:
             prof = json.load(fh)
-        with open(os.path.join(ROOT, kernel_source), "rb") as fh:
+        with open(os.path.join(ROOT, prof["source"]), "rb") as fh:
             h = hashlib.sha256(fh.read()).hexdigest()
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         return None
     return prof["dram_bytes_per_step"] if prof.get("source_sha256") == h else None
 
@@ -227,68 +234,54 @@ def run_reference(args, cfg):
     return 0
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="mixtral_prefill")
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-sample", type=int, default=1024, help="tokens in the CPU-oracle sample")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--backward-steps", type=int, default=10,
-                    help="also time moe_backward (forward recompute + backward) for this many steps; 0 = off")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+def choose_peak(P, clk, region_ms: float):
+    """The bf16 peak that matches the timed region's conditions: the burst
+    figure (a short run at full clocks) when the region lasted under a second
+    or the median sampled SM clock was at least 95% of the maximum; the
+    sustained, power-capped figure otherwise."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    burst = region_ms < 1000.0 or (sm is not None and smax and sm >= 0.95 * smax)
+    return ("burst", P["bf16_tflops"]) if burst else ("sustained", P["bf16_tflops_sustained"])
 
-    from top_routing_expert_then_b300.inputs import CONFIGS
-    cfg = CONFIGS[args.config]
-    if args.impl == "reference":
-        return run_reference(args, cfg)
 
+def ffn_work(cfg, R: int, hit: int):
+    """Algorithmic FLOPs and bytes of one step's expert GEMMs: 4 d f FLOPs per
+    kept row (two Linears) plus the shared expert's per token; bytes = the
+    weights of every expert that received rows (+ the shared expert's, + one
+    fp32 scale per output channel with FP8) + x rows in, hidden rows out and
+    back in, output rows out."""
+    T, d, f = cfg.T, cfg.d_model, cfg.d_ff
+    flops = 4.0 * R * d * f + (4.0 * T * d * f if cfg.has_shared else 0.0)
+    rows_all = R + (T if cfg.has_shared else 0)
+    fp8 = cfg.weights == "fp8_e4m3"
+    w_bytes = 2.0 * d * f * (1 if fp8 else 2) + ((d + f) * 4 if fp8 else 0)
+    nbytes = (hit + (1 if cfg.has_shared else 0)) * w_bytes + rows_all * (2 * d + 4 * f + 2 * d)
+    return flops, nbytes
+
+
+def time_forward(cfg, dev, pg, seed: int, steps: int, warmup: int):
+    """Warm-up, then `steps` timed forwards with per-stage CUDA-event marks on
+    the launching stream, barrier + synchronize on both sides and nvidia-smi
+    clock samples during the timed region. Returns the inputs, the layer and
+    the measurements."""
     import torch
     from top_routing_expert_then_b300 import lib
-    from top_routing_expert_then_b300.inputs import make_dy, make_inputs
+    from top_routing_expert_then_b300.inputs import make_inputs
 
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        pg = dist
-
-    inp = make_inputs(cfg, args.seed + rank, device=dev)
+    inp = make_inputs(cfg, seed, device=dev)
     layer = lib.MoELayer.from_inputs(inp)
     ro = layer.route_outputs()
     y = torch.empty_like(inp.x)
     stream = torch.cuda.current_stream()
-    P = peaks()
-
-    # warm-up (also yields the kept-row count for the FLOP figure)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         layer.forward(inp.x, inp.sel_bias, y=y, route_out=ro)
     torch.cuda.synchronize()
     if lib.device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{cfg.name}: device error during warm-up")
     R = int(ro.expert_offsets[-1].item())
     hit = int((ro.kept > 0).sum().item())
-    T, d, f = cfg.T, cfg.d_model, cfg.d_ff
-    ffn_flops = 4.0 * R * d * f + (4.0 * T * d * f if cfg.has_shared else 0.0)
-    # algorithmic bytes of the two grouped GEMMs: weights of every expert that
-    # received rows (+ shared), x_perm in, H out and back in, y_perm out
-    rows_all = R + (T if cfg.has_shared else 0)
-    fp8 = cfg.weights == "fp8_e4m3"
-    w_elem = 1 if fp8 else 2  # bytes per expert weight (+ one fp32 scale per output channel with FP8)
-    w_bytes = 2.0 * d * f * w_elem + ((d + f) * 4 if fp8 else 0)
-    ffn_bytes = (hit + (1 if cfg.has_shared else 0)) * w_bytes + rows_all * (2 * d + 4 * f + 2 * d)
 
-    # ---- timed region: K steps, per-stage marks on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
     for row in ev:  # torch creates the CUDA event on its first record
         for e in row:
             e.record(stream)
@@ -306,7 +299,7 @@ def main():
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         layer.forward_marked(inp.x, ev[i], inp.sel_bias, y=y, route_out=ro)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -316,25 +309,104 @@ def main():
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(pg, start.elapsed_time(stop), dev)
     if lib.device_error() != 0:
-        raise RuntimeError("device error during the timed region")
+        raise RuntimeError(f"{cfg.name}: device error during the timed region")
+    stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / steps for j in range(5)]
+    return {"inp": inp, "layer": layer, "R": R, "hit": hit, "elapsed_ms": elapsed_ms, "stage_ms": stage_ms,
+            "launches": launches, "clocks": clk, "stream": stream}
 
-    stage_names = ["route_aux", "dispatch", "ffn_gemm1", "ffn_gemm2", "combine"]
-    stage_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ev) / args.steps for j in range(5)]
-    gemm_ms = stage_ms[2] + stage_ms[3]
-    achieved_tflops = ffn_flops / (gemm_ms * 1e-3) / 1e12
-    peak_t = P["bf16_tflops_sustained"]
-    achieved_gbs = ffn_bytes / (gemm_ms * 1e-3) / 1e9
-    # the binding roof: tensor when the GEMMs' FLOP per byte exceeds the
-    # machine balance (sustained bf16 / HBM), else HBM
-    tensor_bound = ffn_flops / ffn_bytes > peak_t * 1e12 / (P["hbm_gbs"] * 1e9)
 
-    # HBM-bound stages: algorithmic bytes per step
-    K, N = cfg.K, cfg.N
+STAGES = ["route_aux", "dispatch", "ffn_gemm1", "ffn_gemm2", "combine"]
+
+
+def gemm_roofline(cfg, m, P, peak_kind, peak_t):
+    """Roofline of the grouped expert GEMM (the dominant kernel) for one timed
+    workload: its launches' time per step from the stage marks, algorithmic
+    FLOPs and bytes per step, the binding roof chosen by FLOPs per byte
+    against the machine balance at the chosen bf16 peak."""
+    flops, nbytes = ffn_work(cfg, m["R"], m["hit"])
+    gemm_ms = m["stage_ms"][2] + m["stage_ms"][3]
+    tflops = flops / (gemm_ms * 1e-3) / 1e12
+    gbs = nbytes / (gemm_ms * 1e-3) / 1e9
+    tensor_bound = cfg.weights == "bf16" and flops / nbytes > peak_t * 1e12 / (P["hbm_gbs"] * 1e9)
+    fp8 = cfg.weights == "fp8_e4m3"
+    kernel = ("grouped_gemm_fp8t_kernel (expert Linears, FP8 weights widened into tensor memory, "
+              "channel-major tcgen05)") if fp8 else "grouped_gemm_kernel (expert Linears, tcgen05)"
+    return {"kernel": kernel,
+            "bound": "tensor" if tensor_bound else "hbm",
+            "achieved": tflops if tensor_bound else gbs,
+            "peak": peak_t if tensor_bound else P["hbm_gbs"],
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": tflops / peak_t if tensor_bound else gbs / P["hbm_gbs"],
+            "peak_kind": (f"{P['source']} {peak_kind} bf16" if tensor_bound else f"{P['source']} HBM copy"),
+            "tflops": tflops, "gbs": gbs,
+            "frac_of_burst_bf16": tflops / P["bf16_tflops"],
+            "frac_of_sustained_bf16": tflops / P["bf16_tflops_sustained"],
+            "frac_of_hbm": gbs / P["hbm_gbs"],
+            "flops_per_step": flops, "bytes_per_step": nbytes, "ms_per_step": gemm_ms,
+            "traffic": gemm_traffic(cfg.name),
+            "traffic_unit": "DRAM bytes per step (all grouped-GEMM launches), ncu"}
+
+
+def hbm_stages(cfg, m, P):
+    """GB/s of the HBM-bound stages from their algorithmic bytes per step."""
+    T, d, K, N, R = cfg.T, cfg.d_model, cfg.K, cfg.N, m["R"]
     route_bytes = T * d * 2 + N * d * 2 + T * K * 8 + N * 8
     dispatch_bytes = T * K * 4 * 4 + T * d * 2 + R * d * 2
     combine_bytes = R * d * 2 + T * d * 2 + (T * d * 2 if cfg.has_shared else 0) + T * K * 8
+    sm = m["stage_ms"]
+    return {"route_aux": {"bytes": route_bytes, "gbs": route_bytes / (sm[0] * 1e-3) / 1e9},
+            "dispatch": {"bytes": dispatch_bytes, "gbs": dispatch_bytes / (sm[1] * 1e-3) / 1e9},
+            "combine": {"bytes": combine_bytes, "gbs": combine_bytes / (sm[4] * 1e-3) / 1e9},
+            "peak_gbs": P["hbm_gbs"]}
 
-    value = whole_job_rate(world, T, args.steps, elapsed_ms)
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dsv3",
+                    help="headline workload (default: the DeepSeek-V3-shaped layer, the largest that fits one GPU)")
+    ap.add_argument("--extras", default="mixtral_prefill,mixtral_decode16,mixtral_decode16_fp8",
+                    help="further workloads timed in the same run and reported under 'workloads' "
+                         "(comma-separated names, or 'none')")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-sample", type=int, default=512, help="tokens in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--backward-steps", type=int, default=10,
+                    help="also time moe_backward (forward recompute + backward) for this many steps; 0 = off")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from top_routing_expert_then_b300.inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+    from top_routing_expert_then_b300 import lib
+    from top_routing_expert_then_b300.inputs import make_dy
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    P = peaks()
+
+    # ---- headline workload
+    m = time_forward(cfg, dev, pg, args.seed + rank, args.steps, args.warmup)
+    inp, layer, stream = m["inp"], m["layer"], m["stream"]
+    T, d = cfg.T, cfg.d_model
+    value = whole_job_rate(world, T, args.steps, m["elapsed_ms"])
+    peak_kind, peak_t = choose_peak(P, m["clocks"], m["elapsed_ms"])
+    roof = gemm_roofline(cfg, m, P, peak_kind, peak_t)
 
     # ---- end to end through the public API with host buffers
     # (moe_forward_hostio_batches: every step copies its input from pinned host
@@ -357,6 +429,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
     e2e_value = whole_job_rate(world, T, args.e2e_steps, e2e_ms)
+    del xd, yd
 
     # ---- training step: moe_backward (recomputes the forward, then every gradient)
     train = None
@@ -376,7 +449,35 @@ def main():
         bwd_ms = max_over_ranks(pg, b0.elapsed_time(b1), dev) / args.backward_steps
         train = {"ms_per_step": bwd_ms, "tokens_per_s": whole_job_rate(world, T, 1, bwd_ms),
                  "steps": args.backward_steps, "what": "moe_backward: forward recompute + all gradients (fp32)"}
-        del bws
+        del bws, dy
+        if lib.device_error() != 0:
+            raise RuntimeError("device error during the backward")
+
+    inp_cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_cpu = inp.to("cpu")
+    del layer, inp, m["layer"], m["inp"]
+    torch.cuda.empty_cache()
+
+    # ---- further workloads: the prefill tensor-core target and the decode
+    # weight-streaming targets, each timed like the headline
+    workloads = {}
+    extras = [] if args.extras.strip().lower() == "none" else [w for w in args.extras.split(",") if w]
+    for name in extras:
+        if name == cfg.name:
+            continue
+        xc = CONFIGS[name]
+        mx = time_forward(xc, dev, pg, args.seed + rank, args.steps, args.warmup)
+        pk, pt = choose_peak(P, mx["clocks"], mx["elapsed_ms"])
+        workloads[name] = {
+            "value": whole_job_rate(world, xc.T, args.steps, mx["elapsed_ms"]), "unit": UNIT,
+            "ms_per_step": mx["elapsed_ms"] / args.steps,
+            "roofline": gemm_roofline(xc, mx, P, pk, pt),
+            "stages_us": {n: round(1e3 * v, 2) for n, v in zip(STAGES, mx["stage_ms"])},
+            "hbm_stages": hbm_stages(xc, mx, P),
+            "kept_rows": mx["R"], "gpu_launches": mx["launches"], "clocks": mx["clocks"]}
+        del mx
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if pg:
@@ -384,47 +485,29 @@ def main():
         return 0
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if inp_cpu is not None:
         import oracle
         oracle.build()
-        inp_cpu = inp.to("cpu")
-        dt, n = oracle_sample(cfg, inp_cpu, args.cpu_sample, seed=7)
+        dt, n = oracle_sample(cfg, inp_cpu, min(args.cpu_sample, cfg.T), seed=7)
         cpu = {"value": n / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": sample_desc(cfg, n), "seconds": round(dt, 2)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": m["elapsed_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(cfg, {"kept_rows": R, "parallelism": f"replicas{world}"}),
-        "roofline": {"kernel": ("grouped_gemm_fp8t_kernel (both expert Linears, FP8 weights widened into tensor "
-                                "memory, channel-major tcgen05)") if fp8 else
-                               "grouped_gemm_kernel (both expert Linears, tcgen05)",
-                     "bound": "tensor" if tensor_bound else "hbm",
-                     "achieved": achieved_tflops if tensor_bound else achieved_gbs,
-                     "peak": peak_t if tensor_bound else P["hbm_gbs"],
-                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
-                     "frac": achieved_tflops / peak_t if tensor_bound else achieved_gbs / P["hbm_gbs"],
-                     "tflops": achieved_tflops, "gbs": achieved_gbs, "bytes_per_step": ffn_bytes,
-                     "traffic": gemm_traffic("top_routing_expert_then_b300/csrc/grouped_gemm.cuh")
-                     if cfg.name == "mixtral_prefill" else None,
-                     "traffic_unit": "DRAM bytes per step (both launches), ncu",
-                     "peak_kind": f"{P['source']} sustained bf16" if tensor_bound else f"{P['source']} HBM copy",
-                     "frac_of_burst": achieved_tflops / P["bf16_tflops"],
-                     "flops_per_step": ffn_flops, "ms_per_step": gemm_ms},
-        "stages_us": {n: round(1e3 * m, 2) for n, m in zip(stage_names, stage_ms)},
-        "hbm_stages": {
-            "route_aux": {"bytes": route_bytes, "gbs": route_bytes / (stage_ms[0] * 1e-3) / 1e9},
-            "dispatch": {"bytes": dispatch_bytes, "gbs": dispatch_bytes / (stage_ms[1] * 1e-3) / 1e9},
-            "combine": {"bytes": combine_bytes, "gbs": combine_bytes / (stage_ms[4] * 1e-3) / 1e9},
-            "peak_gbs": P["hbm_gbs"]},
+        "config": workload_config(cfg, {"kept_rows": m["R"], "parallelism": f"replicas{world}"}),
+        "roofline": roof,
+        "stages_us": {n: round(1e3 * v, 2) for n, v in zip(STAGES, m["stage_ms"])},
+        "hbm_stages": hbm_stages(cfg, m, P),
         "cpu_baseline": cpu,
         "train_step": train,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2,
                 "api": "moe_forward_hostio_batches (pinned host in/out every step, copies overlapped)",
                 "steps": args.e2e_steps},
-        "gpu_launches": launches,
-        "clocks": clk,
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
     if pg:

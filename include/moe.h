@@ -47,8 +47,7 @@
  *  - Kernel variants (environment variables read once per process; every
  *    variant computes the same function and passes the same parity tests,
  *    the defaults are the measured fastest): MOE_GEMM_VARIANT=pair (bf16
- *    expert GEMM on SM pairs, cta_group::2, 256-row tiles) or share_a (2-CTA
- *    clusters sharing the token tile by TMA multicast); MOE_ROUTE_VARIANT=
+ *    expert GEMM on SM pairs, cta_group::2, 256-row tiles); MOE_ROUTE_VARIANT=
  *    legacy (gate GEMM + TopK + finalize kernels for every N instead of the
  *    fused router for N <= 256); MOE_FP8_GEMM=token_major (FP8 expert GEMM
  *    with token rows as the MMA's M and the weights widened in shared memory
@@ -170,7 +169,9 @@ typedef struct {
     int32_t *slot_of;        /* [T, K] row of (t, k) in the per-expert blocks, -1 = dropped */
     float *aux;              /* [1] balance loss */
     float *z_loss;           /* [1] router z-loss beta * (1/T) * sum_t logsumexp(s_t)^2
-                                (lmnt.cn/news/351908 sec. 5.3), fp32 per token, fp64 sum */
+                                (lmnt.cn/news/351908 sec. 5.3): fp32 per token, per-block fp32
+                                partial sums added in block order with compensated (Neumaier)
+                                fp32 summation */
     float *aux_kl;           /* [1] kl_coef * sum_e (1/N) (log(1/N) - log f_e), f_e = demand_e/(T K)
                                 (KL-to-uniform balance loss of the CSDN MoELayer listing);
                                 +inf when an expert receives nothing */
@@ -234,7 +235,8 @@ MOE_API moe_status moe_route(const moe_shape *shape, const moe_bf16 *x, const mo
  * nothing: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. All calls share the one array: calls whose work
+ * before any stream capture. Only a successful lookup is kept: if the first
+ * call fails (MOE_ERR_CUDA), a later call on that device retries it. All calls share the one array: calls whose work
  * overlaps on the GPU (different streams, or different host threads on one
  * device) race on it and must be serialised by the caller. */
 MOE_API moe_status moe_route_noalloc(const moe_shape *shape, const moe_bf16 *x, const moe_bf16 *Wg,
@@ -317,8 +319,6 @@ MOE_API moe_status moe_forward_hostio(const moe_shape *shape, const moe_weights 
                               moe_bf16 *y_dev, moe_bf16 *y_host, const moe_route_out *out,
                               void *workspace, size_t workspace_bytes, void *stream);
 
-/* Reads (and, if clear != 0, resets) the device error word of the current
- * device. Synchronises the device. *code_out receives the MOE_DEVERR_* bits. */
 /* Host-to-host forward over a sequence of nbatch batches of T tokens with the
  * transfers overlapped: batch i is read from x_host + i * host_stride and
  * written to y_host + i * host_stride (host_stride in elements; 0 = the same
@@ -357,6 +357,8 @@ MOE_API moe_status moe_backward(const moe_shape *shape, const moe_weights *weigh
                                 const float *sel_bias, const moe_bf16 *dy, float g_aux, float g_z,
                                 const moe_grads *grads, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Reads (and, if clear != 0, resets) the device error word of the current
+ * device. Synchronises the device. *code_out receives the MOE_DEVERR_* bits. */
 MOE_API moe_status moe_get_device_error(int32_t clear, int32_t *code_out);
 
 /* Number of kernels this library has launched in this process (all devices,

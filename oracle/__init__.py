@@ -122,6 +122,9 @@ class Oracle:
         lib.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [P] * 17 + [f64, f64, f64, f64, i32] + [P] * 12
+        lib.oracle_combine_backward.argtypes = [i32, i32, i32, P, P, P, P]
+        lib.oracle_gate_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, f64, f64, f64, P]
+        lib.oracle_expert_backward.argtypes = [i32, i32, i32, i32, i32, i32] + [P] * 11 + [i32] + [P] * 4
         lib.oracle_health.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_fp8_value.restype = f64
         lib.oracle_fp8_value.argtypes = [ctypes.c_uint8]
@@ -321,6 +324,57 @@ class Oracle:
             _p(out["dx"]), _p(out.get("dWg")), _p(out.get("dW1")), _p(out.get("db1")),
             _p(out.get("dW2")), _p(out.get("db2")), _p(out.get("dWs1")), _p(out.get("dbs1")), _p(out.get("dWs2")),
             _p(out.get("dbs2")), _p(out["dw"]))
+        return out
+
+    # ---- pieces of the backward (for full-size checks)
+    def combine_backward(self, dy, y_perm, slot_of) -> np.ndarray:
+        """dw [T, K] = <dy_t, o_tk> from the forward's stored expert outputs."""
+        dy = _np(dy, np.uint16)
+        y_perm = _np(y_perm, np.uint16)
+        if y_perm.size == 0:
+            y_perm = np.zeros((1, dy.shape[1]), dtype=np.uint16)  # never read: every slot is -1
+        slot_of = _np(slot_of, np.int32)
+        T, d = dy.shape
+        K = slot_of.shape[1]
+        dw = np.zeros((T, K))
+        self.lib.oracle_combine_backward(T, d, K, _p(dy), _p(y_perm), _p(slot_of), _p(dw))
+        return dw
+
+    def gate_backward(self, x, fwd: "OracleResult", dw, aux_alpha: float, z_beta: float, g_aux: float = 1.0,
+                      g_z: float = 1.0) -> np.ndarray:
+        """dW_g [N, d] from the slot gradients dw [T, K] and the forward's routing."""
+        x = _np(x, np.uint16)
+        T, d = x.shape
+        s = np.ascontiguousarray(fwd.logits, dtype=np.float64)
+        N = s.shape[1]
+        K = fwd.topk_idx.shape[1]
+        dWg = np.zeros((N, d))
+        self.lib.oracle_gate_backward(T, d, N, K, _p(x), _p(s), _p(np.ascontiguousarray(fwd.topk_idx, np.int32)),
+                                      _p(np.ascontiguousarray(dw, np.float64)),
+                                      _p(np.ascontiguousarray(fwd.demand, np.int32)), float(aux_alpha),
+                                      float(z_beta), float(g_aux), float(g_z), _p(dWg))
+        return dWg
+
+    def expert_backward(self, x, fwd: "OracleResult", e: int, W1e, b1e, W2e, b2e, dy,
+                        round_stored: bool = True) -> dict:
+        """Weight and bias gradients of routed expert e (e >= 0) or of the
+        shared expert (e < 0, weight 1 on every token): dW1 [f, d], db1 [f],
+        dW2 [d, f], db2 [d]."""
+        x = _np(x, np.uint16)
+        W1e, W2e = _np(W1e, np.uint16), _np(W2e, np.uint16)
+        b1e, b2e = _np(b1e, np.float32), _np(b2e, np.float32)
+        dy = _np(dy, np.uint16)
+        T, d = x.shape
+        f = W1e.shape[0]
+        s = np.ascontiguousarray(fwd.logits, dtype=np.float64)
+        N = s.shape[1]
+        K = fwd.topk_idx.shape[1]
+        out = {"dW1": np.zeros((f, d)), "db1": np.zeros(f), "dW2": np.zeros((d, f)), "db2": np.zeros(d)}
+        self.lib.oracle_expert_backward(
+            T, d, f, N, K, int(e), _p(s), _p(np.ascontiguousarray(fwd.topk_idx, np.int32)),
+            _p(np.ascontiguousarray(fwd.slot_of, np.int32)), _p(np.ascontiguousarray(fwd.offsets, np.int32)),
+            _p(np.ascontiguousarray(fwd.row_token, np.int32)), _p(x), _p(W1e), _p(b1e), _p(W2e), _p(b2e), _p(dy),
+            1 if round_stored else 0, _p(out["dW1"]), _p(out["db1"]), _p(out["dW2"]), _p(out["db2"]))
         return out
 
     # ---- the whole layer

@@ -593,6 +593,77 @@ static double expert_row_backward(int d, int f, const uint16_t *xrow, const uint
     return dw;
 }
 
+/* Routing weights in double: softmax over the K selected, unbiased logits
+ * ([Infra] sec. 2.1), w[t*K + k] for the expert in slot k. */
+static void routing_weights(int T, int N, int K, const double *s, const int32_t *idx, double *w)
+{
+    for (int t = 0; t < T; ++t) {
+        double m = -INFINITY, z = 0.0;
+        for (int k = 0; k < K; ++k)
+            m = fmax(m, s[(size_t)t * N + idx[(size_t)t * K + k]]);
+        for (int k = 0; k < K; ++k)
+            z += exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m);
+        for (int k = 0; k < K; ++k)
+            w[(size_t)t * K + k] = exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m) / z;
+    }
+}
+
+/* Gradient of the loss with respect to the gate logits, ds [T, N], for the
+ * tokens with want[t] != 0 (want may be NULL = all; other rows are left as
+ * they are):
+ *   ds_t[e] = w_te (dw_te - sum_k w_tk dw_tk) on the TopK set (softmax over
+ *             the K kept logits, [Infra] sec. 2.1)
+ *           + g_aux alpha N / T p_te (f_e - sum_e' f_e' p_te')   ([Infra] sec. 5.2,
+ *             f = demand / (T K) held constant, p_t = softmax over all N)
+ *           + g_z 2 beta / T lse_t p_te                           ([Infra] sec. 5.3). */
+static void gate_logit_grads(int T, int N, int K, const double *s, const int32_t *idx, const double *w,
+                             const double *dw_out, const int32_t *demand, double alpha, double beta,
+                             double g_aux, double g_z, const uint8_t *want, double *ds)
+{
+    const double TK = (double)T * (double)K;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        if (want && !want[t])
+            continue;
+        const double *st = s + (size_t)t * N;
+        double *dst = ds + (size_t)t * N;
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < N; ++e)
+            m = fmax(m, st[e]);
+        for (int e = 0; e < N; ++e)
+            z += exp(st[e] - m);
+        const double lse = m + log(z);
+        double fp = 0.0;
+        for (int e = 0; e < N; ++e)
+            fp += ((double)demand[e] / TK) * exp(st[e] - m) / z;
+        for (int e = 0; e < N; ++e) {
+            const double p = exp(st[e] - m) / z;
+            dst[e] = g_aux * alpha * (double)N / (double)T * p * ((double)demand[e] / TK - fp)
+                   + g_z * 2.0 * beta / (double)T * lse * p;
+        }
+        double sdw = 0.0;
+        for (int k = 0; k < K; ++k)
+            sdw += w[(size_t)t * K + k] * dw_out[(size_t)t * K + k];
+        for (int k = 0; k < K; ++k)
+            dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (dw_out[(size_t)t * K + k] - sdw);
+    }
+}
+
+/* dW_g[e, :] = sum_t ds[t, e] x[t, :] (written, not accumulated into). */
+static void gate_weight_grads(int T, int d, int N, const double *ds, const uint16_t *x, double *dWg)
+{
+    memset(dWg, 0, sizeof(double) * (size_t)N * d);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int e = 0; e < N; ++e)
+        for (int t = 0; t < T; ++t) {
+            const double g = ds[(size_t)t * N + e];
+            if (g == 0.0)
+                continue;
+            for (int i = 0; i < d; ++i)
+                dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);
+        }
+}
+
 /* Gradients of the layer given the upstream gradient dy of y and weights
  * g_aux, g_z on the balance loss and the router z-loss (the training signal
  * the pages build around; [Infra] sec. 5). The TopK sets, the capacity drops
@@ -628,15 +699,8 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
     double *dx_shared = Ws1 ? (double *)calloc((size_t)T * d, sizeof(double)) : NULL;
     int *slot_k = (int *)malloc(sizeof(int) * (size_t)(R > 0 ? R : 1));
 
-    /* routing weights in double: softmax over the K selected, unbiased logits */
+    routing_weights(T, N, K, s, idx, w);
     for (int t = 0; t < T; ++t) {
-        double m = -INFINITY, z = 0.0;
-        for (int k = 0; k < K; ++k)
-            m = fmax(m, s[(size_t)t * N + idx[(size_t)t * K + k]]);
-        for (int k = 0; k < K; ++k)
-            z += exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m);
-        for (int k = 0; k < K; ++k)
-            w[(size_t)t * K + k] = exp(s[(size_t)t * N + idx[(size_t)t * K + k]] - m) / z;
         for (int k = 0; k < K; ++k) {
             int r = slot_of[(size_t)t * K + k];
             if (r >= 0)
@@ -705,35 +769,13 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
     }
 
     /* gate and the token gradient */
-    if (weights)
-        memset(dWg, 0, sizeof(double) * (size_t)N * d);
     double *ds = (double *)calloc((size_t)T * N, sizeof(double));
-    const double TK = (double)T * (double)K;
+    gate_logit_grads(T, N, K, s, idx, w, dw_out, demand, alpha, beta, g_aux, g_z, want, ds);
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t) {
         if (want && !want[t])
             continue;
-        const double *st = s + (size_t)t * N;
-        double *dst = ds + (size_t)t * N;
-        double m = -INFINITY, z = 0.0;
-        for (int e = 0; e < N; ++e)
-            m = fmax(m, st[e]);
-        for (int e = 0; e < N; ++e)
-            z += exp(st[e] - m);
-        const double lse = m + log(z);
-        double fp = 0.0;
-        for (int e = 0; e < N; ++e)
-            fp += ((double)demand[e] / TK) * exp(st[e] - m) / z;
-        for (int e = 0; e < N; ++e) {
-            const double p = exp(st[e] - m) / z;
-            dst[e] = g_aux * alpha * (double)N / (double)T * p * ((double)demand[e] / TK - fp)
-                   + g_z * 2.0 * beta / (double)T * lse * p;
-        }
-        double sdw = 0.0;
-        for (int k = 0; k < K; ++k)
-            sdw += w[(size_t)t * K + k] * dw_out[(size_t)t * K + k];
-        for (int k = 0; k < K; ++k)
-            dst[idx[(size_t)t * K + k]] += w[(size_t)t * K + k] * (dw_out[(size_t)t * K + k] - sdw);
+        const double *dst = ds + (size_t)t * N;
         double *dxt = dx + (size_t)t * d;
         for (int i = 0; i < d; ++i) {
             double acc = dx_shared ? dx_shared[(size_t)t * d + i] : 0.0;
@@ -747,19 +789,136 @@ void oracle_backward(int T, int d, int f, int N, int K, const uint16_t *x, const
             dxt[i] = acc;
         }
     }
-    for (int e = 0; e < N && weights; ++e)
-        for (int t = 0; t < T; ++t) {
-            const double g = ds[(size_t)t * N + e];
-            if (g == 0.0)
-                continue;
-            for (int i = 0; i < d; ++i)
-                dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);
-        }
+    if (weights)
+        gate_weight_grads(T, d, N, ds, x, dWg);
     free(ds);
     free(slot_k);
     free(dx_shared);
     free(dx_perm);
     free(w);
+}
+
+/* Pieces of the backward for full-size checks, each the same arithmetic as
+ * oracle_backward (which calls the same helpers) restricted to one part. */
+
+/* dw_tk = <dy_t, o_tk>: the combine's gradient with respect to the routing
+ * weight of slot k ([Infra] sec. 3.2 combine equation), from the forward's
+ * stored expert outputs y_perm [R, d] (bf16); 0 for a dropped slot. */
+void oracle_combine_backward(int T, int d, int K, const uint16_t *dy, const uint16_t *y_perm,
+                             const int32_t *slot_of, double *dw)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) {
+            const int r = slot_of[(size_t)t * K + k];
+            double dot = 0.0;
+            if (r >= 0)
+                for (int c = 0; c < d; ++c)
+                    dot += bf16_val(dy[(size_t)t * d + c]) * bf16_val(y_perm[(size_t)r * d + c]);
+            dw[(size_t)t * K + k] = dot;
+        }
+}
+
+/* dW_g [N, d] from the slot gradients dw [T, K] (see gate_logit_grads). */
+void oracle_gate_backward(int T, int d, int N, int K, const uint16_t *x, const double *s, const int32_t *idx,
+                          const double *dw, const int32_t *demand, double alpha, double beta, double g_aux,
+                          double g_z, double *dWg)
+{
+    double *w = (double *)malloc(sizeof(double) * (size_t)T * K);
+    double *ds = (double *)calloc((size_t)T * N, sizeof(double));
+    routing_weights(T, N, K, s, idx, w);
+    gate_logit_grads(T, N, K, s, idx, w, dw, demand, alpha, beta, g_aux, g_z, NULL, ds);
+    gate_weight_grads(T, d, N, ds, x, dWg);
+    free(ds);
+    free(w);
+}
+
+/* Weight and bias gradients of ONE expert: routed expert e >= 0 (its rows
+ * [offsets[e], offsets[e+1]), token row_token[r], routing weight from the
+ * logits), or the shared expert for e < 0 (every token, weight 1). W1e [f, d],
+ * b1e [f], W2e [d, f], b2e [d] are that expert's. Every row is first taken
+ * through expert_row_backward (the backward's own per-row step: h, dO, da),
+ * then the sums over the rows are formed one output row at a time:
+ *   dW2e[c, :] = sum_r dO[r, c] h[r, :],  db2e[c] = sum_r dO[r, c],
+ *   dW1e[j, :] = sum_r da[r, j] x[t_r, :], db1e[j] = sum_r da[r, j]. */
+void oracle_expert_backward(int T, int d, int f, int N, int K, int e, const double *s, const int32_t *idx,
+                            const int32_t *slot_of, const int32_t *offsets, const int32_t *row_token,
+                            const uint16_t *x, const uint16_t *W1e, const float *b1e, const uint16_t *W2e,
+                            const float *b2e, const uint16_t *dy, int round_stored, double *dW1e, double *db1e,
+                            double *dW2e, double *db2e)
+{
+    const int n = e >= 0 ? offsets[e + 1] - offsets[e] : T;
+    int *tok = (int *)malloc(sizeof(int) * (size_t)(n > 0 ? n : 1));
+    double *wgt = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (e >= 0) {
+        double *w = (double *)malloc(sizeof(double) * (size_t)T * K);
+        routing_weights(T, N, K, s, idx, w);
+        for (int t = 0; t < T; ++t)
+            for (int k = 0; k < K; ++k) {
+                const int r = slot_of[(size_t)t * K + k];
+                if (r >= offsets[e] && r < offsets[e + 1]) {
+                    tok[r - offsets[e]] = t;
+                    wgt[r - offsets[e]] = w[(size_t)t * K + k];
+                }
+            }
+        free(w);
+    } else {
+        for (int t = 0; t < T; ++t) {
+            tok[t] = t;
+            wgt[t] = 1.0;
+        }
+    }
+    (void)row_token;
+    double *H = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * f);
+    double *DO = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double *DA = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * f);
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)f);
+        double *dxrow = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int i = 0; i < n; ++i)
+            (void)expert_row_backward(d, f, x + (size_t)tok[i] * d, W1e, b1e, W2e, b2e, dy + (size_t)tok[i] * d,
+                                      wgt[i], round_stored, a, H + (size_t)i * f, DO + (size_t)i * d,
+                                      DA + (size_t)i * f, NULL, NULL, NULL, NULL, dxrow);
+        free(dxrow);
+        free(a);
+    }
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < d; ++c) {
+        double *out = dW2e + (size_t)c * f;
+        double bsum = 0.0;
+        for (int j = 0; j < f; ++j)
+            out[j] = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const double g = DO[(size_t)i * d + c];
+            const double *hi = H + (size_t)i * f;
+            bsum += g;
+            for (int j = 0; j < f; ++j)
+                out[j] += g * hi[j];
+        }
+        db2e[c] = bsum;
+    }
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < f; ++j) {
+        double *out = dW1e + (size_t)j * d;
+        double bsum = 0.0;
+        for (int q = 0; q < d; ++q)
+            out[q] = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const double g = DA[(size_t)i * f + j];
+            const uint16_t *xi = x + (size_t)tok[i] * d;
+            bsum += g;
+            for (int q = 0; q < d; ++q)
+                out[q] += g * bf16_val(xi[q]);
+        }
+        db1e[j] = bsum;
+    }
+    free(DA);
+    free(DO);
+    free(H);
+    free(wgt);
+    free(tok);
 }
 
 /* ---------------------------------------------------------------- KL balance loss */

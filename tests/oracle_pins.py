@@ -616,6 +616,41 @@ def pin_backward_token_mask(orc):
     assert np.array_equal(part["dw"][want], full["dw"][want])
 
 
+def pin_backward_pieces(orc):
+    """The per-part backward functions used on full-size workloads agree with
+    the whole backward (itself pinned to torch autograd): dw from the stored
+    expert outputs, dW_g from dw, and each expert's weight and bias gradients
+    (routed experts with drops, and the shared expert)."""
+    rng = np.random.default_rng(31)
+    T, d, f, N, K = 40, 16, 24, 5, 2
+    x, Wg, W1, b1, W2, b2 = _small_layer(rng, T, d, f, N)
+    Ws1 = randn_bf16(rng, (f, d), d ** -0.5)
+    Ws2 = randn_bf16(rng, (d, f), f ** -0.5)
+    bs1 = (rng.standard_normal(f) * 0.02).astype(np.float32)
+    bs2 = (rng.standard_normal(d) * 0.02).astype(np.float32)
+    dy = bits(torch.from_numpy(rng.standard_normal((T, d))).to(torch.bfloat16))
+    alpha, beta, g_aux, g_z = 0.01, 1e-3, 2.0, 3.0
+    fwd = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=0.8, aux_alpha=alpha, z_beta=beta,
+                      Ws1=Ws1, bs1=bs1, Ws2=Ws2, bs2=bs2)
+    assert (fwd.slot_of < 0).any() and (fwd.kept > 0).sum() >= 3
+    full = orc.backward(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, Ws1, bs1, Ws2, bs2)
+
+    def close(a, b, what):
+        scale = max(np.abs(b).max(), 1e-30)
+        assert np.abs(a - b).max() <= 1e-12 * scale, what
+
+    dw = orc.combine_backward(dy, fwd.y_perm, fwd.slot_of)
+    close(dw, full["dw"], "dw")
+    close(orc.gate_backward(x, fwd, dw, alpha, beta, g_aux, g_z), full["dWg"], "dWg")
+    for e in range(N):
+        g = orc.expert_backward(x, fwd, e, W1[e], b1[e], W2[e], b2[e], dy)
+        for k in ("dW1", "db1", "dW2", "db2"):
+            close(g[k], full[k][e], f"{k}[{e}]")
+    g = orc.expert_backward(x, fwd, -1, Ws1, bs1, Ws2, bs2, dy)
+    for k, ks in (("dW1", "dWs1"), ("db1", "dbs1"), ("dW2", "dWs2"), ("db2", "dbs2")):
+        close(g[k], full[ks], f"shared {k}")
+
+
 def pin_health(orc):
     """Router health statistics: entropy vs scipy.stats.entropy per token;
     equal logits give log N and a spread of 0 over equal loads; a closed-form
@@ -651,7 +686,7 @@ ALL_PINS = [
     pin_bf16_round, pin_gelu, pin_capacity, pin_gate_exact, pin_route_bruteforce,
     pin_route_closed_forms, pin_worked_example, pin_dispatch_bruteforce,
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
-    pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask, pin_health,
+    pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask, pin_backward_pieces, pin_health,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
     pin_dispatch_rank_major, pin_aux_kl,
 ]

@@ -47,29 +47,74 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
     return np.array(sorted(pick)[:max(n, 2)], dtype=np.int64)
 
 
+def covering_tokens(ref, T: int, n_random: int = 16, seed: int = 0, tile_rows=(128, 256)) -> np.ndarray:
+    """Tokens whose outputs exercise every tile boundary of the expert GEMMs:
+    for each expert that keeps rows, the tokens of its first and last kept
+    row (its last, partial m-tile) and of the rows on both sides of every
+    128- and 256-row tile edge inside its block; the first and the last token
+    (the shared expert's tail tile); plus seeded random picks."""
+    N = len(ref.kept)
+    pick = {0, T - 1}
+    for e in range(N):
+        r0, r1 = int(ref.offsets[e]), int(ref.offsets[e + 1])
+        if r1 <= r0:
+            continue
+        rows = {r0, r1 - 1}
+        for tr in tile_rows:
+            for edge in range(r0 + tr, r1, tr):
+                rows |= {edge - 1, edge}
+        pick |= {int(ref.row_token[r]) for r in rows}
+    rng = np.random.default_rng(seed)
+    pick |= set(rng.choice(T, size=min(n_random, T), replace=False).tolist())
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_forward_cached(cfg: MoEConfig, seed: int, cpu):
+    """The oracle's full forward (every token) of (cfg, seed), computed once
+    per test process: the full-size workloads' forward and backward checks
+    share it."""
+    key = (cfg, seed)
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle.forward_inputs(cpu)
+    return _ORACLE_CACHE[key]
+
+
 def gpu_inputs(cfg: MoEConfig, seed: int = 0):
     inp = make_inputs(cfg, seed, device="cuda")
     torch.cuda.synchronize()
     return inp
 
 
-def check_layer(cfg: MoEConfig, seed: int = 0, sample: int | None = None, stages: bool = True):
+def check_layer(cfg: MoEConfig, seed: int = 0, sample=None, stages: bool = True, cache: bool = False):
     """Full comparison of one configuration.
 
     Routing, dispatch, kept counts, drops, prob sums and the aux loss are
-    compared on every token. FFN outputs are compared on every row, or on the
-    rows of `sample` tokens when the oracle cannot do the whole batch in
-    seconds. With `stages`, each ABI stage is also run on oracle-produced
-    inputs, isolating it from the stages before it.
+    compared on every token. FFN outputs are compared on every row
+    (sample=None), on the rows of `sample` random tokens (an int), or on
+    sample="cover": the tokens of covering_tokens (every expert's first and
+    last kept row, both sides of every 128/256-row tile edge, the first and
+    last token). With `stages`, each ABI stage is also run on oracle-produced
+    inputs, isolating it from the stages before it. With `cache`, the oracle's
+    full forward is kept for later tests of the same (cfg, seed).
     """
     inp = gpu_inputs(cfg, seed)
     cpu = inp.to("cpu")
     T, K, N, d = cfg.T, cfg.K, cfg.N, cfg.d_model
     want = None
-    if sample is not None and sample < T:
+    if sample == "cover":
+        routing = oracle.forward_inputs(cpu, skip_ffn=True)
+        want = np.zeros(T, dtype=np.uint8)
+        want[covering_tokens(routing, T, seed=seed)] = 1
+    elif sample is not None and sample < T:
         want = np.zeros(T, dtype=np.uint8)
         want[sample_tokens(T, sample, seed)] = 1
-    ref = oracle.forward_inputs(cpu, want=want)
+    if want is None and cache:
+        ref = oracle_forward_cached(cfg, seed, cpu)
+    else:
+        ref = oracle.forward_inputs(cpu, want=want)
     shape = lib.shape_of(cfg)
     assert lib.capacity(shape) == ref.capacity
 

@@ -2,9 +2,13 @@
 
 The oracle mirrors the two bf16 storage points of the GPU backward (dO and da
 between the GEMMs) and otherwise computes in fp64; the GPU accumulates in
-fp32. Every gradient must agree within rel-L2 1e-2 and max |diff| <= 5e-2 of
-the tensor's largest magnitude (fp32 accumulation order and occasional one-ulp
-bf16 flips of dO / da; the gate gradients go through fp32 softmax Jacobians).
+fp32. Every gradient must agree within rel-L2 1e-2, max |diff| <= 5e-2 of the
+tensor's largest magnitude, and element by element |diff| <= 1e-2 (rms + |ref|)
+with rms the reference tensor's root mean square: fp32 accumulation order and
+occasional one-ulp bf16 flips of dO / da move an entry by a small fraction of
+the tensor's typical size, whatever that entry's own size; a gradient's scale
+is not 1 (it grows with the rows summed), so the tensor's rms stands where
+the forward's bound has 1.
 """
 
 import numpy as np
@@ -19,6 +23,7 @@ pytestmark = pytest.mark.gpu
 
 REL_L2 = 1e-2
 MAX_FRAC = 5e-2
+ELEM = 1e-2
 
 CASES = [
     MoEConfig("bwd_tiny_drops", 256, 128, 256, 8, 2, 1.25),
@@ -30,13 +35,21 @@ CASES = [
 
 
 def _compare(name, got, ref):
-    g = got.detach().double().cpu().numpy()
+    g = got.detach().double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     assert g.shape == ref.shape, (name, g.shape, ref.shape)
     assert np.all(np.isfinite(g)), name
+    if ref.size == 0:
+        return
     scale = max(np.abs(ref).max(), 1e-30)
     rel = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
     worst = np.abs(g - ref).max() / scale
     assert rel <= REL_L2 and worst <= MAX_FRAC, (name, rel, worst)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    err = np.abs(g - ref)
+    bound = ELEM * (rms + np.abs(ref))
+    i = np.argmax(err - bound)
+    assert np.all(err <= bound), (f"{name}: element {np.unravel_index(i, ref.shape)} got {g.flat[i]} ref "
+                                  f"{ref.flat[i]} (rms {rms})")
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=[c.name for c in CASES])
@@ -67,14 +80,7 @@ def test_backward_deterministic():
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "skewed"])
-def test_backward_full_size_sampled(name):
-    """Full-size workload: dx and dw of 12 sampled tokens against the oracle
-    (each computable one token at a time); the rest finite and run-to-run
-    identical."""
-    from top_routing_expert_then_b300.inputs import CONFIGS
-    from parity_util import sample_tokens
-    cfg = CONFIGS[name]
+def _gpu_backward(cfg):
     inp = make_inputs(cfg, 0, device="cuda")
     dy = make_dy(cfg, 0, device="cuda")
     layer = lib.MoELayer.from_inputs(inp)
@@ -85,12 +91,53 @@ def test_backward_full_size_sampled(name):
     for k in got:
         assert torch.isfinite(got[k]).all(), k
         assert torch.equal(got[k], again[k]), k
-    del again
+    del again, layer
+    return inp, dy, got
+
+
+def test_backward_full_size_skewed():
+    """The skewed workload at full size (T=8192, 64 experts, capacity 128):
+    every gradient against the oracle's whole backward."""
+    from top_routing_expert_then_b300.inputs import CONFIGS
+    cfg = CONFIGS["skewed"]
+    inp, dy, got = _gpu_backward(cfg)
     cpu = inp.to("cpu")
     fwd = oracle.forward_inputs(cpu, skip_ffn=True)
+    ref = oracle.backward_inputs(cpu, fwd, dy.cpu(), 1.0, 1.0)
+    for name, r in ref.items():
+        _compare(name, got[name], r)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral_prefill", "dsv3"])
+def test_backward_full_size(name):
+    """Full-size workloads: dw of every token, dW_g, the weight and bias
+    gradients of one routed expert (the last expert that keeps rows: its
+    block ends the regrouped buffer) and of the shared expert, and dx of 12
+    sampled tokens, against the oracle; the rest finite and run-to-run
+    identical. The oracle's full forward is shared with the forward parity
+    test of the same workload."""
+    from top_routing_expert_then_b300.inputs import CONFIGS
+    from parity_util import oracle_forward_cached, sample_tokens
+    cfg = CONFIGS[name]
+    inp, dy, got = _gpu_backward(cfg)
+    cpu = inp.to("cpu")
+    dyc = dy.cpu()
+    orc = oracle.default()
+    fwd = oracle_forward_cached(cfg, 0, cpu)
+    dw = orc.combine_backward(dyc, fwd.y_perm, fwd.slot_of)
+    _compare("dw", got["dw"], dw)
+    _compare("dWg", got["dWg"], orc.gate_backward(cpu.x, fwd, dw, cfg.aux_alpha, cfg.z_beta, 1.0, 1.0))
+    e = int(np.nonzero(fwd.kept)[0].max())
+    g = orc.expert_backward(cpu.x, fwd, e, cpu.W1[e], cpu.b1[e], cpu.W2[e], cpu.b2[e], dyc)
+    for k in ("dW1", "db1", "dW2", "db2"):
+        _compare(f"{k}[{e}]", got[k][e], g[k])
+    if cfg.has_shared:
+        g = orc.expert_backward(cpu.x, fwd, -1, cpu.Ws1, cpu.bs1, cpu.Ws2, cpu.bs2, dyc)
+        for k, ks in (("dW1", "dWs1"), ("db1", "dbs1"), ("dW2", "dWs2"), ("db2", "dbs2")):
+            _compare(ks, got[ks], g[k])
     toks = sample_tokens(cfg.T, 12, 3)
     want = np.zeros(cfg.T, dtype=bool)
     want[toks] = True
-    ref = oracle.backward_inputs(cpu, fwd, dy.cpu(), 1.0, 1.0, want=want)
+    ref = oracle.backward_inputs(cpu, fwd, dyc, 1.0, 1.0, want=want)
     _compare("dx", got["dx"][torch.from_numpy(toks).cuda()], ref["dx"][toks])
-    _compare("dw", got["dw"][torch.from_numpy(toks).cuda()], ref["dw"][toks])

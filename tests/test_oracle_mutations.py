@@ -21,8 +21,8 @@ MUTATIONS = [
     ("dx_without_shared_expert", [("double acc = dx_shared ? dx_shared[(size_t)t * d + i] : 0.0;", "double acc = 0.0;")]),
     ("dx_without_gate_term", [("acc += dst[e] * bf16_val(Wg[(size_t)e * d + i]);", "acc += 0.0 * dst[e];")]),
     ("z_grad_without_lse", [("+ g_z * 2.0 * beta / (double)T * lse * p;", "+ g_z * 2.0 * beta / (double)T * p;")]),
-    ("dWg_from_gate_weights", [("dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);",
-                                "dWg[(size_t)e * d + i] += g * bf16_val(Wg[(size_t)e * d + i]);")]),
+    ("dWg_from_wrong_row", [("dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)t * d + i]);",
+                             "dWg[(size_t)e * d + i] += g * bf16_val(x[(size_t)e * d + i]);")]),
     ("health_drop_rate_inverted", [("h[1] = 1.0 - kept_all / TK;", "h[1] = kept_all / TK;")]),
     ("health_mean_weight_over_kept", [("mean_w[e] = demand[e] > 0 ? mean_w[e] / (double)demand[e] : 0.0;",
                                        "mean_w[e] = kept[e] > 0 ? mean_w[e] / (double)kept[e] : 0.0;")]),
@@ -60,6 +60,12 @@ MUTATIONS = [
                             ("const int t = rank_major ? b : a, k = rank_major ? a : b;",
                              "const int t = a, k = b;")]),
     ("kl_direction_swapped", [("acc += u * (log(u) - log(f));", "acc += f * (log(f) - log(u));")]),
+    ("expert_backward_wrong_token", [("const uint16_t *xi = x + (size_t)tok[i] * d;",
+                                      "const uint16_t *xi = x + (size_t)i * d;")]),
+    ("expert_backward_bias_from_hidden", [("            bsum += g;\n            for (int j = 0; j < f; ++j)",
+                                           "            bsum += g * hi[0];\n            for (int j = 0; j < f; ++j)")]),
+    ("combine_backward_wrong_operand", [("dot += bf16_val(dy[(size_t)t * d + c]) * bf16_val(y_perm[(size_t)r * d + c]);",
+                                         "dot += bf16_val(dy[(size_t)t * d + c]) * bf16_val(y_perm[(size_t)t * d + c]);")]),
     ("dispatch_priority_inverted", [("const int outer = rank_major ? K : T, inner = rank_major ? T : K;",
                                      "const int outer = rank_major ? T : K, inner = rank_major ? K : T;"),
                                     ("const int t = rank_major ? b : a, k = rank_major ? a : b;",

@@ -5,8 +5,6 @@ in a child process of its own:
   MOE_FP8_GEMM=token_major   FP8 expert GEMM with the weights widened in
                              shared memory (token rows as the MMA's M)
   MOE_GEMM_VARIANT=pair      bf16 expert GEMM on SM pairs (cta_group::2, M=256)
-  MOE_GEMM_VARIANT=share_a   bf16 expert GEMM on 2-CTA clusters sharing the
-                             token tile by TMA multicast
   MOE_ROUTE_VARIANT=legacy   the general router (gate GEMM, TopK, finalize
                              kernels) for every N instead of the fused kernel
 """
@@ -37,9 +35,6 @@ VARIANTS = {
         'MoEConfig("fp8_experts", 700, 256, 640, 8, 2, 1.25, weights="fp8_e4m3")',
         'MoEConfig("fp8_decode_small", 24, 256, 384, 8, 2, 0.0, has_shared=True, weights="fp8_e4m3")']),
     "gemm_pair": ("MOE_GEMM_VARIANT", "pair", [
-        'MoEConfig("ragged", 300, 192, 320, 6, 2, 0.0)',
-        'MoEConfig("multi_tile_shared", 1500, 256, 512, 4, 2, 0.0, has_shared=True, sel_bias=True)']),
-    "gemm_share_a": ("MOE_GEMM_VARIANT", "share_a", [
         'MoEConfig("ragged", 300, 192, 320, 6, 2, 0.0)',
         'MoEConfig("multi_tile_shared", 1500, 256, 512, 4, 2, 0.0, has_shared=True, sel_bias=True)']),
     "route_legacy": ("MOE_ROUTE_VARIANT", "legacy", [

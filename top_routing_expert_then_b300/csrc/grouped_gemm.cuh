@@ -63,10 +63,11 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024; 
 #ifndef MOE_L2_PREFETCH_KBLOCKS
 #define MOE_L2_PREFETCH_KBLOCKS 0
 #endif
-// The producer asks for the weight (B) tile of k-block kb + PF_DIST into L2
-// while loading k-block kb: weights stream from HBM exactly once, and the
-// ring of 4 stages (~1 us of MMA work) is shorter than an HBM round trip
-// under load, so without the prefetch every stage would wait on DRAM.
+// Optional L2 prefetch of the weight (B) tile of k-block kb + PF_DIST while
+// loading k-block kb (compile-time switch; 0 = off, the default). Measured on
+// the Mixtral-shaped prefill layer, prefetching 4-16 k-blocks ahead was 6%
+// slower than none: the raster groups already keep each weight tile's readers
+// in step, so the first reader's fetch serves the others from L2.
 constexpr int PF_DIST = MOE_L2_PREFETCH_KBLOCKS;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s
@@ -635,238 +636,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS)
-                     : "memory");
-    }
-}
-
-// ============================================================================
-// Cluster variant with a shared A tile: a cluster of two CTAs computes the
-// tiles (m, n) and (m, n + 1) of one expert -- the same 128 rows of A against
-// two 256-column slices of B. Each CTA loads one 64-row half of the A tile
-// with TMA multicast into both CTAs' shared memory (so the A tile leaves L2
-// once per cluster) plus its own B tile. A stage may be refilled only when
-// both CTAs' MMAs have finished with it: every MMA commit arrives on the
-// stage's empty barrier in both CTAs (count 2). When n + 1 is past the last
-// n-tile the second CTA still loads and multiplies (rows of B past the
-// tensor read as zeros) but stores nothing.
-constexpr int MC_A_HALF_BYTES = 64 * BK * 2;  // 8 KB
-
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t mc_cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void mc_cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Work unit u -> (m-tile, pair of n-tiles np): the same raster groups as
-// tile_of, with n-tile pairs in place of n-tiles; this CTA takes n-tile
-// 2 np + rank. t.ok covers the m-tile only.
-__device__ __forceinline__ Tile unit_of(const Params &p, int u, int num_m, int num_np, int rank) {
-    Tile t = tile_of<BM>(p, u, num_m, num_np);  // t.n0 = np * BN here
-    t.n0 = (t.n0 / BN * 2 + rank) * BN;
-    return t;
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_mc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmC, const Params p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Shared *sh = reinterpret_cast<Shared *>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
-
-    const int warp = warp_id();
-    const int lane = lane_id();
-    const uint32_t rank = mc_cluster_rank();
-    const uint16_t both = 0x3;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&sh->full[s]), 1);
-            mbar_init(smem_u32(&sh->empty[s]), 2);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(smem_u32(&sh->tfull[a]), 1);
-            mbar_init(smem_u32(&sh->tempty[a]), 4);
-        }
-        mbar_init(smem_u32(&sh->drain), 1);
-        sh->abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&sh->tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    mc_cluster_sync();  // both CTAs' barriers are initialised before any multicast lands
-    tc_fence_after();
-    const uint32_t tmem_base = sh->tmem_base;
-
-    const int num_m = num_m_tiles<BM>(p);
-    const int num_n = (p.n_out + BN - 1) / BN;
-    const int num_np = (num_n + 1) / 2;
-    const int total = num_m * num_np;
-    const int kblocks = p.k_dim / BK;
-    const int cluster_id = blockIdx.x >> 1;
-    const int num_clusters = gridDim.x >> 1;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            uint32_t stage = 0, phase = 0;
-            bool stop = false;
-            for (int u = cluster_id; u < total && !stop; u += num_clusters) {
-                Tile t = unit_of(p, u, num_m, num_np, rank);
-                if (!t.ok) continue;  // an invalid m-tile: the same decision in both CTAs
-                const int brow = t.group * p.n_out + t.n0;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
-                        stop = true;
-                        break;
-                    }
-                    const uint32_t fb = smem_u32(&sh->full[stage]);
-                    uint8_t *a_s = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d_mc(smem_u32(a_s + rank * MC_A_HALF_BYTES), &tmA, fb, kb * BK, t.row0 + (int)rank * 64,
-                                   both);
-                    tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            uint32_t stage = 0, phase = 0;
-            uint32_t acc = 0, acc_phase = 0;
-            bool stop = false;
-            for (int u = cluster_id; u < total && !stop; u += num_clusters) {
-                Tile t = unit_of(p, u, num_m, num_np, rank);
-                if (!t.ok) continue;
-                if (!wait_bounded(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!wait_bounded(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true)) {
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
-                                 (kb != 0 || kk != 0) ? 1u : 0u);
-                    }
-                    mma_commit_mc(smem_u32(&sh->empty[stage]), both);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (stop) break;
-                mma_commit(smem_u32(&sh->tfull[acc]));
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
-            }
-            mma_commit(smem_u32(&sh->drain));
-            wait_bounded(sh, smem_u32(&sh->drain), 0, DRAIN_LIMIT_NS, false);
-        }
-    } else {
-        // ---------------------------------------------------- epilogue (warps 2-5)
-        const int q = warp & 3;
-        const int row = q * 32 + lane;
-        uint8_t *ebuf = smem + STAGES * STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
-        int ebuf_idx = 0;
-        uint32_t acc = 0, acc_phase = 0;
-        for (int u = cluster_id; u < total; u += num_clusters) {
-            Tile t = unit_of(p, u, num_m, num_np, rank);
-            if (!t.ok) {
-                if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
-                continue;
-            }
-            // an n-tile past the last one (odd count) is computed but stores nothing:
-            // its first column is already >= n_out
-            if (!wait_bounded(sh, smem_u32(&sh->tfull[acc]), acc_phase, WAIT_LIMIT_NS, true)) break;
-            tc_fence_after();
-            const int rows_valid = max(0, min(32, t.rows - q * 32));
-            uint16_t *out_row = p.out + (size_t)(t.row0 + row) * p.n_out;
-            const float *bias = p.bias + (size_t)t.group * p.n_out;
-            const uint32_t tbase = tmem_base + acc * ACC_COLS + ((uint32_t)(q * 32) << 16);
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                const int col = t.n0 + c0;
-                if (col >= p.n_out) break;  // warp-uniform
-                uint32_t r[32];
-                tmem_ld32(tbase + c0, r);
-                uint32_t packed[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(bias + col + j));
-                    float v0 = __uint_as_float(r[j + 0]) + b.x;
-                    float v1 = __uint_as_float(r[j + 1]) + b.y;
-                    float v2 = __uint_as_float(r[j + 2]) + b.z;
-                    float v3 = __uint_as_float(r[j + 3]) + b.w;
-                    if (p.gelu) {
-                        v0 = gelu_erf(v0);
-                        v1 = gelu_erf(v1);
-                        v2 = gelu_erf(v2);
-                        v3 = gelu_erf(v3);
-                    }
-                    packed[j / 2] = pack_bf16x2(v0, v1);
-                    packed[j / 2 + 1] = pack_bf16x2(v2, v3);
-                }
-                store_chunk_bf16(&tmC, ebuf, ebuf_idx, lane, packed, rows_valid, t.row0 + q * 32, col, out_row);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[acc]));
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
-        }
-        store_drain(lane);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    mc_cluster_sync();  // no multicast copy or commit still targets either CTA
-    tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                      : "memory");
     }
 }

@@ -345,9 +345,6 @@ moe_status device_state(DeviceState **out) {
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_pair_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::P_SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_mc_kernel,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
-        if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8w_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::Q_SMEM_BYTES);
         if (e == cudaSuccess)
@@ -587,7 +584,7 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
 // rows; measured on the Mixtral-shaped layer it is slower than the single-SM
 // kernel (128-row tiles), so the default is the single-SM kernel.
 // MOE_GEMM_VARIANT=single|pair (environment, read once) forces one of them.
-enum GemmVariant { kAuto = 0, kSingle = 1, kPair = 2, kShareA = 3 };
+enum GemmVariant { kAuto = 0, kSingle = 1, kPair = 2 };
 constexpr int kRasterSingle = 8;  // m-tiles (128 rows) per raster group
 constexpr int kRasterPair = 4;    // m-tiles (256 rows) per raster group
 int gemm_variant_override() {
@@ -596,7 +593,6 @@ int gemm_variant_override() {
         if (e == nullptr) return (int)kAuto;
         if (std::strcmp(e, "single") == 0) return (int)kSingle;
         if (std::strcmp(e, "pair") == 0) return (int)kPair;
-        if (std::strcmp(e, "share_a") == 0) return (int)kShareA;
         return (int)kAuto;
     }();
     return v;
@@ -610,17 +606,14 @@ bool use_pair(int64_t expected_rows_per_group) {
     return false;
 }
 
-bool use_share_a() { return gemm_variant_override() == kShareA; }
-
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
                        cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges) {
     CUtensorMap ta, tb, tc, ta32;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
-    const bool share_a = !pair && out_f32 == nullptr && k_splits == 1 && use_share_a();
     if (out_f32 != nullptr) pair = false;  // the fp32 (raw accumulator) mode is single-SM only
-    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, share_a ? 64 : 128)) return MOE_ERR_CUDA;
+    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
     if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
     if (out != nullptr) {
         if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
@@ -658,12 +651,6 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
         if (clusters < 1) clusters = 1;
         moe::gg::grouped_gemm_pair_kernel<<<2 * clusters, moe::gg::NUM_THREADS, moe::gg::P_SMEM_BYTES, st>>>(ta, tb, tc,
                                                                                                         p);
-    } else if (share_a) {
-        const int64_t units = (int64_t)m_upper * ((n_tiles + 1) / 2);
-        int clusters = dev->num_sms / 2;
-        if (units < clusters) clusters = (int)units;
-        if (clusters < 1) clusters = 1;
-        moe::gg::grouped_gemm_mc_kernel<<<2 * clusters, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p);
     } else {
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
@@ -1053,15 +1040,16 @@ static __device__ __align__(256) unsigned char moe_route_scratch[kRouteScratchBy
 
 namespace {
 struct ScratchAddress {
-    std::once_flag once;
-    void *ptr = nullptr;
-    cudaError_t err = cudaSuccess;
+    std::mutex mu;
+    void *ptr = nullptr;  // set once a lookup has succeeded; a failed lookup is retried on the next call
 };
 ScratchAddress g_route_scratch_addr[kMaxDevices];
 
 // Device address of moe_route_scratch on the current device. In host code the
 // symbol's name is only a host-side stand-in; the address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, with that device current. Only a successful lookup is
+// kept, so a first call that failed (for example one made during a stream
+// capture) does not poison later calls on that device.
 moe_status route_scratch(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -1069,11 +1057,15 @@ moe_status route_scratch(void **out) {
         return MOE_ERR_CUDA;
     }
     ScratchAddress &a = g_route_scratch_addr[dev];
-    std::call_once(a.once, [&a]() {
-        a.err = cudaGetSymbolAddress(&a.ptr, moe_route_scratch);
-        if (a.err != cudaSuccess) cudaGetLastError();
-    });
-    if (a.err != cudaSuccess || a.ptr == nullptr) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(a.mu);
+    if (a.ptr == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, moe_route_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        a.ptr = p;
+    }
     *out = a.ptr;
     return MOE_OK;
 }
