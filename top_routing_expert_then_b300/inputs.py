@@ -75,6 +75,11 @@ CONFIGS: Dict[str, MoEConfig] = {
                         note="fine-grained 64 experts, Zipf-skewed gate, capacity factor 1.0"),
     "dsv3": MoEConfig("dsv3", 4096, 7168, 2048, 256, 8, 0.0, has_shared=True, sel_bias=True,
                       note="DeepSeek-V3-shaped: 256 routed + 1 shared expert, top-8, selection bias"),
+    # a slice of the DeepSeek-V3-shaped layer for profiling: 16 routed experts
+    # of the same shape and the same 128 rows per expert on average (2 GB of
+    # weights instead of 15)
+    "dsv3_slice16": MoEConfig("dsv3_slice16", 256, 7168, 2048, 16, 8, 0.0, has_shared=True, sel_bias=True,
+                              note="16 experts of the DeepSeek-V3 shape, 128 rows per expert"),
     "mixtral_decode16_fp8": MoEConfig("mixtral_decode16_fp8", 16, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
                                       note="Mixtral-shaped decode, 16 tokens, FP8 E4M3 expert weights"),
     "mixtral_decode64_fp8": MoEConfig("mixtral_decode64_fp8", 64, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
