@@ -50,8 +50,29 @@ constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // one k-block of both operands
+// grouped_gemm_kernel's pipeline: G_STAGES stages of KPS k-blocks each (the
+// MMA issuer waits once and commits once per stage)
+#ifndef MOE_GEMM_KPS
+#define MOE_GEMM_KPS 1
+#endif
+constexpr int KPS = MOE_GEMM_KPS;
+constexpr int G_STAGES = STAGES / KPS;
+constexpr int G_STAGE_BYTES = KPS * STAGE_BYTES;
+static_assert(G_STAGES * KPS == STAGES, "k-blocks per stage must divide the ring");
+constexpr int NUM_THREADS = 192;      // SM-pair kernel: producer, MMA, 4 epilogue warps
+// Row-gather warps (gathered-A mode), taking the stage fills in turn. Measured
+// on the Mixtral-shaped prefill and DeepSeek-V3-shaped layers: one warp
+// (each fill arrived a fill late) made the first expert GEMM 1.2x / 1.5x
+// slower than TMA boxes of a pre-permuted copy, two 1.1x / 1.0x, four (each
+// arriving as soon as its own copies land) 1.03x / 1.0x, so the gather's
+// saving (the dispatch no longer writes the copy) is kept.
+#ifndef MOE_GATHER_WARPS
+#define MOE_GATHER_WARPS 4
+#endif
+constexpr int GATHER_WARPS = MOE_GATHER_WARPS;
+constexpr int NUM_THREADS_G = 192 + 32 * GATHER_WARPS;  // grouped_gemm_kernel: the same plus the row-gather warps
+constexpr int GATHER_WARP = 6;
 constexpr int ACC_COLS = BN;          // fp32 accumulator columns per buffer
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int BAR_BYTES = 256;
@@ -97,6 +118,10 @@ struct Params {
     const int *k_ranges;      // fp32 mode: non-null = split s covers the reduction columns
                               // [k_ranges[s], k_ranges[s + 1]) (multiples of 64, device memory);
                               // an empty range writes zeros (per-expert weight gradients)
+    const int32_t *a_rows;    // non-null: row r of A is row a_rows[r] of a_ptr (a gather by the
+                              // copy warp; tmA is not read), [out_rows] device ints
+    const uint16_t *a_ptr;    // the gathered tensor, [a_rows_limit, k_dim] bf16 row-major
+    int a_rows_limit;         // rows of the gathered tensor (bounds check of a_rows)
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -171,6 +196,12 @@ __device__ __forceinline__ uint64_t l2_policy_normal() {
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+
+// 16 bytes global -> shared, asynchronous, through L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 
 // Ask the TMA unit to pull a tile into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
@@ -401,7 +432,7 @@ __device__ __forceinline__ void load_a_tile(uint32_t dst, const CUtensorMap *tmA
     }
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS_G, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const Params p,
                     const __grid_constant__ CUtensorMap tmA32) {
@@ -409,14 +440,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Shared *sh = reinterpret_cast<Shared *>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
+    Shared *sh = reinterpret_cast<Shared *>(smem + G_STAGES * G_STAGE_BYTES + EPI_BYTES);
 
     const int warp = warp_id();
     const int lane = lane_id();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&sh->full[s]), 1);
+        for (int s = 0; s < G_STAGES; ++s) {
+            // the B tile's arrive.expect_tx, plus one arrival per lane of the row-gather warp
+            mbar_init(smem_u32(&sh->full[s]), p.a_rows != nullptr ? 33u : 1u);
             mbar_init(smem_u32(&sh->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -449,14 +481,134 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int kblocks = p.k_dim / BK;
     const int kb_per_split = (kblocks + splits - 1) / splits;
 
-    if (warp == 0) {
+    if (warp >= GATHER_WARP) {
+        // ---------------------------------------------------- row-gather warps (a_rows mode)
+        // Row i of the A tile is row a_rows[row0 + i] of a_ptr (for the first
+        // expert GEMM: the token of each regrouped row, so the dispatch never
+        // writes a regrouped copy of x). The GATHER_WARPS warps take the
+        // stage fills in turn. For its fill a warp copies the tile's rows'
+        // 128-byte segments of the k-block with 16-byte cp.async, lane l
+        // taking chunk l % 8 of rows 4 j + l / 8, straight to the positions the
+        // 128-byte swizzle gives them (chunk c of row i at i * 128 + (c ^ (i %
+        // 8)) * 16), so the MMA reads them as it reads a TMA box. Rows past
+        // the tile's rows are not copied (their accumulator rows are never
+        // stored). The stage's full barrier counts the B tile's bytes and one
+        // arrival per lane of the filling warp: a lane arrives once its copies
+        // have landed (cp.async.wait_group) and it has fenced them for the
+        // async proxy -- at once when the warps are many enough to keep every
+        // stage's copies in flight, else one of its fills later.
+        if (p.a_rows != nullptr) {
+            const int c = lane & 7, rsub = lane >> 3;
+            const int gw = warp - GATHER_WARP;  // this warp fills every GATHER_WARPS-th stage fill
+            int fill = 0;
+            // the source rows of a tile (rows 4 j + rsub, j < nj, this lane's):
+            // all loads are issued first; check_rows, run when the rows are
+            // used, validates them (a check right after each load would make
+            // the 32 loads wait on one another)
+            auto load_rows = [&](const Tile &t, int (&src)[32], int &nj) {
+                nj = max(0, (t.rows - rsub + 3) / 4);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) src[j] = j < nj ? __ldg(p.a_rows + t.row0 + 4 * j + rsub) : 0;
+            };
+            auto check_rows = [&](int (&src)[32], int nj) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < nj && (src[j] < 0 || src[j] >= p.a_rows_limit)) {
+                        flag_error(MOE_DEVERR_ROW_INDEX);
+                        src[j] = 0;
+                    }
+            };
+            auto next_tile = [&](int w, Tile &t) {
+                for (; w < total; w += gridDim.x) {
+                    t = tile_of<BM>(p, w / splits, num_m, num_n);
+                    if (t.ok) return w;
+                }
+                return total;
+            };
+            uint32_t stage = 0, phase = 0;
+            int prev = -1;  // stage of the previous fill, not yet arrived
+            bool stop = false;
+            Tile t, tn;
+            int src[32], nsrc[32], nj = 0, nnj = 0;
+            int w = next_tile(blockIdx.x, t);
+            if (w < total) {
+                load_rows(t, src, nj);
+                check_rows(src, nj);
+            }
+            while (w < total && !stop) {
+                // the next tile's rows load while this tile's copies are issued
+                const int wn = next_tile(w + gridDim.x, tn);
+                if (wn < total) load_rows(tn, nsrc, nnj);
+                const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
+                const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
+                const uint32_t sw0 = (uint32_t)((c ^ rsub) << 4), sw1 = (uint32_t)((c ^ (rsub + 4)) << 4);
+                for (int kb = kb0; kb < kb1; kb += KPS) {
+                    if ((fill++ % GATHER_WARPS) != gw) {  // another gather warp's fill
+                        if (++stage == G_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+                    bool ok = true;
+                    if (lane == 0) ok = wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true);
+                    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
+                        stop = true;
+                        break;
+                    }
+                    const int nk = min(KPS, kb1 - kb);
+                    for (int part = 0; part < nk; ++part) {
+                        const uint32_t a_s =
+                            smem_u32(smem + stage * G_STAGE_BYTES + part * STAGE_BYTES) + (uint32_t)rsub * 128u;
+                        const uint16_t *col = p.a_ptr + (size_t)(kb + part) * BK + c * 8;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nj) {
+                                const uint32_t dst = a_s + (uint32_t)j * 512u + ((j & 1) ? sw1 : sw0);
+                                const uint16_t *from = col + (size_t)src[j] * (size_t)p.k_dim;
+                                cp_async16(dst, from);
+                            }
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    if (2 * GATHER_WARPS > G_STAGES) {
+                        // arriving a fill late would hold the MMA back (with W gather warps and S
+                        // stages, fill f + W needs the stage the MMA frees after fill f + W - S)
+                        asm volatile("cp.async.wait_group 0;" ::: "memory");
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        mbar_arrive(smem_u32(&sh->full[stage]));
+                    } else {
+                        if (prev >= 0) {
+                            asm volatile("cp.async.wait_group 1;" ::: "memory");
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            mbar_arrive(smem_u32(&sh->full[prev]));
+                        }
+                        prev = (int)stage;
+                    }
+                    if (++stage == G_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                w = wn;
+                nj = nnj;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) src[j] = nsrc[j];
+                check_rows(src, nj);
+            }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            if (prev >= 0 && !stop) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(smem_u32(&sh->full[prev]));
+            }
+        }
+    } else if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint64_t pol_a = (MOE_TMA_L2_HINTS == 1 || MOE_TMA_L2_HINTS == 2) ? l2_policy_evict_last() : 0;
             const uint64_t pol_b = (MOE_TMA_L2_HINTS == 1 || MOE_TMA_L2_HINTS == 3) ? l2_policy_evict_first() : 0;
             uint32_t stage = 0, phase = 0;
-            int issued_phase[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
+            int issued_phase[G_STAGES];
+            for (int s = 0; s < G_STAGES; ++s) issued_phase[s] = -1;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
                 Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
@@ -466,20 +618,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
                 if (PF_DIST > 0)
                     for (int kb = kb0; kb < kb1 && kb < kb0 + PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += KPS) {
                     if (PF_DIST > 0 && kb + PF_DIST < kb1) tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
                     if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
                     }
                     const uint32_t fb = smem_u32(&sh->full[stage]);
-                    uint8_t *a_s = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, a_tile_bytes(t.rows) + B_BYTES);
-                    load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, kb * BK, t.row0, t.rows, pol_a);
-                    if (pol_b) tma_load_2d_hint(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow, pol_b);
-                    else tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, kb * BK, brow);
+                    const int nk = min(KPS, kb1 - kb);
+                    // with a_rows the row-gather warp fills the A tile (and arrives on fb itself)
+                    mbar_arrive_expect_tx(fb, (uint32_t)nk * ((p.a_rows ? 0u : a_tile_bytes(t.rows)) + B_BYTES));
+                    for (int part = 0; part < nk; ++part) {
+                        uint8_t *a_s = smem + stage * G_STAGE_BYTES + part * STAGE_BYTES;
+                        const int x = (kb + part) * BK;
+                        if (!p.a_rows) load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, x, t.row0, t.rows, pol_a);
+                        if (pol_b) tma_load_2d_hint(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow, pol_b);
+                        else tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow);
+                    }
                     issued_phase[stage] = (int)phase;
-                    if (++stage == STAGES) {
+                    if (++stage == G_STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -487,7 +644,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             if (stop) {
                 // let this block's copies in flight land before the block exits
-                for (int s = 0; s < STAGES; ++s)
+                for (int s = 0; s < G_STAGES; ++s)
                     if (issued_phase[s] >= 0)
                         wait_bounded(sh, smem_u32(&sh->full[s]), (uint32_t)issued_phase[s],
                                      DRAIN_LIMIT_NS, false);
@@ -508,21 +665,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
                 const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
                 const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += KPS) {
                     if (!wait_bounded(sh, smem_u32(&sh->full[stage]), phase, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t b_addr = a_addr + A_BYTES;
+                    const int nk = min(KPS, kb1 - kb);
+                    for (int part = 0; part < nk; ++part) {
+                        const uint32_t a_addr = smem_u32(smem + stage * G_STAGE_BYTES + part * STAGE_BYTES);
+                        const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
-                                 (kb != kb0 || kk != 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
+                                     (kb != kb0 || part != 0 || kk != 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit(smem_u32(&sh->empty[stage]));
-                    if (++stage == STAGES) {
+                    if (++stage == G_STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -542,7 +702,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ---------------------------------------------------- epilogue (warps 2-5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
-        uint8_t *ebuf = smem + STAGES * STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
+        uint8_t *ebuf = smem + G_STAGES * G_STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
         int ebuf_idx = 0;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {

@@ -436,10 +436,11 @@ bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
 
 // ------------------------------------------------------------------ stage launchers (no validation)
 
-moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
+moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows_n, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1, const int *k_ranges = nullptr);
+                       cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1, const int *k_ranges = nullptr,
+                       const int32_t *a_rows = nullptr);
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
@@ -545,7 +546,7 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 
 moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint16_t *x, int32_t *kept,
                         int32_t *offsets, int32_t *slot_of, int32_t *row_token, uint16_t *x_perm,
-                        const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr) {
+                        const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr, bool permute = true) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model;
     const int C = capacity_of(s);
     const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
@@ -569,13 +570,13 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
             topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
         count_launch();
     }
-    {
+    if (permute) {
         const int vec = d / 8;
         const int thr = vec < 256 ? 64 : 256;
         dim3 grid((T + moe::dispatch::kRowTok - 1) / moe::dispatch::kRowTok, (vec + thr - 1) / thr);
         moe::dispatch::permute_kernel<<<grid, thr, 0, st>>>(x, slot_of, T, K, d, rows, x_perm);
+        count_launch();
     }
-    count_launch();
     return launch_status();
 }
 
@@ -606,14 +607,14 @@ bool use_pair(int64_t expected_rows_per_group) {
     return false;
 }
 
-moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows, const void *B, uint64_t b_rows,
+moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows_n, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges) {
+                       cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges, const int32_t *a_rows) {
     CUtensorMap ta, tb, tc, ta32;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
-    if (out_f32 != nullptr) pair = false;  // the fp32 (raw accumulator) mode is single-SM only
-    if (!make_tmap(&ta, A, a_rows, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
+    if (out_f32 != nullptr || a_rows != nullptr) pair = false;  // fp32 mode and gathered A: single-SM kernel
+    if (!make_tmap(&ta, A, a_rows_n, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
     if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
     if (out != nullptr) {
         if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
@@ -639,6 +640,9 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     p.out_f32 = out_f32;
     p.k_splits = k_splits;
     p.k_ranges = k_ranges;
+    p.a_rows = a_rows;  // gathered A: the row-gather warp copies rows a_rows[r] of A
+    p.a_ptr = static_cast<const uint16_t *>(A);
+    p.a_rows_limit = (int)a_rows_n;
     if (pair && (out_f32 != nullptr || k_splits != 1)) return MOE_ERR_UNSUPPORTED;
     const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
     p.raster = pair ? kRasterPair : kRasterSingle;
@@ -655,8 +659,8 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
-        if (!make_tmap(&ta32, A, a_rows, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
-        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p, ta32);
+        if (!make_tmap(&ta32, A, a_rows_n, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
+        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS_G, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p, ta32);
     }
     count_launch();
     return MOE_OK;
@@ -775,9 +779,12 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
     return MOE_OK;
 }
 
+// x_perm: the regrouped rows; or, with gather_rows (bf16 weights only), the
+// first GEMM reads row gather_rows[r] of x for regrouped row r instead (x_perm
+// is then not read).
 moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm, const int32_t *offsets,
                    const moe_weights *wt, const uint16_t *x, uint16_t *y_perm, uint16_t *z,
-                   const FfnWs &w, cudaStream_t st, cudaEvent_t mid = nullptr) {
+                   const FfnWs &w, cudaStream_t st, cudaEvent_t mid = nullptr, const int32_t *gather_rows = nullptr) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model, f = s->d_ff;
     const int rows = T * K;
     const int mt = max_mtiles(s);
@@ -785,7 +792,7 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     const int C = capacity_of(s);
     if (per_expert > C) per_expert = C;
     const bool fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
-    const bool pair_routed = !fp8 && use_pair(per_expert);
+    const bool pair_routed = !fp8 && gather_rows == nullptr && use_pair(per_expert);
     const bool pair_shared = !fp8 && use_pair(T);
     const int tile_rows = fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
                               : (pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
@@ -816,8 +823,12 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
         return launch_status();
     }
     // routed experts: H = GELU(x_perm W1^T + b1), y_perm = H W2^T + b2
-    r = launch_gemm(dev, pair_routed, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
-                    w.num_mtiles, mt, 0, true, st);
+    if (gather_rows != nullptr)
+        r = launch_gemm(dev, false, x, T, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows, w.mtiles,
+                        w.num_mtiles, mt, 0, true, st, nullptr, 1, nullptr, gather_rows);
+    else
+        r = launch_gemm(dev, pair_routed, x_perm, rows, wt->W1, (uint64_t)N * f, d, f, N, wt->b1, w.H, rows,
+                        w.mtiles, w.num_mtiles, mt, 0, true, st);
     if (r != MOE_OK) return r;
     if (s->has_shared) {
         r = launch_gemm(dev, pair_shared, x, T, wt->Ws1, f, d, f, 1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T, true,
@@ -1223,12 +1234,17 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
                        st, z_loss, aux_kl, health, mean_weight)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
+    // bf16 experts: the first expert GEMM gathers its rows from x by row_token,
+    // so the regrouped copy of x is never written (FP8 experts read x_perm)
+    const bool gather = weights->format == MOE_WEIGHTS_BF16;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st,
-                          health ? health + 1 : nullptr)) != MOE_OK)
+                          health ? health + 1 : nullptr, !gather)) != MOE_OK)
         return r;
     if (!mark(2)) return MOE_ERR_CUDA;
     cudaEvent_t mid = events ? reinterpret_cast<cudaEvent_t>(events[3]) : nullptr;
-    if ((r = run_ffn(shape, dev, w.x_perm, offsets, weights, x, w.y_perm, w.z, w.ffn, st, mid)) != MOE_OK) return r;
+    if ((r = run_ffn(shape, dev, w.x_perm, offsets, weights, x, w.y_perm, w.z, w.ffn, st, mid,
+                     gather ? w.row_token : nullptr)) != MOE_OK)
+        return r;
     if (!mark(4)) return MOE_ERR_CUDA;
     if ((r = run_combine(shape, w.y_perm, slot_of, topk_w, w.z, y, st)) != MOE_OK) return r;
     if (!mark(5)) return MOE_ERR_CUDA;
