@@ -94,12 +94,16 @@ scan_kernel(const int32_t *__restrict__ hist, int chunks, int N, int C, int32_t 
     if (drop_rate != nullptr && e == N - 1) drop_rate[0] = (float)((double)(total - v) / (double)total);
 }
 
-// slot_of[t, k] = offsets[e] + p if p < C else -1; row_token[slot] = t.
+// slot_of[t, k] = offsets[e] + p if p < C else -1; row_token[slot] = t, and
+// row_token[r] = -1 for the rows r in [offsets[N], rows) that nothing keeps.
 __global__ void __launch_bounds__(kChunk)
 assign_kernel(const int32_t *__restrict__ topk_idx, Order o, int N, int C, const int32_t *__restrict__ base,
-              const int32_t *__restrict__ offsets, int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token) {
+              const int32_t *__restrict__ offsets, int32_t *__restrict__ slot_of, int32_t *__restrict__ row_token,
+              int rows) {
     extern __shared__ unsigned bits[];  // [4][N]
     for (int i = threadIdx.x; i < 4 * N; i += blockDim.x) bits[i] = 0u;
+    for (int r = __ldg(offsets + N) + blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x)
+        row_token[r] = -1;
     __syncthreads();
     const int w = warp_id(), lane = lane_id();
     const int v = blockIdx.x * kChunk + threadIdx.x;

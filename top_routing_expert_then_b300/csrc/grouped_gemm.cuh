@@ -1130,12 +1130,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
 // The m-tile list of the routed experts, from the expert offsets:
 // expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / tile_rows)
-// tiles, grouped for rasterisation (see tile_of).
-// One block of 1024 threads; N <= 1024; at most 65535 tiles.
-__global__ void __launch_bounds__(1024)
-build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int tile_rows, int raster,
-                    int max_tiles, int4 *__restrict__ mtiles, int *__restrict__ num_mtiles) {
-    __shared__ int sc[1024];
+// tiles, grouped for rasterisation (see tile_of). Called by all threads of a
+// block of 1024 (N <= 1024, at most 65535 tiles); `offsets` may be global or
+// shared memory; sc is 1024 ints of shared scratch.
+__device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N, int total_rows, int tile_rows,
+                                                   int raster, int max_tiles, int4 *__restrict__ mtiles,
+                                                   int *__restrict__ num_mtiles, int *sc) {
     const int e = threadIdx.x;
     int cnt = 0, r0 = 0, r1 = 0;
     bool bad = false;
@@ -1175,6 +1175,13 @@ build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, 
         }
     }
     if (e == 1023) *num_mtiles = v < max_tiles ? v : max_tiles;
+}
+
+__global__ void __launch_bounds__(1024)
+build_mtiles_kernel(const int32_t *__restrict__ offsets, int N, int total_rows, int tile_rows, int raster,
+                    int max_tiles, int4 *__restrict__ mtiles, int *__restrict__ num_mtiles) {
+    __shared__ int sc[1024];
+    build_mtiles_block(offsets, N, total_rows, tile_rows, raster, max_tiles, mtiles, num_mtiles, sc);
 }
 
 }  // namespace gg

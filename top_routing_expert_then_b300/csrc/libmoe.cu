@@ -21,6 +21,7 @@
 #include "gemm_fp8w.cuh"
 #include "gemm_fp8t.cuh"
 #include "backward.cuh"
+#include "plan.cuh"
 
 namespace {
 
@@ -92,11 +93,12 @@ int max_mtiles(const moe_shape *s) {
 struct RouteWs {
     float *logits;                 // general path: gate logits (K-split planes)
     float *partial;                // general path: per-block probability sums
-    float *lse_partial;            // per-block sums of logsumexp^2
-    unsigned long long *acc;       // fused path: fixed-point probability sums  } zeroed
-    int32_t *dem;                  // fused path: assignments per expert         } by one
-    unsigned long long *wacc;      // fixed-point routing-weight sums            } memset
-    unsigned int *done;            // finished-block ticket                      } (fused path)
+    float *lse_partial;            // per-block sums of logsumexp^2, entropy, max |logit|
+    unsigned long long *wacc;      // general path: fixed-point routing-weight sums (zeroed per call)
+    unsigned int *done;            // general path: finished-block ticket (zeroed per call)
+    int32_t *tile_hist;            // fused path: per 128-token tile, [tiles][N] assignments
+    unsigned long long *tile_prob; // fused path: [tiles][N] fixed-point probability sums
+    unsigned long long *tile_w;    // fused path: [tiles][N] fixed-point routing-weight sums
 };
 
 // Routing for N <= 256 runs as one fused kernel (tensor-core gate, TopK,
@@ -136,17 +138,17 @@ int gate_splits(const moe_shape *s) {
 
 RouteWs carve_route(Carve &c, const moe_shape *s) {
     RouteWs w{};
-    const bool fused = fused_route(s);
-    size_t rows = moe::route::kMaxPartialRows;
-    if (fused) {
-        rows = std::max(rows, (size_t)fused_route_grid(s));
-    } else {
-        w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
-        w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
+    if (fused_route(s)) {
+        const size_t tiles = (size_t)moe::rtc::num_tiles(s->T);
+        w.lse_partial = c.take<float>((size_t)fused_route_grid(s) * moe::route::kPartialStride);
+        w.tile_hist = c.take<int32_t>(tiles * s->N);
+        w.tile_prob = c.take<unsigned long long>(tiles * s->N);
+        w.tile_w = c.take<unsigned long long>(tiles * s->N);
+        return w;
     }
-    w.lse_partial = c.take<float>(rows * moe::route::kPartialStride);
-    w.acc = c.take<unsigned long long>(s->N);
-    w.dem = c.take<int32_t>(s->N);
+    w.logits = c.take<float>((size_t)gate_splits(s) * s->T * s->N);
+    w.partial = c.take<float>((size_t)moe::route::kMaxPartialRows * s->N);
+    w.lse_partial = c.take<float>((size_t)moe::route::kMaxPartialRows * moe::route::kPartialStride);
     w.wacc = c.take<unsigned long long>(s->N);
     w.done = c.take<unsigned int>(4);
     return w;
@@ -442,14 +444,23 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
                        cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1, const int *k_ranges = nullptr,
                        const int32_t *a_rows = nullptr);
 
+// The dispatch plan the fused router's plan kernel also forms (forward path):
+// per-chunk bases, kept counts, expert offsets and the grouped GEMMs' m-tile list.
+struct DispatchPlan {
+    int C;
+    int32_t *base, *kept, *offsets;
+    int tile_rows, raster, max_tiles;
+    int4 *mtiles;
+    int *num_mtiles;
+};
+
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
                      float *prob_sum, float *aux, const RouteWs &w, cudaStream_t st, float *z_loss = nullptr,
-                     float *aux_kl = nullptr, float *health = nullptr, float *mean_weight = nullptr) {
+                     float *aux_kl = nullptr, float *health = nullptr, float *mean_weight = nullptr,
+                     const DispatchPlan *dplan = nullptr) {
     const int T = s->T, d = s->d_model, N = s->N, K = s->K;
     if (fused_route(s)) {
-        const size_t zero_bytes = (size_t)(reinterpret_cast<char *>(w.done + 4) - reinterpret_cast<char *>(w.acc));
-        if (cudaMemsetAsync(w.acc, 0, zero_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
         CUtensorMap tx, tw;
         if (!make_tmap(&tx, x, (uint64_t)T, (uint64_t)d, moe::rtc::kTile)) return MOE_ERR_CUDA;
         if (!make_tmap(&tw, Wg, (uint64_t)N, (uint64_t)d, (uint32_t)moe::rtc::npad(N))) return MOE_ERR_CUDA;
@@ -467,21 +478,10 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         p.sel_bias = sel_bias;
         p.topk_idx = topk_idx;
         p.topk_w = topk_w;
-        p.prob_acc = w.acc;
-        p.dem_acc = w.dem;
-        p.w_acc = w.wacc;
-        p.health = health;
-        p.mean_weight = mean_weight;
-        p.done = w.done;
+        p.tile_hist = w.tile_hist;
+        p.tile_prob = w.tile_prob;
+        p.tile_w = w.tile_w;
         p.lse_partial = w.lse_partial;
-        p.demand = demand;
-        p.prob_sum = prob_sum;
-        p.aux = aux;
-        p.z_loss = z_loss;
-        p.aux_kl = aux_kl;
-        p.alpha = s->aux_alpha;
-        p.beta = s->z_beta;
-        p.kl_coef = s->kl_coef;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)fused_route_grid(s));
         cfg.blockDim = dim3(moe::rtc::kThreads);
@@ -503,6 +503,41 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
+        // one block: statistics and losses from the per-tile rows (and, on the
+        // forward path, the dispatch plan and the m-tile list)
+        moe::plan::Params q{};
+        q.T = T;
+        q.N = N;
+        q.K = K;
+        q.tiles = moe::rtc::num_tiles(T);
+        q.route_blocks = fused_route_grid(s);
+        q.tile_hist = w.tile_hist;
+        q.tile_prob = w.tile_prob;
+        q.tile_w = w.tile_w;
+        q.lse_partial = w.lse_partial;
+        if (dplan != nullptr) {
+            q.C = dplan->C;
+            q.base = dplan->base;
+            q.kept = dplan->kept;
+            q.offsets = dplan->offsets;
+            q.tile_rows = dplan->tile_rows;
+            q.raster = dplan->raster;
+            q.max_tiles = dplan->max_tiles;
+            q.mtiles = dplan->mtiles;
+            q.num_mtiles = dplan->num_mtiles;
+        }
+        q.demand = demand;
+        q.prob_sum = prob_sum;
+        q.aux = aux;
+        q.z_loss = z_loss;
+        q.aux_kl = aux_kl;
+        q.health = health;
+        q.mean_weight = mean_weight;
+        q.alpha = s->aux_alpha;
+        q.beta = s->z_beta;
+        q.kl_coef = s->kl_coef;
+        moe::plan::plan_kernel<<<1, moe::plan::kThreads, 0, st>>>(q);
+        count_launch();
         return launch_status();
     }
     const int splits = gate_splits(s);
@@ -546,20 +581,24 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 
 moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint16_t *x, int32_t *kept,
                         int32_t *offsets, int32_t *slot_of, int32_t *row_token, uint16_t *x_perm,
-                        const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr, bool permute = true) {
+                        const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr, bool permute = true,
+                        bool planned = false) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model;
     const int C = capacity_of(s);
     const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
     const int chunks = moe::dispatch::num_chunks(order.rank_major ? T * K : T);
     const int rows = T * K;
-    if (chunks == 1) {
+    if (planned) {
+        // the router's plan kernel has formed w.base, kept and offsets (token order)
+        moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
+            topk_idx, order, N, C, w.base, offsets, slot_of, row_token, rows);
+        count_launch();
+    } else if (chunks == 1) {
         // a decode-sized batch: count, scan and assign in one block
         moe::dispatch::dispatch_small_kernel<<<1, moe::dispatch::kChunk, (6 * (size_t)N + 1) * sizeof(int), st>>>(
             topk_idx, order, N, C, kept, offsets, slot_of, row_token, drop_rate, rows);
         count_launch();
     } else {
-        if (cudaMemsetAsync(row_token, 0xFF, sizeof(int32_t) * (size_t)rows, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
         moe::dispatch::count_kernel<<<chunks, moe::dispatch::kChunk, N * sizeof(int), st>>>(topk_idx, order, N,
                                                                                             w.hist);
         count_launch();
@@ -567,7 +606,7 @@ moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint1
                                                                      drop_rate, rows);
         count_launch();
         moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
-            topk_idx, order, N, C, w.base, offsets, slot_of, row_token);
+            topk_idx, order, N, C, w.base, offsets, slot_of, row_token, rows);
         count_launch();
     }
     if (permute) {
@@ -782,24 +821,42 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
 // x_perm: the regrouped rows; or, with gather_rows (bf16 weights only), the
 // first GEMM reads row gather_rows[r] of x for regrouped row r instead (x_perm
 // is then not read).
+// The routed experts' GEMM kernel and its m-tile shape: FP8 (64-row tiles, or
+// 128 token-major), the SM-pair kernel (256) or the single-SM kernel (128).
+struct FfnTiling {
+    bool fp8, pair_routed, pair_shared;
+    int tile_rows, raster;
+};
+FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
+    FfnTiling t;
+    int64_t per_expert = (int64_t)s->T * s->K / s->N;
+    const int C = capacity_of(s);
+    if (per_expert > C) per_expert = C;
+    t.fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
+    t.pair_routed = !t.fp8 && !gather && use_pair(per_expert);
+    t.pair_shared = !t.fp8 && use_pair(s->T);
+    t.tile_rows = t.fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
+                        : (t.pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
+    t.raster = t.pair_routed ? kRasterPair : kRasterSingle;
+    return t;
+}
+
+// tiles_ready: w.mtiles already holds the m-tile list of ffn_tiling(s, wt,
+// gather_rows != nullptr) (the router's plan kernel built it).
 moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm, const int32_t *offsets,
                    const moe_weights *wt, const uint16_t *x, uint16_t *y_perm, uint16_t *z,
-                   const FfnWs &w, cudaStream_t st, cudaEvent_t mid = nullptr, const int32_t *gather_rows = nullptr) {
+                   const FfnWs &w, cudaStream_t st, cudaEvent_t mid = nullptr, const int32_t *gather_rows = nullptr,
+                   bool tiles_ready = false) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model, f = s->d_ff;
     const int rows = T * K;
     const int mt = max_mtiles(s);
-    int64_t per_expert = (int64_t)T * K / N;
-    const int C = capacity_of(s);
-    if (per_expert > C) per_expert = C;
-    const bool fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
-    const bool pair_routed = !fp8 && gather_rows == nullptr && use_pair(per_expert);
-    const bool pair_shared = !fp8 && use_pair(T);
-    const int tile_rows = fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
-                              : (pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
-    moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, tile_rows,
-                                                     pair_routed ? kRasterPair : kRasterSingle, mt, w.mtiles,
-                                                     w.num_mtiles);
-    count_launch();
+    const FfnTiling tl = ffn_tiling(s, wt, gather_rows != nullptr);
+    const bool fp8 = tl.fp8, pair_routed = tl.pair_routed, pair_shared = tl.pair_shared;
+    if (!tiles_ready) {
+        moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, tl.tile_rows, tl.raster, mt, w.mtiles,
+                                                         w.num_mtiles);
+        count_launch();
+    }
     moe_status r;
     if (fp8) {
         // the same four GEMMs with FP8 expert weights and per-channel scales
@@ -1229,21 +1286,27 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
         return events == nullptr || events[i] == nullptr ||
                cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
     };
-    if (!mark(0)) return MOE_ERR_CUDA;
-    if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
-                       st, z_loss, aux_kl, health, mean_weight)) != MOE_OK)
-        return r;
-    if (!mark(1)) return MOE_ERR_CUDA;
     // bf16 experts: the first expert GEMM gathers its rows from x by row_token,
     // so the regrouped copy of x is never written (FP8 experts read x_perm)
     const bool gather = weights->format == MOE_WEIGHTS_BF16;
+    // the fused router's plan kernel also forms the dispatch plan (token-order
+    // capacity) and the m-tile list
+    const bool planned = fused_route(shape) && shape->drop_policy == MOE_DROP_TOKEN_ORDER;
+    const FfnTiling tl = ffn_tiling(shape, weights, gather);
+    const DispatchPlan dplan{capacity_of(shape), w.disp.base, kept, offsets, tl.tile_rows, tl.raster,
+                             max_mtiles(shape), w.ffn.mtiles, w.ffn.num_mtiles};
+    if (!mark(0)) return MOE_ERR_CUDA;
+    if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
+                       st, z_loss, aux_kl, health, mean_weight, planned ? &dplan : nullptr)) != MOE_OK)
+        return r;
+    if (!mark(1)) return MOE_ERR_CUDA;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st,
-                          health ? health + 1 : nullptr, !gather)) != MOE_OK)
+                          health ? health + 1 : nullptr, !gather, planned)) != MOE_OK)
         return r;
     if (!mark(2)) return MOE_ERR_CUDA;
     cudaEvent_t mid = events ? reinterpret_cast<cudaEvent_t>(events[3]) : nullptr;
     if ((r = run_ffn(shape, dev, w.x_perm, offsets, weights, x, w.y_perm, w.z, w.ffn, st, mid,
-                     gather ? w.row_token : nullptr)) != MOE_OK)
+                     gather ? w.row_token : nullptr, planned)) != MOE_OK)
         return r;
     if (!mark(4)) return MOE_ERR_CUDA;
     if ((r = run_combine(shape, w.y_perm, slot_of, topk_w, w.z, y, st)) != MOE_OK) return r;

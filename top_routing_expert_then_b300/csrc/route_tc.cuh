@@ -3,8 +3,8 @@
 //   s = W_g x                      (lmnt.cn/news/351908 sec. 2.1)
 //   TopK over s + b, then softmax over the K kept unbiased logits
 //   demand[e], sum_t softmax_N(s_t)[e], sum_t logsumexp(s_t)^2   (sec. 5.2-5.3)
-// and, in the last block to finish, the balance loss, the router z-loss and
-// the KL(uniform || f) loss variant.
+// and per-tile rows of the statistics from which the plan kernel forms the
+// balance loss, the router z-loss and the KL(uniform || f) loss variant.
 //
 // Work split. A tile is 128 tokens. The d_model reduction of one tile is split
 // over a cluster of S CTAs (S in {1, 2, 4, 8}, chosen from T and d_model only,
@@ -29,9 +29,10 @@
 // Statistics without floating-point atomics: per-expert probability sums are
 // accumulated as unsigned 64-bit fixed point (2^-31 units; each fp32
 // probability rounds to that grid with a 32-bit conversion, then integer
-// additions in any order give the same total), demand as integers. Each block adds its totals to global
-// counters; the last block (ticket on a counter) converts them and forms the
-// losses with fp32 terms and compensated fp32 sums in a fixed order.
+// additions in any order give the same total), demand as integers. The CTAs
+// of a cluster add theirs into one row per 128-token tile (the dispatch's
+// per-chunk histogram is that row's counts); a single-block plan kernel
+// (dispatch.cuh) reduces the rows into demand, prob_sum and the losses.
 #pragma once
 
 #include <cuda.h>
@@ -75,16 +76,12 @@ struct Params {
     const float *sel_bias;
     int32_t *topk_idx;
     float *topk_w;
-    // zeroed by the caller before the launch, contiguous
-    unsigned long long *prob_acc;  // [N] sum_t softmax_N(s_t)[e] in 2^-31 units
-    int32_t *dem_acc;              // [N] assignments per expert
-    unsigned long long *w_acc;     // [N] sum of the routing weights given to e, 2^-31 units
-    unsigned int *done;            // finished-block ticket
-    float *lse_partial;            // [gridDim.x][4] per-block sums of logsumexp^2 and entropy, max |logit|
-    // written by the last block (demand and prob_sum required)
-    int32_t *demand;
-    float *prob_sum, *aux, *z_loss, *aux_kl, *health, *mean_weight;
-    float alpha, beta, kl_coef;
+    // per 128-token tile (row = tile, the S CTAs of its cluster added up in rank
+    // order; every row is written, nothing needs zeroing beforehand):
+    int32_t *tile_hist;             // [tiles][N] assignments to e among the tile's tokens
+    unsigned long long *tile_prob;  // [tiles][N] sum of softmax_N(s_t)[e], 2^-31 units
+    unsigned long long *tile_w;     // [tiles][N] sum of the routing weights given to e, 2^-31 units
+    float *lse_partial;             // [gridDim.x][4] per-CTA sums of logsumexp^2 and entropy, max |logit|
 };
 
 struct Shared {
@@ -94,11 +91,8 @@ struct Shared {
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
-    int last;
     float lsq_w[kWarps], ent_w[kWarps], amax_w[kWarps];
     float bias[kMaxN];
-    route::KSum red[5 * 32];
-    float mred[32];
     int dcount[kMaxN];
     unsigned long long pacc[kMaxN];
     unsigned long long wacc[kMaxN];
@@ -158,6 +152,17 @@ __device__ __forceinline__ void mma_bf16_id(uint32_t d_tmem, uint64_t a, uint64_
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t cluster_addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
@@ -542,11 +547,6 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < N; e += kThreads) {
-        if (sh.pacc[e] != 0ull) atomicAdd(p.prob_acc + e, sh.pacc[e]);
-        if (sh.dcount[e] != 0) atomicAdd(p.dem_acc + e, sh.dcount[e]);
-        if (sh.wacc[e] != 0ull) atomicAdd(p.w_acc + e, sh.wacc[e]);
-    }
     if (threadIdx.x == 0) {
         float a = 0.f, b = 0.f, c = 0.f;
         for (int w = 0; w < kWarps; ++w) {
@@ -559,18 +559,35 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         p.lse_partial[(size_t)blockIdx.x * route::kPartialStride + 2] = c;
     }
 
-    // -------------------------------------------------------- last block: totals and losses
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();  // this block's totals (ordered before by the barrier) precede the ticket
-        sh.last = atomicAdd(p.done, 1u) == gridDim.x - 1;
+    // -------------------------------------------------------- the tile's per-expert row
+    // The S CTAs of the cluster route disjoint token ranges of one 128-token
+    // tile; CTA r adds their counts and fixed-point sums for experts
+    // r, r + S, ... in rank order (integers: any order gives the same total)
+    // and writes them. No global atomics, no zeroed counters, no ticket.
+    const size_t row = (size_t)(blockIdx.x / (unsigned)S) * N;
+    if (S == 1) {
+        for (int e = threadIdx.x; e < N; e += kThreads) {
+            p.tile_hist[row + e] = sh.dcount[e];
+            p.tile_prob[row + e] = sh.pacc[e];
+            p.tile_w[row + e] = sh.wacc[e];
+        }
+    } else {
+        gg::cluster_sync_all();  // every CTA's per-expert totals are visible cluster-wide
+        for (int e = (int)rank + S * (int)threadIdx.x; e < N; e += S * kThreads) {
+            uint32_t dc = 0;
+            unsigned long long pa = 0ull, wa = 0ull;
+#pragma unroll
+            for (int sp = 0; sp < S; ++sp) {
+                dc += ld_dsmem_u32(gg::map_to_rank(gg::smem_u32(&sh.dcount[e]), (uint32_t)sp));
+                pa += ld_dsmem_u64(gg::map_to_rank(gg::smem_u32(&sh.pacc[e]), (uint32_t)sp));
+                wa += ld_dsmem_u64(gg::map_to_rank(gg::smem_u32(&sh.wacc[e]), (uint32_t)sp));
+            }
+            p.tile_hist[row + e] = (int32_t)dc;
+            p.tile_prob[row + e] = pa;
+            p.tile_w[row + e] = wa;
+        }
+        gg::cluster_sync_all();  // the peers have finished reading this CTA's totals
     }
-    __syncthreads();
-    if (!sh.last) return;
-    __threadfence();
-    route::block_losses(N, p.T, K, p.demand, p.prob_sum, p.lse_partial, (int)gridDim.x, p.w_acc, p.alpha, p.beta,
-                        p.kl_coef, p.aux, p.z_loss, p.aux_kl, p.health, p.mean_weight, sh.red, sh.mred, p.prob_acc,
-                        p.dem_acc, kProbUnit);
 }
 
 }  // namespace rtc
