@@ -1131,12 +1131,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 // The m-tile list of the routed experts, from the expert offsets:
 // expert e owns rows [offsets[e], offsets[e+1]) and ceil(rows / tile_rows)
 // tiles, grouped for rasterisation (see tile_of). Called by all threads of a
-// block of 1024 (N <= 1024, at most 65535 tiles); `offsets` may be global or
-// shared memory; sc is 1024 ints of shared scratch.
+// block of blockDim.x >= N threads (at most 65535 tiles); `offsets` may be
+// global or shared memory; sc is blockDim.x ints of shared scratch.
 __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N, int total_rows, int tile_rows,
                                                    int raster, int max_tiles, int4 *__restrict__ mtiles,
                                                    int *__restrict__ num_mtiles, int *sc) {
-    const int e = threadIdx.x;
+    const int e = threadIdx.x, nthr = blockDim.x;
     int cnt = 0, r0 = 0, r1 = 0;
     bool bad = false;
     if (e < N) {
@@ -1152,7 +1152,7 @@ __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N
     sc[e] = cnt;
     __syncthreads();
     int v = cnt;
-    for (int o = 1; o < 1024; o <<= 1) {
+    for (int o = 1; o < nthr; o <<= 1) {
         int add = (e >= o) ? sc[e - o] : 0;
         __syncthreads();
         sc[e] = v = v + add;
@@ -1174,7 +1174,7 @@ __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N
             mtiles[m] = make_int4(rr, rows, e, ((start + lo) << 16) | (hi - lo));
         }
     }
-    if (e == 1023) *num_mtiles = v < max_tiles ? v : max_tiles;
+    if (e == nthr - 1) *num_mtiles = v < max_tiles ? v : max_tiles;
 }
 
 __global__ void __launch_bounds__(1024)

@@ -446,13 +446,28 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
 
 // The dispatch plan the fused router's plan kernel also forms (forward path):
 // per-chunk bases, kept counts, expert offsets and the grouped GEMMs' m-tile list.
-struct DispatchPlan {
-    int C;
-    int32_t *base, *kept, *offsets;
-    int tile_rows, raster, max_tiles;
-    int4 *mtiles;
-    int *num_mtiles;
-};
+using DispatchPlan = moe::plan::Dispatch;
+
+moe::plan::Stats plan_stats(const moe_shape *s, const RouteWs &w, int32_t *demand, float *prob_sum, float *aux,
+                            float *z_loss, float *aux_kl, float *health, float *mean_weight) {
+    moe::plan::Stats q{};
+    q.T = s->T;
+    q.N = s->N;
+    q.K = s->K;
+    q.route_blocks = fused_route_grid(s);
+    q.lse_partial = w.lse_partial;
+    q.demand = demand;
+    q.prob_sum = prob_sum;
+    q.aux = aux;
+    q.z_loss = z_loss;
+    q.aux_kl = aux_kl;
+    q.health = health;
+    q.mean_weight = mean_weight;
+    q.alpha = s->aux_alpha;
+    q.beta = s->z_beta;
+    q.kl_coef = s->kl_coef;
+    return q;
+}
 
 moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, const uint16_t *Wg,
                      const float *sel_bias, int32_t *topk_idx, float *topk_w, int32_t *demand,
@@ -482,6 +497,11 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         p.tile_prob = w.tile_prob;
         p.tile_w = w.tile_w;
         p.lse_partial = w.lse_partial;
+        // a single-tile batch on the forward path: the router forms the plan itself
+        const bool in_router = dplan != nullptr && moe::rtc::num_tiles(T) == 1;
+        p.fuse_plan = in_router ? 1 : 0;
+        p.st = plan_stats(s, w, demand, prob_sum, aux, z_loss, aux_kl, health, mean_weight);
+        if (dplan != nullptr) p.dp = *dplan;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)fused_route_grid(s));
         cfg.blockDim = dim3(moe::rtc::kThreads);
@@ -503,39 +523,16 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
+        if (in_router) return launch_status();
         // one block: statistics and losses from the per-tile rows (and, on the
         // forward path, the dispatch plan and the m-tile list)
         moe::plan::Params q{};
-        q.T = T;
-        q.N = N;
-        q.K = K;
+        q.st = plan_stats(s, w, demand, prob_sum, aux, z_loss, aux_kl, health, mean_weight);
+        if (dplan != nullptr) q.dp = *dplan;
         q.tiles = moe::rtc::num_tiles(T);
-        q.route_blocks = fused_route_grid(s);
         q.tile_hist = w.tile_hist;
         q.tile_prob = w.tile_prob;
         q.tile_w = w.tile_w;
-        q.lse_partial = w.lse_partial;
-        if (dplan != nullptr) {
-            q.C = dplan->C;
-            q.base = dplan->base;
-            q.kept = dplan->kept;
-            q.offsets = dplan->offsets;
-            q.tile_rows = dplan->tile_rows;
-            q.raster = dplan->raster;
-            q.max_tiles = dplan->max_tiles;
-            q.mtiles = dplan->mtiles;
-            q.num_mtiles = dplan->num_mtiles;
-        }
-        q.demand = demand;
-        q.prob_sum = prob_sum;
-        q.aux = aux;
-        q.z_loss = z_loss;
-        q.aux_kl = aux_kl;
-        q.health = health;
-        q.mean_weight = mean_weight;
-        q.alpha = s->aux_alpha;
-        q.beta = s->z_beta;
-        q.kl_coef = s->kl_coef;
         moe::plan::plan_kernel<<<1, moe::plan::kThreads, 0, st>>>(q);
         count_launch();
         return launch_status();
@@ -582,13 +579,15 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
 moe_status run_dispatch(const moe_shape *s, const int32_t *topk_idx, const uint16_t *x, int32_t *kept,
                         int32_t *offsets, int32_t *slot_of, int32_t *row_token, uint16_t *x_perm,
                         const DispatchWs &w, cudaStream_t st, float *drop_rate = nullptr, bool permute = true,
-                        bool planned = false) {
+                        bool planned = false, bool placed = false) {
     const int T = s->T, N = s->N, K = s->K, d = s->d_model;
     const int C = capacity_of(s);
     const moe::dispatch::Order order{T, K, s->drop_policy == MOE_DROP_RANK_ORDER ? 1 : 0};
     const int chunks = moe::dispatch::num_chunks(order.rank_major ? T * K : T);
     const int rows = T * K;
-    if (planned) {
+    if (placed) {
+        // the router has placed the assignments itself (a single-tile batch)
+    } else if (planned) {
         // the router's plan kernel has formed w.base, kept and offsets (token order)
         moe::dispatch::assign_kernel<<<chunks, moe::dispatch::kChunk, 4 * N * sizeof(unsigned), st>>>(
             topk_idx, order, N, C, w.base, offsets, slot_of, row_token, rows);
@@ -1292,16 +1291,17 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     // the fused router's plan kernel also forms the dispatch plan (token-order
     // capacity) and the m-tile list
     const bool planned = fused_route(shape) && shape->drop_policy == MOE_DROP_TOKEN_ORDER;
+    const bool placed = planned && moe::rtc::num_tiles(shape->T) == 1;  // the router places them itself
     const FfnTiling tl = ffn_tiling(shape, weights, gather);
     const DispatchPlan dplan{capacity_of(shape), w.disp.base, kept, offsets, tl.tile_rows, tl.raster,
-                             max_mtiles(shape), w.ffn.mtiles, w.ffn.num_mtiles};
+                             max_mtiles(shape), w.ffn.mtiles, w.ffn.num_mtiles, slot_of, w.row_token};
     if (!mark(0)) return MOE_ERR_CUDA;
     if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
                        st, z_loss, aux_kl, health, mean_weight, planned ? &dplan : nullptr)) != MOE_OK)
         return r;
     if (!mark(1)) return MOE_ERR_CUDA;
     if ((r = run_dispatch(shape, topk_idx, x, kept, offsets, slot_of, w.row_token, w.x_perm, w.disp, st,
-                          health ? health + 1 : nullptr, !gather, planned)) != MOE_OK)
+                          health ? health + 1 : nullptr, !gather, planned, placed)) != MOE_OK)
         return r;
     if (!mark(2)) return MOE_ERR_CUDA;
     cudaEvent_t mid = events ? reinterpret_cast<cudaEvent_t>(events[3]) : nullptr;

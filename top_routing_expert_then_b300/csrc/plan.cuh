@@ -1,6 +1,6 @@
-// plan.cuh -- the single-block step between the fused router and the
-// dispatch's assign kernel: it turns the router's per-tile rows (one row of
-// per-expert counts and fixed-point sums per 128-token tile) into
+// plan.cuh -- the step between the fused router and the expert GEMMs: from
+// the router's per-tile rows (one row of per-expert counts and fixed-point
+// sums per 128-token tile) it forms
 //   the dispatch plan  (lmnt.cn/news/351908 sec. 3.1, 3.3)
 //     base[c][e]  = assignments to e in tiles before c (exclusive prefix),
 //     demand[e]   = all assignments to e, kept[e] = min(demand[e], C),
@@ -14,6 +14,9 @@
 //              (the CSDN page's MoELayer KL balance loss; +inf for an idle expert),
 //     health = [std_e f_e, drop rate, mean routing entropy, max |logit|],
 //     mean_weight[e] = mean routing weight of the assignments to e.
+// plan_kernel does this in one block of 1024 threads for any number of
+// tiles; a single-tile batch (decode) does it inside the router kernel with
+// the block-level pieces below, which also place its assignments.
 // Every sum runs in a fixed order, so results do not depend on scheduling:
 // integers for the counts and the fixed-point probability and weight sums;
 // fp32 for the few hundred loss terms, each a non-negative quantity added in a
@@ -33,23 +36,33 @@ namespace plan {
 constexpr int kThreads = 1024;
 constexpr float kFixUnit = 1.0f / 2147483648.0f;  // 2^-31, the routers' fixed-point unit
 
-struct Params {
-    int T, N, K, C;
-    int tiles;                        // rows of the tile tables (128-token tiles)
-    int route_blocks;                 // rows of lse_partial
-    const int32_t *tile_hist;         // [tiles][N]
-    const unsigned long long *tile_prob, *tile_w;  // [tiles][N]
-    const float *lse_partial;         // [route_blocks][route::kPartialStride]
-    // dispatch plan (base == nullptr: statistics only)
-    int32_t *base, *kept, *offsets;
-    // m-tile list (mtiles == nullptr: none)
-    int tile_rows, raster, max_tiles;
-    int4 *mtiles;
-    int *num_mtiles;
-    // statistics (demand and prob_sum required; the rest may be null)
+// What the statistics need and where they go (demand and prob_sum required;
+// the rest may be null).
+struct Stats {
+    int T, N, K;
+    int route_blocks;            // rows of lse_partial
+    const float *lse_partial;    // [route_blocks][route::kPartialStride]
     int32_t *demand;
     float *prob_sum, *aux, *z_loss, *aux_kl, *health, *mean_weight;
     float alpha, beta, kl_coef;
+};
+
+// The dispatch plan's outputs (base == nullptr: statistics only).
+struct Dispatch {
+    int C;
+    int32_t *base, *kept, *offsets;
+    int tile_rows, raster, max_tiles;  // m-tile list (mtiles == nullptr: none)
+    int4 *mtiles;
+    int *num_mtiles;
+    int32_t *slot_of, *row_token;      // single-tile batches placed by the router itself
+};
+
+struct Params {
+    Stats st;
+    Dispatch dp;
+    int tiles;                                     // rows of the tile tables
+    const int32_t *tile_hist;                      // [tiles][N]
+    const unsigned long long *tile_prob, *tile_w;  // [tiles][N]
 };
 
 // Pairwise sum over the 32 lanes of a warp (fixed order; valid in every lane).
@@ -59,16 +72,133 @@ __device__ __forceinline__ float warp_tree_sum(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
-    __shared__ int s_kept[1024];
-    __shared__ int s_off[1025];
-    __shared__ int sc[1024];
-    __shared__ float t_aux[1024], t_kl[1024], t_var[1024];  // per-expert loss terms
-    const int N = p.N, tid = threadIdx.x;
+// kept[e] = min(demand[e], C) and the expert offsets (exclusive scan; s_off
+// in shared memory gets offsets[0..N]). All threads of a block of
+// blockDim.x >= N; sc: blockDim.x ints of shared scratch.
+__device__ __forceinline__ void expert_offsets(const int *s_dem, int N, int C, int *s_off, int *sc,
+                                               int32_t *kept, int32_t *offsets) {
+    const int tid = threadIdx.x;
+    int v = tid < N ? min(s_dem[tid], C) : 0;
+    if (tid < N) kept[tid] = v;
+    sc[tid] = v;
+    __syncthreads();
+    for (int o = 1; o < N; o <<= 1) {
+        const int add = tid >= o ? sc[tid - o] : 0;
+        __syncthreads();
+        sc[tid] = v = v + add;
+        __syncthreads();
+    }
+    if (tid < N) {
+        s_off[tid + 1] = v;
+        offsets[tid + 1] = v;
+    }
+    if (tid == 0) {
+        s_off[0] = 0;
+        offsets[0] = 0;
+    }
+    __syncthreads();
+}
 
-    // ---- per expert: counts and sums over the tiles. G lanes (a power of two
-    // <= 32) share an expert; lane j of the group takes a contiguous run of
-    // tiles, so the tile order is kept by an exclusive scan across the group.
+// The losses and health statistics from the per-expert totals s_dem / s_prob
+// (shared) and the router blocks' partial sums. kept_rows >= 0 also gives the
+// drop rate. All threads of a block of blockDim.x >= max(N, 64); t_aux, t_kl,
+// t_var: N floats of shared scratch each.
+__device__ __forceinline__ void losses(const Stats &q, const int *s_dem, const float *s_prob, float *t_aux,
+                                       float *t_kl, float *t_var, int kept_rows) {
+    const int N = q.N, tid = threadIdx.x;
+    const float TKf = (float)q.T * (float)q.K, Tf = (float)q.T, inv_n = 1.0f / (float)N;
+    if (tid < N) {
+        const int dem = s_dem[tid];
+        const float f = (float)dem / TKf;
+        t_aux[tid] = f * (s_prob[tid] / Tf);
+        t_kl[tid] = q.aux_kl != nullptr ? route::kl_summand(dem, (long long)q.T * q.K, N) : 0.f;
+        t_var[tid] = (f - inv_n) * (f - inv_n);
+    }
+    __syncthreads();
+    const int warp = warp_id(), lane = lane_id();
+    if (warp == 0) {
+        float a = 0.f, k = 0.f, v = 0.f;
+        for (int i = lane; i < N; i += 32) {
+            a += t_aux[i];
+            k += t_kl[i];
+            v += t_var[i];
+        }
+        a = warp_tree_sum(a);
+        k = warp_tree_sum(k);
+        v = warp_tree_sum(v);
+        if (lane == 0) {
+            if (q.aux != nullptr) q.aux[0] = q.alpha * (float)N * a;
+            if (q.aux_kl != nullptr) q.aux_kl[0] = q.kl_coef * k;
+            if (q.health != nullptr) {
+                q.health[0] = sqrtf(v * inv_n);
+                if (kept_rows >= 0) q.health[1] = (float)(q.T * q.K - kept_rows) / TKf;
+            }
+        }
+    } else if (warp == 1) {
+        float l = 0.f, en = 0.f, am = 0.f;
+        for (int r = lane; r < q.route_blocks; r += 32) {
+            l += __ldcg(q.lse_partial + (size_t)r * route::kPartialStride);
+            en += __ldcg(q.lse_partial + (size_t)r * route::kPartialStride + 1);
+            am = fmaxf(am, __ldcg(q.lse_partial + (size_t)r * route::kPartialStride + 2));
+        }
+        l = warp_tree_sum(l);
+        en = warp_tree_sum(en);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) {
+            if (q.z_loss != nullptr) q.z_loss[0] = q.beta * (l / Tf);
+            if (q.health != nullptr) {
+                q.health[2] = en / Tf;
+                q.health[3] = am;
+            }
+        }
+    }
+}
+
+// Places the assignments of a batch of T <= blockDim.x tokens in token order
+// (the dispatch's position rule: assignment (t, k) to expert e gets position
+// p = number of tokens t' < t that chose e, and is kept iff p < C): thread t
+// owns token t; bits (blockDim.x / 32 x N words of shared scratch) mark, per
+// warp and expert, the warp's tokens that chose it. Writes slot_of, and
+// row_token (-1 past offsets[N], up to `rows`). All threads.
+__device__ __forceinline__ void assign_tokens(const int32_t *topk_idx, int T, int K, int N, int C, const int *s_off,
+                                              unsigned *bits, int32_t *slot_of, int32_t *row_token, int rows) {
+    const int tid = threadIdx.x, w = warp_id(), lane = lane_id(), nw = blockDim.x / 32;
+    for (int i = tid; i < nw * N; i += blockDim.x) bits[i] = 0u;
+    for (int r = s_off[N] + tid; r < rows; r += blockDim.x) row_token[r] = -1;
+    __syncthreads();
+    if (tid < T)
+        for (int k = 0; k < K; ++k) {
+            const int e = __ldcg(topk_idx + (size_t)tid * K + k);
+            if (e >= 0 && e < N) atomicOr(&bits[w * N + e], 1u << lane);
+        }
+    __syncthreads();
+    const unsigned below = (1u << lane) - 1u;
+    for (int k = 0; k < (tid < T ? K : 0); ++k) {
+        const int e = __ldcg(topk_idx + (size_t)tid * K + k);
+        int slot = -1;
+        if (e >= 0 && e < N) {
+            int pos = __popc(bits[w * N + e] & below);
+            for (int w2 = 0; w2 < w; ++w2) pos += __popc(bits[w2 * N + e]);
+            if (pos < C) {
+                slot = s_off[e] + pos;
+                row_token[slot] = tid;
+            }
+        } else {
+            flag_error(MOE_DEVERR_EXPERT_ID);
+        }
+        slot_of[(size_t)tid * K + k] = slot;
+    }
+}
+
+// One block of 1024 threads: per-expert totals over the tiles (G lanes, a
+// power of two <= 32, share an expert; lane j of the group takes a contiguous
+// run of tiles, so the tile order is kept by an exclusive scan across the
+// group), then the plan, the m-tile list and the statistics.
+__global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
+    __shared__ int s_dem[1024], s_off[1025], sc[1024];
+    __shared__ float s_prob[1024], t_aux[1024], t_kl[1024], t_var[1024];
+    const int N = p.st.N, tid = threadIdx.x;
     int G = 32;
     while (G > 1 && G * N > kThreads) G >>= 1;
     const int e = tid / G, j = tid % G;
@@ -93,100 +223,33 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
         wr += __shfl_xor_sync(0xffffffffu, wr, o, G);
     }
     const int dem = __shfl_sync(0xffffffffu, incl, G - 1, G);
-    if (e < N && p.base != nullptr) {
+    if (e < N && p.dp.base != nullptr) {
         int run = incl - cnt;
         for (int c = c0; c < c1; ++c) {
             const size_t i = (size_t)c * N + e;
-            p.base[i] = run;
+            p.dp.base[i] = run;
             run += __ldcg(p.tile_hist + i);
         }
     }
-    const float prob = __ull2float_rn(pr) * kFixUnit;  // the integer total rounded once, then scaled exactly
     if (e < N && j == 0) {
-        p.demand[e] = dem;
-        p.prob_sum[e] = prob;
-        if (p.mean_weight != nullptr) p.mean_weight[e] = dem > 0 ? __ull2float_rn(wr) * kFixUnit / (float)dem : 0.f;
-    }
-
-    // ---- kept rows and the expert offsets (exclusive scan over the experts)
-    const bool lead = e < N && j == 0;
-    if (p.base != nullptr) {
-        if (tid < N) s_kept[tid] = 0;
-        __syncthreads();
-        if (lead) s_kept[e] = min(dem, p.C);
-        __syncthreads();
-        int v = tid < N ? s_kept[tid] : 0;
-        sc[tid] = v;
-        __syncthreads();
-        for (int o = 1; o < N; o <<= 1) {
-            const int add = tid >= o ? sc[tid - o] : 0;
-            __syncthreads();
-            sc[tid] = v = v + add;
-            __syncthreads();
-        }
-        if (tid < N) {
-            s_off[tid + 1] = v;
-            p.kept[tid] = s_kept[tid];
-            p.offsets[tid + 1] = v;
-        }
-        if (tid == 0) {
-            s_off[0] = 0;
-            p.offsets[0] = 0;
-        }
-        __syncthreads();
-        if (p.mtiles != nullptr)
-            gg::build_mtiles_block(s_off, N, p.T * p.K, p.tile_rows, p.raster, p.max_tiles, p.mtiles, p.num_mtiles,
-                                   sc);
-    }
-
-    // ---- losses and health: per-expert terms, then warp 0 adds the expert
-    // terms and warp 1 the router blocks' partial sums, each in a fixed order
-    const float TKf = (float)p.T * (float)p.K, Tf = (float)p.T, inv_n = 1.0f / (float)N;
-    if (lead) {
-        const float f = (float)dem / TKf;
-        t_aux[e] = f * (prob / Tf);
-        t_kl[e] = p.aux_kl != nullptr ? route::kl_summand(dem, (long long)p.T * p.K, N) : 0.f;
-        t_var[e] = (f - inv_n) * (f - inv_n);
+        const float prob = __ull2float_rn(pr) * kFixUnit;  // the integer total rounded once, then scaled exactly
+        s_dem[e] = dem;
+        s_prob[e] = prob;
+        p.st.demand[e] = dem;
+        p.st.prob_sum[e] = prob;
+        if (p.st.mean_weight != nullptr)
+            p.st.mean_weight[e] = dem > 0 ? __ull2float_rn(wr) * kFixUnit / (float)dem : 0.f;
     }
     __syncthreads();
-    const int warp = warp_id(), lane = lane_id();
-    if (warp == 0) {
-        float a = 0.f, k = 0.f, v = 0.f;
-        for (int i = lane; i < N; i += 32) {
-            a += t_aux[i];
-            k += t_kl[i];
-            v += t_var[i];
-        }
-        a = warp_tree_sum(a);
-        k = warp_tree_sum(k);
-        v = warp_tree_sum(v);
-        if (lane == 0) {
-            if (p.aux != nullptr) p.aux[0] = p.alpha * (float)N * a;
-            if (p.aux_kl != nullptr) p.aux_kl[0] = p.kl_coef * k;
-            if (p.health != nullptr) {
-                p.health[0] = sqrtf(v * inv_n);
-                if (p.base != nullptr) p.health[1] = (float)(p.T * p.K - s_off[N]) / TKf;
-            }
-        }
-    } else if (warp == 1) {
-        float l = 0.f, en = 0.f, am = 0.f;
-        for (int r = lane; r < p.route_blocks; r += 32) {
-            l += __ldcg(p.lse_partial + (size_t)r * route::kPartialStride);
-            en += __ldcg(p.lse_partial + (size_t)r * route::kPartialStride + 1);
-            am = fmaxf(am, __ldcg(p.lse_partial + (size_t)r * route::kPartialStride + 2));
-        }
-        l = warp_tree_sum(l);
-        en = warp_tree_sum(en);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        if (lane == 0) {
-            if (p.z_loss != nullptr) p.z_loss[0] = p.beta * (l / Tf);
-            if (p.health != nullptr) {
-                p.health[2] = en / Tf;
-                p.health[3] = am;
-            }
-        }
+    int kept_rows = -1;
+    if (p.dp.base != nullptr) {
+        expert_offsets(s_dem, N, p.dp.C, s_off, sc, p.dp.kept, p.dp.offsets);
+        kept_rows = s_off[N];
+        if (p.dp.mtiles != nullptr)
+            gg::build_mtiles_block(s_off, N, p.st.T * p.st.K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles,
+                                   p.dp.mtiles, p.dp.num_mtiles, sc);
     }
+    losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, kept_rows);
 }
 
 }  // namespace plan

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "grouped_gemm.cuh"
+#include "plan.cuh"
 #include "route.cuh"
 
 namespace moe {
@@ -82,6 +83,12 @@ struct Params {
     unsigned long long *tile_prob;  // [tiles][N] sum of softmax_N(s_t)[e], 2^-31 units
     unsigned long long *tile_w;     // [tiles][N] sum of the routing weights given to e, 2^-31 units
     float *lse_partial;             // [gridDim.x][4] per-CTA sums of logsumexp^2 and entropy, max |logit|
+    // a single-tile batch (T <= 128) with fuse_plan: CTA rank 0 also forms the
+    // statistics, the dispatch plan and the m-tile list and places the
+    // assignments (slot_of, row_token), so no plan or assign kernel follows
+    int fuse_plan;
+    plan::Stats st;
+    plan::Dispatch dp;
 };
 
 struct Shared {
@@ -587,6 +594,40 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             p.tile_w[row + e] = wa;
         }
         gg::cluster_sync_all();  // the peers have finished reading this CTA's totals
+    }
+
+    // -------------------------------------------------------- single tile: the plan here
+    // Every CTA's rows, routing weights and expert ids are visible to CTA 0
+    // after the cluster barrier above (release / acquire at cluster scope);
+    // the operand ring is free, so its shared memory is the scratch.
+    if (p.fuse_plan && rank == 0) {
+        __syncthreads();  // (one CTA: its own row writes)
+        int *s_dem = reinterpret_cast<int *>(smem);
+        float *s_prob = reinterpret_cast<float *>(s_dem + kMaxN);
+        int *s_off = reinterpret_cast<int *>(s_prob + kMaxN);  // kMaxN + 1
+        int *sc = s_off + kMaxN + 4;                             // kThreads
+        float *t_aux = reinterpret_cast<float *>(sc + kThreads);
+        float *t_kl = t_aux + kMaxN, *t_var = t_kl + kMaxN;
+        unsigned *bits = reinterpret_cast<unsigned *>(t_var + kMaxN);  // kWarps x N
+        for (int e = threadIdx.x; e < N; e += kThreads) {
+            const int dem = __ldcg(p.tile_hist + e);
+            const float prob = __ull2float_rn(__ldcg(p.tile_prob + e)) * plan::kFixUnit;
+            s_dem[e] = dem;
+            s_prob[e] = prob;
+            p.st.demand[e] = dem;
+            p.st.prob_sum[e] = prob;
+            if (p.st.mean_weight != nullptr)
+                p.st.mean_weight[e] =
+                    dem > 0 ? __ull2float_rn(__ldcg(p.tile_w + e)) * plan::kFixUnit / (float)dem : 0.f;
+        }
+        __syncthreads();
+        plan::expert_offsets(s_dem, N, p.dp.C, s_off, sc, p.dp.kept, p.dp.offsets);
+        plan::assign_tokens(p.topk_idx, p.T, K, N, p.dp.C, s_off, bits, p.dp.slot_of, p.dp.row_token, p.T * K);
+        __syncthreads();
+        if (p.dp.mtiles != nullptr)
+            gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles, p.dp.mtiles,
+                                   p.dp.num_mtiles, sc);
+        plan::losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, s_off[N]);
     }
 }
 
