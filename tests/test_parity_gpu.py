@@ -53,6 +53,9 @@ SMALL = [
     # a ragged last shared tile
     MoEConfig("shared_groups", 2100, 1024, 512, 16, 4, 0.0, has_shared=True, sel_bias=True),
     MoEConfig("shared_groups_n64", 4096, 512, 256, 64, 2, 1.0, has_shared=True),
+    # >= 1024 rows per expert and a long second reduction: the second expert
+    # GEMM runs on the SM-pair kernel (256-row tiles, ragged last tiles)
+    MoEConfig("pair_gemm2", 1100, 256, 8192, 2, 2, 0.0),
     # FP8 E4M3 expert weights (per-output-channel scales): several n-tiles, a
     # ragged expert, the shared expert, drops
     MoEConfig("fp8_experts", 700, 256, 640, 8, 2, 1.25, weights="fp8_e4m3"),

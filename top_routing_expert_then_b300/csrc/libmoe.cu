@@ -172,8 +172,10 @@ constexpr int kSplitRows = 128;
 constexpr int kMaxFp8Splits = 4;
 
 struct FfnWs {
-    int4 *mtiles;
+    int4 *mtiles;       // m-tile list of the first expert GEMM
     int *num_mtiles;
+    int4 *mtiles2;      // of the second, when its tiles differ (SM-pair kernel)
+    int *num_mtiles2;
     uint16_t *H;
     uint16_t *Hs;
     float *part;  // nullptr: no split-K
@@ -182,6 +184,8 @@ FfnWs carve_ffn(Carve &c, const moe_shape *s) {
     FfnWs w;
     w.mtiles = c.take<int4>((size_t)max_mtiles(s));
     w.num_mtiles = c.take<int>(4);
+    w.mtiles2 = c.take<int4>((size_t)max_mtiles(s));
+    w.num_mtiles2 = c.take<int>(4);
     w.H = c.take<uint16_t>((size_t)s->T * s->K * s->d_ff);
     w.Hs = s->has_shared ? c.take<uint16_t>((size_t)s->T * s->d_ff) : nullptr;
     const int64_t rows = (int64_t)s->T * s->K;
@@ -645,6 +649,18 @@ bool use_pair(int64_t expected_rows_per_group) {
     return false;
 }
 
+// The second expert GEMM on the SM-pair kernel by default when its tiles are
+// long and the experts' blocks large: measured on the Mixtral-shaped prefill
+// layer (about 1024 rows per expert, reduction 14336) it took 688 us against
+// 748 us on the single-SM kernel; with 640-row blocks (capacity factor 1.25,
+// each padded to 768) or a 4096-long reduction the single-SM kernel is faster.
+bool use_pair_gemm2(int64_t expected_rows_per_group, int k_dim) {
+    const int o = gemm_variant_override();
+    if (o == kSingle) return false;
+    if (o == kPair) return true;
+    return expected_rows_per_group >= 1024 && k_dim >= 8192;
+}
+
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows_n, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
@@ -823,8 +839,9 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
 // The routed experts' GEMM kernel and its m-tile shape: FP8 (64-row tiles, or
 // 128 token-major), the SM-pair kernel (256) or the single-SM kernel (128).
 struct FfnTiling {
-    bool fp8, pair_routed, pair_shared;
-    int tile_rows, raster;
+    bool fp8, pair_routed, pair_routed2, pair_shared;
+    int tile_rows, raster;    // first expert GEMM's m-tiles
+    int tile_rows2, raster2;  // second's (a second list is built when they differ)
 };
 FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
     FfnTiling t;
@@ -833,10 +850,13 @@ FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
     if (per_expert > C) per_expert = C;
     t.fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
     t.pair_routed = !t.fp8 && !gather && use_pair(per_expert);
+    t.pair_routed2 = !t.fp8 && use_pair_gemm2(per_expert, s->d_ff);
     t.pair_shared = !t.fp8 && use_pair(s->T);
     t.tile_rows = t.fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
                         : (t.pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
     t.raster = t.pair_routed ? kRasterPair : kRasterSingle;
+    t.tile_rows2 = t.fp8 ? t.tile_rows : (t.pair_routed2 ? moe::gg::PAIR_BM : moe::gg::BM);
+    t.raster2 = t.fp8 ? t.raster : (t.pair_routed2 ? kRasterPair : kRasterSingle);
     return t;
 }
 
@@ -851,10 +871,18 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     const int mt = max_mtiles(s);
     const FfnTiling tl = ffn_tiling(s, wt, gather_rows != nullptr);
     const bool fp8 = tl.fp8, pair_routed = tl.pair_routed, pair_shared = tl.pair_shared;
+    const bool two_lists = tl.tile_rows2 != tl.tile_rows;
+    const int4 *mtiles2 = two_lists ? w.mtiles2 : w.mtiles;
+    const int *num_mtiles2 = two_lists ? w.num_mtiles2 : w.num_mtiles;
     if (!tiles_ready) {
         moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, tl.tile_rows, tl.raster, mt, w.mtiles,
                                                          w.num_mtiles);
         count_launch();
+        if (two_lists) {
+            moe::gg::build_mtiles_kernel<<<1, 1024, 0, st>>>(offsets, N, rows, tl.tile_rows2, tl.raster2, mt,
+                                                             w.mtiles2, w.num_mtiles2);
+            count_launch();
+        }
     }
     moe_status r;
     if (fp8) {
@@ -892,8 +920,8 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
         if (r != MOE_OK) return r;
     }
     if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
-    r = launch_gemm(dev, pair_routed, w.H, rows, wt->W2, (uint64_t)N * d, f, d, N, wt->b2, y_perm, rows, w.mtiles,
-                    w.num_mtiles, mt, 0, false, st);
+    r = launch_gemm(dev, tl.pair_routed2, w.H, rows, wt->W2, (uint64_t)N * d, f, d, N, wt->b2, y_perm, rows,
+                    mtiles2, num_mtiles2, mt, 0, false, st);
     if (r != MOE_OK) return r;
     if (s->has_shared) {
         r = launch_gemm(dev, pair_shared, w.Hs, T, wt->Ws2, d, f, d, 1, wt->bs2, z, T, nullptr, nullptr, 0, T, false,
@@ -1293,8 +1321,10 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     const bool planned = fused_route(shape) && shape->drop_policy == MOE_DROP_TOKEN_ORDER;
     const bool placed = planned && moe::rtc::num_tiles(shape->T) == 1;  // the router places them itself
     const FfnTiling tl = ffn_tiling(shape, weights, gather);
+    const bool two_lists = tl.tile_rows2 != tl.tile_rows;
     const DispatchPlan dplan{capacity_of(shape), w.disp.base, kept, offsets, tl.tile_rows, tl.raster,
-                             max_mtiles(shape), w.ffn.mtiles, w.ffn.num_mtiles, slot_of, w.row_token};
+                             max_mtiles(shape), w.ffn.mtiles, w.ffn.num_mtiles, slot_of, w.row_token,
+                             tl.tile_rows2, tl.raster2, two_lists ? w.ffn.mtiles2 : nullptr, w.ffn.num_mtiles2};
     if (!mark(0)) return MOE_ERR_CUDA;
     if ((r = run_route(shape, dev, x, weights->Wg, sel_bias, topk_idx, topk_w, demand, prob_sum, aux, w.route,
                        st, z_loss, aux_kl, health, mean_weight, planned ? &dplan : nullptr)) != MOE_OK)

@@ -55,6 +55,9 @@ struct Dispatch {
     int4 *mtiles;
     int *num_mtiles;
     int32_t *slot_of, *row_token;      // single-tile batches placed by the router itself
+    int tile_rows2, raster2;           // a second m-tile list (mtiles2 == nullptr: none)
+    int4 *mtiles2;
+    int *num_mtiles2;
 };
 
 struct Params {
@@ -248,6 +251,10 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
         if (p.dp.mtiles != nullptr)
             gg::build_mtiles_block(s_off, N, p.st.T * p.st.K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles,
                                    p.dp.mtiles, p.dp.num_mtiles, sc);
+        __syncthreads();
+        if (p.dp.mtiles2 != nullptr)
+            gg::build_mtiles_block(s_off, N, p.st.T * p.st.K, p.dp.tile_rows2, p.dp.raster2, p.dp.max_tiles,
+                                   p.dp.mtiles2, p.dp.num_mtiles2, sc);
     }
     losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, kept_rows);
 }

@@ -627,6 +627,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         if (p.dp.mtiles != nullptr)
             gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles, p.dp.mtiles,
                                    p.dp.num_mtiles, sc);
+        __syncthreads();
+        if (p.dp.mtiles2 != nullptr)
+            gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows2, p.dp.raster2, p.dp.max_tiles, p.dp.mtiles2,
+                                   p.dp.num_mtiles2, sc);
         plan::losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, s_off[N]);
     }
 }
