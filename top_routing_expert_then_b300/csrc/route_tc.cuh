@@ -469,6 +469,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 
             // K rounds of arg-max on u = s + b over the unselected experts:
             // larger u first, equal u -> smaller expert id first
+            // (the rounds are not unrolled: with up to 8 rounds over up to 32
+            // experts per lane the unrolled body was large enough that
+            // instruction fetch, from a cold cache every layer, dominated)
             unsigned taken = 0u;
             int sel_e[route::kMaxK];
             float sel_s[route::kMaxK];
@@ -476,7 +479,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             for (int k = 0; k < route::kMaxK; ++k) {
                 sel_e[k] = -1;
                 sel_s[k] = 0.f;
-                if (k < K) {
+            }
+#pragma unroll 1
+            for (int k = 0; k < K; ++k) {
+                {
                     float bu = -INFINITY, bs = 0.f;
                     int be = 0x7fffffff;
 #pragma unroll
@@ -500,8 +506,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         }
                     }
                     if (be != 0x7fffffff && be % G == gl) taken |= 1u << (be / G);
-                    sel_e[k] = be;
-                    sel_s[k] = bs;
+#pragma unroll
+                    for (int q = 0; q < route::kMaxK; ++q)  // keeps the arrays in registers
+                        if (q == k) {
+                            sel_e[q] = be;
+                            sel_s[q] = bs;
+                        }
                 }
             }
             if (gl == 0 && live) {
