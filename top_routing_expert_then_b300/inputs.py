@@ -80,6 +80,9 @@ CONFIGS: Dict[str, MoEConfig] = {
     # weights instead of 15)
     "dsv3_slice16": MoEConfig("dsv3_slice16", 256, 7168, 2048, 16, 8, 0.0, has_shared=True, sel_bias=True,
                               note="16 experts of the DeepSeek-V3 shape, 128 rows per expert"),
+    # a larger slice (64 experts, 128 rows each) whose GEMMs run several waves of tiles
+    "dsv3_slice64": MoEConfig("dsv3_slice64", 1024, 7168, 2048, 64, 8, 0.0, has_shared=True, sel_bias=True,
+                              note="64 experts of the DeepSeek-V3 shape, 128 rows per expert"),
     "mixtral_decode16_fp8": MoEConfig("mixtral_decode16_fp8", 16, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
                                       note="Mixtral-shaped decode, 16 tokens, FP8 E4M3 expert weights"),
     "mixtral_decode64_fp8": MoEConfig("mixtral_decode64_fp8", 64, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
