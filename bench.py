@@ -246,16 +246,20 @@ def choose_peak(P, clk, region_ms: float):
 
 def ffn_work(cfg, R: int, hit: int):
     """Algorithmic FLOPs and bytes of one step's expert GEMMs: 4 d f FLOPs per
-    kept row (two Linears) plus the shared expert's per token; bytes = the
+    kept row (two Linears) plus the shared expert's per token. Bytes: the
     weights of every expert that received rows (+ the shared expert's, + one
-    fp32 scale per output channel with FP8) + x rows in, hidden rows out and
-    back in, output rows out."""
+    fp32 scale per output channel with FP8); x once (the bf16 path gathers the
+    kept rows of x inside the first GEMM; the FP8 path reads the regrouped
+    copy, one row per kept row, and the shared expert reads x); the hidden
+    rows written and read back; the output rows written (and z)."""
     T, d, f = cfg.T, cfg.d_model, cfg.d_ff
     flops = 4.0 * R * d * f + (4.0 * T * d * f if cfg.has_shared else 0.0)
     rows_all = R + (T if cfg.has_shared else 0)
     fp8 = cfg.weights == "fp8_e4m3"
     w_bytes = 2.0 * d * f * (1 if fp8 else 2) + ((d + f) * 4 if fp8 else 0)
-    nbytes = (hit + (1 if cfg.has_shared else 0)) * w_bytes + rows_all * (2 * d + 4 * f + 2 * d)
+    x_bytes = (R * 2 * d + (T * 2 * d if cfg.has_shared else 0)) if fp8 else T * 2 * d
+    nbytes = ((hit + (1 if cfg.has_shared else 0)) * w_bytes + x_bytes + rows_all * 4 * f
+              + R * 2 * d + (T * 2 * d if cfg.has_shared else 0))
     return flops, nbytes
 
 
@@ -351,7 +355,10 @@ def hbm_stages(cfg, m, P):
     """GB/s of the HBM-bound stages from their algorithmic bytes per step."""
     T, d, K, N, R = cfg.T, cfg.d_model, cfg.K, cfg.N, m["R"]
     route_bytes = T * d * 2 + N * d * 2 + T * K * 8 + N * 8
-    dispatch_bytes = T * K * 4 * 4 + T * d * 2 + R * d * 2
+    # token placement: topk_idx read, slot_of / row_token written, bases read;
+    # the x-row permute runs here only for FP8 experts (the bf16 path gathers
+    # the rows inside the first expert GEMM)
+    dispatch_bytes = T * K * 4 * 4 + ((T * d * 2 + R * d * 2) if cfg.weights != "bf16" else 0)
     combine_bytes = R * d * 2 + T * d * 2 + (T * d * 2 if cfg.has_shared else 0) + T * K * 8
     sm = m["stage_ms"]
     return {"route_aux": {"bytes": route_bytes, "gbs": route_bytes / (sm[0] * 1e-3) / 1e9},

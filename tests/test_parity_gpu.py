@@ -48,9 +48,8 @@ SMALL = [
     MoEConfig("multi_wave", 20000, 128, 128, 8, 2, 1.0),
     # general path (N > 256): CUDA-core tiled gate when N % 32 != 0
     MoEConfig("n300_gate_tiled", 257, 64, 64, 300, 3, 2.0),
-    # the shared expert's tiles inside the routed experts' GEMM launches: several
-    # raster groups of shared tiles spread through the tile list, long reductions,
-    # a ragged last shared tile
+    # a shared expert whose dense GEMMs span several raster groups of 128-row
+    # tiles (17 and 32 m-tiles), long reductions, a ragged last shared tile
     MoEConfig("shared_groups", 2100, 1024, 512, 16, 4, 0.0, has_shared=True, sel_bias=True),
     MoEConfig("shared_groups_n64", 4096, 512, 256, 64, 2, 1.0, has_shared=True),
     # >= 1024 rows per expert and a long second reduction: the second expert
