@@ -480,6 +480,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int total = num_m * num_n * splits;
     const int kblocks = p.k_dim / BK;
     const int kb_per_split = (kblocks + splits - 1) / splits;
+    // Balanced persistent schedule: the fewest blocks that finish the items
+    // in as many rounds as the whole grid would take; block b takes items b,
+    // b + stride, ... and blocks from stride on take none. A last round that
+    // would leave most of the grid idle is spread over the rounds instead,
+    // so a weight-streaming GEMM keeps every working block pulling from HBM
+    // until the end.
+    const int rounds = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int stride = rounds > 0 ? (total + rounds - 1) / rounds : (int)gridDim.x;
+    const int first = (int)blockIdx.x < stride ? (int)blockIdx.x : total;
 
     if (warp >= GATHER_WARP) {
         // ---------------------------------------------------- row-gather warps (a_rows mode)
@@ -519,7 +528,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
             };
             auto next_tile = [&](int w, Tile &t) {
-                for (; w < total; w += gridDim.x) {
+                for (; w < total; w += stride) {
                     t = tile_of<BM>(p, w / splits, num_m, num_n);
                     if (t.ok) return w;
                 }
@@ -530,14 +539,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool stop = false;
             Tile t, tn;
             int src[32], nsrc[32], nj = 0, nnj = 0;
-            int w = next_tile(blockIdx.x, t);
+            int w = next_tile(first, t);
             if (w < total) {
                 load_rows(t, src, nj);
                 check_rows(src, nj);
             }
             while (w < total && !stop) {
                 // the next tile's rows load while this tile's copies are issued
-                const int wn = next_tile(w + gridDim.x, tn);
+                const int wn = next_tile(w + stride, tn);
                 if (wn < total) load_rows(tn, nsrc, nnj);
                 const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
                 const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
@@ -610,7 +619,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int issued_phase[G_STAGES];
             for (int s = 0; s < G_STAGES; ++s) issued_phase[s] = -1;
             bool stop = false;
-            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+            for (int w = first; w < total && !stop; w += stride) {
                 Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int brow = t.group * p.n_out + t.n0;
@@ -656,7 +665,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t stage = 0, phase = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
-            for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
+            for (int w = first; w < total && !stop; w += stride) {
                 Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 if (!wait_bounded(sh, smem_u32(&sh->tempty[acc]), acc_phase ^ 1u, WAIT_LIMIT_NS, true))
@@ -705,7 +714,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint8_t *ebuf = smem + G_STAGES * G_STAGE_BYTES + (warp - 2) * 2 * EPI_BUF_BYTES;
         int ebuf_idx = 0;
         uint32_t acc = 0, acc_phase = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        for (int w = first; w < total; w += stride) {
             Tile t = tile_of<BM>(p, w / splits, num_m, num_n);
             if (!t.ok) {
                 if (threadIdx.x == 64) flag_error(MOE_DEVERR_TILE_LIST);
@@ -969,8 +978,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const int num_n = (p.n_out + BN - 1) / BN;
     const int total = num_m * num_n;
     const int kblocks = p.k_dim / BK;
-    const int cluster_id = blockIdx.x >> 1;
-    const int num_clusters = gridDim.x >> 1;
+    // the single-SM kernel's balanced schedule, over clusters
+    const int rounds = (total + (int)(gridDim.x >> 1) - 1) / (int)(gridDim.x >> 1);
+    const int num_clusters = rounds > 0 ? (total + rounds - 1) / rounds : (int)(gridDim.x >> 1);
+    const int cluster_id = (int)(blockIdx.x >> 1) < num_clusters ? (int)(blockIdx.x >> 1) : total;
 
     if (warp == 0) {
         if (lane == 0) {
