@@ -67,6 +67,8 @@ SMALL = [
     # decode-sized batch: split-K over the k-pairs with an odd k-block count
     # (192 = 3 x 64, 320 = 5 x 64), the shared expert split too
     MoEConfig("fp8_split_k", 40, 192, 320, 4, 2, 0.0, has_shared=True, sel_bias=True, weights="fp8_e4m3"),
+    # a decode-sized batch with a Zipf-skewed gate: a few experts hold most rows
+    MoEConfig("fp8_decode_zipf", 120, 256, 384, 8, 2, 0.0, zipf=True, weights="fp8_e4m3"),
 ]
 
 
