@@ -255,9 +255,14 @@ def ffn_work(cfg, R: int, hit: int):
     T, d, f = cfg.T, cfg.d_model, cfg.d_ff
     flops = 4.0 * R * d * f + (4.0 * T * d * f if cfg.has_shared else 0.0)
     rows_all = R + (T if cfg.has_shared else 0)
-    fp8 = cfg.weights == "fp8_e4m3"
-    w_bytes = 2.0 * d * f * (1 if fp8 else 2) + ((d + f) * 4 if fp8 else 0)
-    x_bytes = (R * 2 * d + (T * 2 * d if cfg.has_shared else 0)) if fp8 else T * 2 * d
+    if cfg.weights == "fp8_e4m3":      # one byte a weight + an fp32 scale per output channel
+        w_bytes = 2.0 * d * f + (d + f) * 4
+    elif cfg.weights == "int4_g128":   # half a byte a weight + a bf16 scale per channel and 128 columns
+        w_bytes = 1.0 * d * f + 2.0 * (d * f / 128) * 2
+    else:
+        w_bytes = 4.0 * d * f
+    quant = cfg.weights != "bf16"
+    x_bytes = (R * 2 * d + (T * 2 * d if cfg.has_shared else 0)) if quant else T * 2 * d
     nbytes = ((hit + (1 if cfg.has_shared else 0)) * w_bytes + x_bytes + rows_all * 4 * f
               + R * 2 * d + (T * 2 * d if cfg.has_shared else 0))
     return flops, nbytes
@@ -332,9 +337,11 @@ def gemm_roofline(cfg, m, P, peak_kind, peak_t):
     tflops = flops / (gemm_ms * 1e-3) / 1e12
     gbs = nbytes / (gemm_ms * 1e-3) / 1e9
     tensor_bound = cfg.weights == "bf16" and flops / nbytes > peak_t * 1e12 / (P["hbm_gbs"] * 1e9)
-    fp8 = cfg.weights == "fp8_e4m3"
-    kernel = ("grouped_gemm_fp8t_kernel (expert Linears, FP8 weights widened into tensor memory, "
-              "channel-major tcgen05)") if fp8 else "grouped_gemm_kernel (expert Linears, tcgen05)"
+    kernel = {"fp8_e4m3": "grouped_gemm_quant_kernel<FP8> (expert Linears, E4M3 codes widened into tensor "
+                          "memory, channel-major tcgen05)",
+              "int4_g128": "grouped_gemm_quant_kernel<INT4> (expert Linears, 4-bit codes and group scales "
+                           "widened into tensor memory, channel-major tcgen05)"}.get(
+        cfg.weights, "grouped_gemm_kernel (expert Linears, tcgen05)")
     return {"kernel": kernel,
             "bound": "tensor" if tensor_bound else "hbm",
             "achieved": tflops if tensor_bound else gbs,
@@ -374,7 +381,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="dsv3",
                     help="headline workload (default: the DeepSeek-V3-shaped layer, the largest that fits one GPU)")
-    ap.add_argument("--extras", default="mixtral_prefill,mixtral_decode16,mixtral_decode16_fp8",
+    ap.add_argument("--extras", default="mixtral_prefill,mixtral_decode16,mixtral_decode16_fp8,mixtral_decode16_int4",
                     help="further workloads timed in the same run and reported under 'workloads' "
                          "(comma-separated names, or 'none')")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

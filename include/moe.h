@@ -109,6 +109,7 @@ typedef struct {
 
 #define MOE_WEIGHTS_BF16 0
 #define MOE_WEIGHTS_FP8_E4M3 1
+#define MOE_WEIGHTS_INT4_G128 2
 
 /* Layer weights, all DEVICE pointers. */
 typedef struct {
@@ -129,16 +130,33 @@ typedef struct {
      * (the "e4m3fn" encoding) in the same nn.Linear layout with one fp32 scale
      * per output channel; the dequantised weight is code value * scale. The
      * gate W_g and all biases stay as above. NaN codes (0x7f, 0xff) are not
-     * supported. */
+     * supported.
+     * MOE_WEIGHTS_INT4_G128: weight-only 4-bit experts (the 4-bit expert
+     * weights of lmnt.cn/news/351908 sec. 4.3; the yunthe.com page measures a
+     * 4-bit Mixtral): W1q / W2q / Ws1q / Ws2q hold 4-bit codes packed two per
+     * byte along the reduction dimension (byte j of a row holds column 2j in
+     * its low nibble and 2j + 1 in its high nibble; code c stands for the
+     * integer c - 8), i.e. [N, d_ff, d_model / 2], [N, d_model, d_ff / 2],
+     * [d_ff, d_model / 2], [d_model, d_ff / 2]; g1 / g2 / gs1 / gs2 hold one
+     * bf16 scale per output channel and group of 128 consecutive reduction
+     * columns, group-major: [N, d_model / 128, d_ff], [N, d_ff / 128, d_model],
+     * [d_model / 128, d_ff], [d_ff / 128, d_model]. The dequantised weight is
+     * (c - 8) * scale rounded once to bf16 (round to nearest even). s1, s2,
+     * ss1, ss2 are ignored. d_model and d_ff must be multiples of 128
+     * (MOE_ERR_UNSUPPORTED otherwise). */
     int32_t format;
-    const uint8_t *W1q;   /* [N, d_ff, d_model] */
-    const float *s1;      /* [N, d_ff] */
-    const uint8_t *W2q;   /* [N, d_model, d_ff] */
-    const float *s2;      /* [N, d_model] */
-    const uint8_t *Ws1q;  /* [d_ff, d_model] (has_shared) */
-    const float *ss1;     /* [d_ff] */
-    const uint8_t *Ws2q;  /* [d_model, d_ff] */
-    const float *ss2;     /* [d_model] */
+    const uint8_t *W1q;   /* FP8 [N, d_ff, d_model]; INT4 [N, d_ff, d_model / 2] */
+    const float *s1;      /* FP8 [N, d_ff] */
+    const uint8_t *W2q;   /* FP8 [N, d_model, d_ff]; INT4 [N, d_model, d_ff / 2] */
+    const float *s2;      /* FP8 [N, d_model] */
+    const uint8_t *Ws1q;  /* (has_shared) FP8 [d_ff, d_model]; INT4 [d_ff, d_model / 2] */
+    const float *ss1;     /* FP8 [d_ff] */
+    const uint8_t *Ws2q;  /* FP8 [d_model, d_ff]; INT4 [d_model, d_ff / 2] */
+    const float *ss2;     /* FP8 [d_model] */
+    const moe_bf16 *g1;   /* INT4 [N, d_model / 128, d_ff] */
+    const moe_bf16 *g2;   /* INT4 [N, d_ff / 128, d_model] */
+    const moe_bf16 *gs1;  /* INT4 (has_shared) [d_model / 128, d_ff] */
+    const moe_bf16 *gs2;  /* INT4 (has_shared) [d_ff / 128, d_model] */
 } moe_weights;
 
 /* Gradients written by moe_backward, all DEVICE fp32 buffers in the layout
@@ -350,7 +368,7 @@ MOE_API moe_status moe_forward_hostio_batches(const moe_shape *shape, const moe_
  *             / T lse p (sec. 5.2-5.3), dWg = ds^T x, dx += ds Wg
  * dO and da are stored in bf16 between the tensor-core GEMMs, every other
  * intermediate and every gradient in fp32. dy: [T, d_model] bf16 (device).
- * grads: see moe_grads. BF16 expert weights only (FP8: MOE_ERR_UNSUPPORTED).
+ * grads: see moe_grads. BF16 expert weights only (FP8, INT4: MOE_ERR_UNSUPPORTED).
  * workspace >= moe_workspace_bytes(shape, MOE_WS_BACKWARD). Asynchronous on
  * `stream`. */
 MOE_API moe_status moe_backward(const moe_shape *shape, const moe_weights *weights, const moe_bf16 *x,

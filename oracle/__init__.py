@@ -121,6 +121,10 @@ class Oracle:
         lib.oracle_shared_ffn.argtypes = [i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_expert_ffn_fp8.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_shared_ffn_fp8.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.oracle_expert_ffn_int4.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
+        lib.oracle_shared_ffn_int4.argtypes = [i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.oracle_int4_dequant.restype = f64
+        lib.oracle_int4_dequant.argtypes = [i32, ctypes.c_uint16]
         lib.oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [P] * 17 + [f64, f64, f64, f64, i32] + [P] * 12
         lib.oracle_combine_backward.argtypes = [i32, i32, i32, P, P, P, P]
         lib.oracle_gate_backward.argtypes = [i32, i32, i32, i32, P, P, P, P, P, f64, f64, f64, f64, P]
@@ -251,6 +255,39 @@ class Oracle:
         z = np.zeros((T, d), dtype=np.uint16)
         self.lib.oracle_shared_ffn_fp8(T, d, f, _p(x), _p(Ws1q), _p(ss1), _p(bs1), _p(Ws2q), _p(ss2), _p(bs2),
                                        _p(want), _p(z))
+        return z
+
+    def int4_dequant(self, code: int, scale_bits: int) -> float:
+        """The dequantised INT4 weight: bf16(RNE) of (code - 8) * scale."""
+        return float(self.lib.oracle_int4_dequant(int(code), int(scale_bits)))
+
+    def expert_ffn_int4(self, x, offsets, row_token, W1q4, g1, b1, W2q4, g2, b2, want=None) -> np.ndarray:
+        """expert_ffn with INT4 group-wise weights: packed codes [N, out, in / 2]
+        (even column in the low nibble) and bf16 group scales [N, in / 128, out]."""
+        x = _np(x, np.uint16)
+        offsets, row_token = _np(offsets, np.int32), _np(row_token, np.int32)
+        W1q4, W2q4 = _np(W1q4, np.uint8), _np(W2q4, np.uint8)
+        g1, g2 = _np(g1, np.uint16), _np(g2, np.uint16)
+        b1, b2 = _np(b1, np.float32), _np(b2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        N, f = W1q4.shape[0], W1q4.shape[1]
+        y_perm = np.zeros((max(int(offsets[N]), 0), d), dtype=np.uint16)
+        self.lib.oracle_expert_ffn_int4(T, d, f, N, _p(offsets), _p(row_token), _p(x), _p(W1q4), _p(g1), _p(b1),
+                                        _p(W2q4), _p(g2), _p(b2), _p(want), _p(y_perm))
+        return y_perm
+
+    def shared_ffn_int4(self, x, Ws1q4, gs1, bs1, Ws2q4, gs2, bs2, want=None) -> np.ndarray:
+        x = _np(x, np.uint16)
+        Ws1q4, Ws2q4 = _np(Ws1q4, np.uint8), _np(Ws2q4, np.uint8)
+        gs1, gs2 = _np(gs1, np.uint16), _np(gs2, np.uint16)
+        bs1, bs2 = _np(bs1, np.float32), _np(bs2, np.float32)
+        want = _np(want, np.uint8)
+        T, d = x.shape
+        f = Ws1q4.shape[0]
+        z = np.zeros((T, d), dtype=np.uint16)
+        self.lib.oracle_shared_ffn_int4(T, d, f, _p(x), _p(Ws1q4), _p(gs1), _p(bs1), _p(Ws2q4), _p(gs2), _p(bs2),
+                                        _p(want), _p(z))
         return z
 
     def shared_ffn(self, x, Ws1, bs1, Ws2, bs2, want=None) -> np.ndarray:
@@ -385,9 +422,10 @@ class Oracle:
         """Full layer forward. Routing, dispatch and the aux loss always cover
         every token; ``want`` (bool/uint8 [T], optional) limits the FFN and the
         combine to a sample of tokens (the others' outputs are left 0).
-        ``quant`` (optional) holds FP8 expert weights instead of W1/W2/Ws1/Ws2:
-        an object with W1q, s1, W2q, s2 (and Ws1q, ss1, Ws2q, ss2 with a shared
-        expert)."""
+        ``quant`` (optional) holds quantised expert weights instead of
+        W1/W2/Ws1/Ws2: an object with ``format`` "fp8_e4m3" and W1q, s1, W2q,
+        s2 (and Ws1q, ss1, Ws2q, ss2 with a shared expert), or "int4_g128" and
+        the packed codes and bf16 group scales in the same fields."""
         x = _np(x, np.uint16)
         T, d = x.shape
         N = _np(Wg, np.uint16).shape[0]
@@ -405,6 +443,11 @@ class Oracle:
                 y_perm = self.expert_ffn(x, offsets, row_token, W1, b1, W2, b2, want_u8)
                 if Ws1 is not None:
                     z = self.shared_ffn(x, Ws1, bs1, Ws2, bs2, want_u8)
+            elif getattr(quant, "format", "fp8_e4m3") == "int4_g128":
+                q = quant
+                y_perm = self.expert_ffn_int4(x, offsets, row_token, q.W1q, q.s1, b1, q.W2q, q.s2, b2, want_u8)
+                if bs1 is not None:
+                    z = self.shared_ffn_int4(x, q.Ws1q, q.ss1, bs1, q.Ws2q, q.ss2, bs2, want_u8)
             else:
                 q = quant
                 y_perm = self.expert_ffn_fp8(x, offsets, row_token, q.W1q, q.s1, b1, q.W2q, q.s2, b2, want_u8)

@@ -282,6 +282,20 @@ static double fp8e4m3_val(uint8_t q)
 
 double oracle_fp8_value(uint8_t q) { return fp8e4m3_val(q); }
 
+/* INT4 group-wise (the 4-bit expert weights of the lmnt.cn/news/351908 sec.
+ * 4.3 remark; the yunthe.com page measures a 4-bit Mixtral): codes packed two
+ * per byte along the reduction dimension, the even column in the low nibble;
+ * code c stands for the integer c - 8; one bf16 scale per output row and
+ * group of 128 consecutive reduction columns. The dequantised weight is
+ * (c - 8) * scale rounded to bf16 (RNE): the bf16 value the matrix product
+ * consumes. */
+static double int4_dequant(int code, uint16_t scale)
+{
+    return bf16_val(bf16_round((double)(code - 8) * bf16_val(scale)));
+}
+
+double oracle_int4_dequant(int code, uint16_t scale) { return int4_dequant(code, scale); }
+
 /* An expert weight matrix [rows, cols] in nn.Linear layout: bf16 values, or
  * (weight-only quantisation: the lmnt.cn/news/351908 sec. 4.3 remark on
  * storing expert weights in 8 or 4 bits, and the CSDN page's sec. 3.2 FP8
@@ -291,12 +305,21 @@ typedef struct {
     const uint16_t *bf;
     const uint8_t *q;
     const float *scale;
+    /* INT4 group-wise: codes [rows][cols / 2], scales group-major [cols / 128][rows] */
+    const uint8_t *q4;
+    const uint16_t *gscale;
+    size_t rows;
 } wmat;
 
 static double wval(const wmat *m, size_t row, size_t col, size_t cols)
 {
     if (m->q)
         return fp8e4m3_val(m->q[row * cols + col]) * (double)m->scale[row];
+    if (m->q4) {
+        const uint8_t byte = m->q4[row * (cols / 2) + col / 2];
+        const int code = (col & 1) ? (byte >> 4) : (byte & 15);
+        return int4_dequant(code, m->gscale[(col / 128) * m->rows + row]);
+    }
     return bf16_val(m->bf[row * cols + col]);
 }
 
@@ -307,6 +330,9 @@ static wmat wexpert(const wmat *m, int e, size_t rows, size_t cols)
     if (r.q) {
         r.q += (size_t)e * rows * cols;
         r.scale += (size_t)e * rows;
+    } else if (r.q4) {
+        r.q4 += (size_t)e * rows * (cols / 2);
+        r.gscale += (size_t)e * (cols / 128) * rows;
     } else {
         r.bf += (size_t)e * rows * cols;
     }
@@ -349,7 +375,7 @@ void oracle_expert_rows(int d, int f, int nrows, const int32_t *rows, const uint
     {
         double *xd = (double *)malloc(sizeof(double) * (size_t)d);
         double *h = (double *)malloc(sizeof(double) * (size_t)f);
-        const wmat w1 = {W1e, NULL, NULL}, w2 = {W2e, NULL, NULL};
+        const wmat w1 = {W1e, NULL, NULL, NULL, NULL, 0}, w2 = {W2e, NULL, NULL, NULL, NULL, 0};
 #pragma omp for schedule(dynamic, 1)
         for (int i = 0; i < nrows; ++i)
             ffn_row(d, f, x + (size_t)rows[i] * d, &w1, b1e, &w2, b2e, xd, h, out + (size_t)i * d);
@@ -395,7 +421,7 @@ void oracle_expert_ffn(int T, int d, int f, int N, const int32_t *offsets, const
                        const uint16_t *x, const uint16_t *W1, const float *b1, const uint16_t *W2,
                        const float *b2, const uint8_t *want, uint16_t *y_perm)
 {
-    const wmat w1 = {W1, NULL, NULL}, w2 = {W2, NULL, NULL};
+    const wmat w1 = {W1, NULL, NULL, NULL, NULL, 0}, w2 = {W2, NULL, NULL, NULL, NULL, 0};
     (void)T;
     expert_ffn(d, f, N, offsets, row_token, x, &w1, b1, &w2, b2, want, y_perm);
 }
@@ -407,7 +433,19 @@ void oracle_expert_ffn_fp8(int T, int d, int f, int N, const int32_t *offsets, c
                            const uint8_t *W2q, const float *s2, const float *b2, const uint8_t *want,
                            uint16_t *y_perm)
 {
-    const wmat w1 = {NULL, W1q, s1}, w2 = {NULL, W2q, s2};
+    const wmat w1 = {NULL, W1q, s1, NULL, NULL, 0}, w2 = {NULL, W2q, s2, NULL, NULL, 0};
+    (void)T;
+    expert_ffn(d, f, N, offsets, row_token, x, &w1, b1, &w2, b2, want, y_perm);
+}
+
+/* The same with INT4 group-wise expert weights: W1q4[N][f][d / 2] with
+ * scales g1[N][d / 128][f], W2q4[N][d][f / 2] with scales g2[N][f / 128][d]. */
+void oracle_expert_ffn_int4(int T, int d, int f, int N, const int32_t *offsets, const int32_t *row_token,
+                            const uint16_t *x, const uint8_t *W1q4, const uint16_t *g1, const float *b1,
+                            const uint8_t *W2q4, const uint16_t *g2, const float *b2, const uint8_t *want,
+                            uint16_t *y_perm)
+{
+    const wmat w1 = {NULL, NULL, NULL, W1q4, g1, (size_t)f}, w2 = {NULL, NULL, NULL, W2q4, g2, (size_t)d};
     (void)T;
     expert_ffn(d, f, N, offsets, row_token, x, &w1, b1, &w2, b2, want, y_perm);
 }
@@ -434,7 +472,7 @@ static void shared_ffn(int T, int d, int f, const uint16_t *x, const wmat *Ws1, 
 void oracle_shared_ffn(int T, int d, int f, const uint16_t *x, const uint16_t *Ws1, const float *bs1,
                        const uint16_t *Ws2, const float *bs2, const uint8_t *want, uint16_t *z)
 {
-    const wmat w1 = {Ws1, NULL, NULL}, w2 = {Ws2, NULL, NULL};
+    const wmat w1 = {Ws1, NULL, NULL, NULL, NULL, 0}, w2 = {Ws2, NULL, NULL, NULL, NULL, 0};
     shared_ffn(T, d, f, x, &w1, bs1, &w2, bs2, want, z);
 }
 
@@ -442,7 +480,15 @@ void oracle_shared_ffn_fp8(int T, int d, int f, const uint16_t *x, const uint8_t
                            const float *bs1, const uint8_t *Ws2q, const float *ss2, const float *bs2,
                            const uint8_t *want, uint16_t *z)
 {
-    const wmat w1 = {NULL, Ws1q, ss1}, w2 = {NULL, Ws2q, ss2};
+    const wmat w1 = {NULL, Ws1q, ss1, NULL, NULL, 0}, w2 = {NULL, Ws2q, ss2, NULL, NULL, 0};
+    shared_ffn(T, d, f, x, &w1, bs1, &w2, bs2, want, z);
+}
+
+void oracle_shared_ffn_int4(int T, int d, int f, const uint16_t *x, const uint8_t *Ws1q4, const uint16_t *gs1,
+                            const float *bs1, const uint8_t *Ws2q4, const uint16_t *gs2, const float *bs2,
+                            const uint8_t *want, uint16_t *z)
+{
+    const wmat w1 = {NULL, NULL, NULL, Ws1q4, gs1, (size_t)f}, w2 = {NULL, NULL, NULL, Ws2q4, gs2, (size_t)d};
     shared_ffn(T, d, f, x, &w1, bs1, &w2, bs2, want, z);
 }
 

@@ -518,6 +518,68 @@ def pin_fp8_experts(orc):
                       what="fp8 dense expert")
 
 
+def pin_int4_dequant(orc):
+    """INT4 dequantisation: every code c in 0..15 stands for c - 8, and the
+    weight is (c - 8) * scale rounded to bf16 (RNE), checked against torch's
+    float32 product (exact: at most 11 significant bits) cast to bfloat16, for
+    scales that need rounding, including an exact halfway case."""
+    scales = torch.tensor([1.0, 1.0078125, 1.9921875, 0.3359375, 3.0e-3, -0.75, 117.0], dtype=torch.bfloat16)
+    for sb in scales:
+        sbits = int(sb.view(torch.int16).item()) & 0xFFFF
+        for c in range(16):
+            want = (torch.tensor(float(c - 8), dtype=torch.float32) * sb.to(torch.float32)).to(torch.bfloat16)
+            assert orc.int4_dequant(c, sbits) == float(want.to(torch.float64)), (c, float(sb))
+    # (11 - 8) * 1.0078125 = 3.0234375 lies halfway between bf16 3.015625 and
+    # 3.03125: round to the even mantissa
+    half_bits = int(torch.tensor(1.0078125, dtype=torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+    assert orc.int4_dequant(11, half_bits) == 3.03125
+    assert orc.int4_dequant(8, half_bits) == 0.0 and orc.int4_dequant(0, 0x3F80) == -8.0
+
+
+def _int4_weights(rng, out, inn, lead=()):
+    """Random INT4 codes packed two per byte (even column low) and random bf16
+    group scales [..., inn / 128, out]; returns them with the dequantised bf16
+    weights [..., out, inn] computed independently in torch."""
+    codes = rng.integers(0, 16, size=lead + (out, inn)).astype(np.uint8)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    sc = torch.from_numpy(rng.uniform(0.004, 0.06, size=lead + (inn // 128, out))).to(torch.bfloat16)
+    s_full = sc.to(torch.float32).transpose(-1, -2).repeat_interleave(128, dim=-1)   # [..., out, inn]
+    w = ((torch.from_numpy(codes.astype(np.float32)) - 8.0) * s_full).to(torch.bfloat16)
+    return packed, bits(sc), bits(w)
+
+
+def pin_int4_experts(orc):
+    """INT4 group-wise experts give bit-identical outputs to bf16 experts
+    holding their dequantised weights (routed and shared), the dequantisation
+    done independently in torch from the packed layout: so the INT4 path
+    inherits the bf16 path's pins, and a swapped nibble, a scale from the
+    wrong row or group, or an unrounded weight fails."""
+    rng = np.random.default_rng(23)
+    T, d, f, N, K = 40, 256, 384, 4, 2
+    x = grid_x(rng, T, d)
+    Wg = grid_wg(rng, N, d)
+    W1q, g1, W1 = _int4_weights(rng, f, d, (N,))
+    W2q, g2, W2 = _int4_weights(rng, d, f, (N,))
+    Ws1q, gs1, Ws1 = _int4_weights(rng, f, d)
+    Ws2q, gs2, Ws2 = _int4_weights(rng, d, f)
+    b1 = (rng.standard_normal((N, f)) * 0.02).astype(np.float32)
+    b2 = (rng.standard_normal((N, d)) * 0.02).astype(np.float32)
+    bs1 = (rng.standard_normal(f) * 0.02).astype(np.float32)
+    bs2 = (rng.standard_normal(d) * 0.02).astype(np.float32)
+    ref = orc.forward(x, Wg, W1, b1, W2, b2, K=K, capacity_factor=0.0, aux_alpha=0.01,
+                      Ws1=Ws1, bs1=bs1, Ws2=Ws2, bs2=bs2)
+
+    class Q:
+        format = "int4_g128"
+    q = Q()
+    q.W1q, q.s1, q.W2q, q.s2, q.Ws1q, q.ss1, q.Ws2q, q.ss2 = W1q, g1, W2q, g2, Ws1q, gs1, Ws2q, gs2
+    got = orc.forward(x, Wg, None, b1, None, b2, K=K, capacity_factor=0.0, aux_alpha=0.01,
+                      bs1=bs1, bs2=bs2, quant=q)
+    assert np.array_equal(got.y_perm, ref.y_perm)
+    assert np.array_equal(got.z, ref.z)
+    assert np.array_equal(got.y, ref.y)
+
+
 def _torch_layer_grads(x, Wg, W1, b1, W2, b2, fwd, dy, alpha, beta, g_aux, g_z, shared=None):
     """torch autograd in float64 of a plain restatement of the layer with the
     forward's routing decisions held fixed; the bf16 storage points (h, o, y)
@@ -688,5 +750,5 @@ ALL_PINS = [
     pin_permutation_roundtrip, pin_dense_special_case, pin_identical_experts, pin_fp8_decode,
     pin_fp8_experts, pin_backward_autograd, pin_backward_token_mask, pin_backward_pieces, pin_health,
     pin_token_major, pin_soft_router, pin_drops_and_shared, pin_aux, pin_z_loss,
-    pin_dispatch_rank_major, pin_aux_kl,
+    pin_dispatch_rank_major, pin_aux_kl, pin_int4_dequant, pin_int4_experts,
 ]

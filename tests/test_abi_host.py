@@ -94,7 +94,7 @@ def test_invalid_arguments(L):
     assert L.moe_expert_ffn(ctypes.byref(sh), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, 1 << 40,
                             None) == lib.MOE_ERR_INVALID_ARG
     # FP8 expert weights: the bf16 matrices may be absent, the codes and scales may not
-    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, 2)              # unknown format
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, 7)              # unknown format
     assert L.moe_expert_ffn(ctypes.byref(ok), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, None, FAKE, 1 << 40,
                             None) == lib.MOE_ERR_INVALID_ARG
     w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, lib.MOE_WEIGHTS_FP8_E4M3,
@@ -105,6 +105,18 @@ def test_invalid_arguments(L):
                        FAKE, FAKE, FAKE, FAKE)                                                 # shared codes missing
     assert L.moe_expert_ffn(ctypes.byref(sh), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, 1 << 40,
                             None) == lib.MOE_ERR_INVALID_ARG
+    # INT4 group-wise expert weights: codes and bf16 group scales, reductions in whole groups of 128
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, lib.MOE_WEIGHTS_INT4_G128,
+                       FAKE, None, FAKE, None, None, None, None, None, FAKE, None)             # g2 missing
+    assert L.moe_expert_ffn(ctypes.byref(ok), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, None, FAKE, 1 << 40,
+                            None) == lib.MOE_ERR_INVALID_ARG
+    w = lib.MoeWeights(FAKE, None, FAKE, None, FAKE, None, None, None, None, lib.MOE_WEIGHTS_INT4_G128,
+                       FAKE, None, FAKE, None, None, None, None, None, FAKE, FAKE)
+    d192 = lib.make_shape(256, 192, 256, 8, 2, 1.25)                                       # 192 = 1.5 groups
+    assert L.moe_expert_ffn(ctypes.byref(d192), FAKE, FAKE, ctypes.byref(w), FAKE, FAKE, None, FAKE, 1 << 40,
+                            None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_forward(ctypes.byref(d192), ctypes.byref(w), FAKE, None, FAKE, None, FAKE, 1 << 40, None) \
+        == lib.MOE_ERR_UNSUPPORTED
     assert L.moe_combine(ctypes.byref(ok), FAKE, FAKE, None, None, FAKE, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_combine(ctypes.byref(ok), FAKE, FAKE, FAKE, FAKE + 8, FAKE, None) == lib.MOE_ERR_INVALID_ARG
     assert L.moe_aux_loss(ctypes.byref(ok), FAKE, None, FAKE, None) == lib.MOE_ERR_INVALID_ARG

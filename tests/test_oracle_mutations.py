@@ -10,6 +10,16 @@ import oracle_pins as pins
 
 # (name, [(exact text in moe_oracle.c, replacement)])
 MUTATIONS = [
+    ("int4_nibble_order_swapped", [("const int code = (col & 1) ? (byte >> 4) : (byte & 15);",
+                                    "const int code = (col & 1) ? (byte & 15) : (byte >> 4);")]),
+    ("int4_code_offset", [("return bf16_val(bf16_round((double)(code - 8) * bf16_val(scale)));",
+                           "return bf16_val(bf16_round((double)(code - 7) * bf16_val(scale)));")]),
+    ("int4_dequant_unrounded", [("return bf16_val(bf16_round((double)(code - 8) * bf16_val(scale)));",
+                                 "return (double)(code - 8) * bf16_val(scale);")]),
+    ("int4_scale_row_major", [("return int4_dequant(code, m->gscale[(col / 128) * m->rows + row]);",
+                               "return int4_dequant(code, m->gscale[row * (cols / 128) + col / 128]);")]),
+    ("int4_scale_first_row", [("return int4_dequant(code, m->gscale[(col / 128) * m->rows + row]);",
+                               "return int4_dequant(code, m->gscale[(col / 128) * m->rows]);")]),
     ("health_std_sample", [("h[0] = sqrt(var / (double)N);", "h[0] = sqrt(var / (double)(N - 1));")]),
     ("health_entropy_sign", [("ent -= p * log(p);", "ent += p * log(p);")]),
     ("gelu_grad_no_phi_term", [("return 0.5 * (1.0 + erf(v / sqrt(2.0))) + v * phi;",

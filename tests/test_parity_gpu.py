@@ -69,6 +69,16 @@ SMALL = [
     MoEConfig("fp8_split_k", 40, 192, 320, 4, 2, 0.0, has_shared=True, sel_bias=True, weights="fp8_e4m3"),
     # a decode-sized batch with a Zipf-skewed gate: a few experts hold most rows
     MoEConfig("fp8_decode_zipf", 120, 256, 384, 8, 2, 0.0, zipf=True, weights="fp8_e4m3"),
+    # INT4 group-wise expert weights (4-bit codes, a bf16 scale per 128 columns):
+    # several channel tiles and groups, drops, a ragged expert
+    MoEConfig("int4_experts", 700, 256, 640, 8, 2, 1.25, weights="int4_g128"),
+    # the shared expert and the selection bias, K = 4
+    MoEConfig("int4_shared_bias", 300, 256, 384, 16, 4, 0.0, has_shared=True, sel_bias=True, weights="int4_g128"),
+    # decode-sized: split-K over the k-pairs with odd k-pair counts (384 = 3 x 128,
+    # 640 = 5 x 128), the shared expert split too
+    MoEConfig("int4_split_k", 40, 384, 640, 4, 2, 0.0, has_shared=True, weights="int4_g128"),
+    # several 64-row tiles per expert with a ragged last one, one group per row
+    MoEConfig("int4_many_rows", 700, 128, 256, 2, 1, 0.0, weights="int4_g128"),
 ]
 
 
@@ -156,7 +166,7 @@ def test_out_of_range_expert_ids_are_flagged_not_trapped():
 FULL = {
     "mixtral_prefill": None, "mixtral_prefill_cf125": "cover", "mixtral_decode16": None,
     "mixtral_decode64": None, "skewed": None, "dsv3": None, "mixtral_decode16_fp8": None,
-    "mixtral_decode64_fp8": None,
+    "mixtral_decode64_fp8": None, "mixtral_decode16_int4": None, "mixtral_decode64_int4": None,
 }
 SLOW = {"mixtral_prefill", "dsv3"}
 

@@ -1,10 +1,15 @@
-// gemm_fp8t.cuh -- the grouped expert GEMM with weight-only FP8 expert
-// weights (E4M3 codes, one fp32 scale per output channel; the weight
-// quantisation of the lmnt.cn/news/351908 sec. 4.3 remark and the CSDN page's
-// sec. 3.2 one-byte FP8 weights), computed transposed so that the weights,
-// not the tokens, fill the 128 rows of the MMA:
+// gemm_quant.cuh -- the grouped expert GEMM with weight-only quantised expert
+// weights (the 8- and 4-bit expert weights of the lmnt.cn/news/351908 sec.
+// 4.3 remark; the CSDN page's sec. 3.2 one-byte FP8 weights; the yunthe.com
+// page's 4-bit Mixtral), computed transposed so that the weights, not the
+// tokens, fill the 128 rows of the MMA. Two formats:
 //
-//   out[r, n] = epilogue( scale[g(r), n] * sum_k code(B[g(r) * n_out + n, k]) * A[r, k] + bias[g(r), n] )
+//   FP8  E4M3 codes, one fp32 scale per output channel:
+//        out[r, n] = epilogue( scale[g(r), n] * sum_k code(B[g(r) n_out + n, k]) A[r, k] + bias )
+//   INT4 4-bit codes two per byte along k (even column in the low nibble,
+//        code c stands for c - 8), one bf16 scale per output channel and
+//        group of 128 reduction columns:
+//        out[r, n] = epilogue( sum_k bf16((c - 8) * scale[g(r), k / 128, n]) A[r, k] + bias )
 //
 // A decode batch gives each expert a handful of rows, so a token-major tile
 // (128 token rows) would spend almost all of its MMA work on padding. Here one
@@ -13,13 +18,16 @@
 // and N = the tile's row count rounded up to 16, so the tensor-core work
 // scales with the real rows and the kernel is left to stream the codes.
 //
-// The codes cross HBM as one byte per element and are widened to bf16 in
-// registers (exact: every E4M3 value is a bf16 value) and written straight
-// into tensor memory, which the MMA reads as its A operand (tcgen05.mma with
-// A in TMEM); only the raw codes and the token tiles pass through shared
-// memory. bf16 x bf16 products are exact in the fp32 accumulator; the
-// per-channel scale is applied in the epilogue, where it factors out of the
-// sum over k.
+// The codes cross HBM at one byte (FP8) or half a byte (INT4) per weight and
+// are widened to bf16 in registers and written straight into tensor memory,
+// which the MMA reads as its A operand (tcgen05.mma with A in TMEM); only the
+// raw codes and the token tiles pass through shared memory. FP8 widening is
+// exact (every E4M3 value is a bf16 value) and bf16 x bf16 products are exact
+// in the fp32 accumulator, so the per-channel scale is applied in the
+// epilogue, where it factors out of the sum over k. An INT4 scale changes
+// every 128 columns, so it is applied while widening: (c - 8) is exact in
+// bf16 and one bf16 multiply rounds the product once (RNE), which is the
+// dequantised weight the format defines.
 //
 // The unit of the pipeline is a k-pair (128 reduction columns): one raw
 // stage of codes, one TMEM A stage, one token stage, 8 MMAs and one commit.
@@ -28,8 +36,9 @@
 // warps sleep on their barrier instead of spinning for issue slots.
 //
 // Block = 16 warps, one block per SM, persistent over the tile list:
-//   warp 0     raw producer (one lane): TMA of 128 channels x 128 codes
-//              (128-byte swizzle) into a 10-deep ring
+//   warp 0     raw producer (one lane): TMA of 128 channels x one k-pair of
+//              codes (FP8: 128 bytes a row, 128-byte swizzle, 10-deep ring;
+//              INT4: 64 bytes a row, 64-byte swizzle, 20-deep ring)
 //   warps 1,15 TMEM allocator (warp 1) + two MMA issuers (one lane each):
 //              even k-pairs into one accumulator, odd into another
 //   warp 2     token producer (one lane): TMA of the tile's rows (16-row
@@ -38,13 +47,14 @@
 //              bias, GELU, bf16, stores (one 64-byte segment per row and warp)
 //   warps 7-14 converters: warp w owns TMEM lanes 32 (w % 4) .. +31 (the
 //              lanes its warp may address) and one k-block of each pair;
-//              lane = channel, 64 codes -> 32 TMEM columns per stage
+//              lane = channel, 64 codes -> 32 TMEM columns per stage (INT4:
+//              times the channel's scale of the k-pair's group)
 // TMEM: 4 A stages x 64 columns, then two buffers of two 64-column
 // accumulators (one per issuer), summed in the epilogue.
 // Split-K (few rows, so that 148 SMs get equal shares): work item = (tile,
 // range of k-pairs); each split writes its raw fp32 sums to its own plane and
-// fp8_split_finalize_kernel adds the planes in a fixed order and applies the
-// scale, bias and GELU.
+// quant_split_finalize_kernel adds the planes in a fixed order and applies
+// the (FP8) scale, bias and GELU.
 // Every wait is bounded (globaltimer); on a timeout the block sets
 // MOE_DEVERR_TIMEOUT, stops, drains its own copies and MMAs and frees TMEM.
 #pragma once
@@ -59,9 +69,29 @@ namespace gg {
 
 constexpr int QT_CH = 128;                      // output channels per tile (MMA M)
 constexpr int QT_ROWS = 64;                     // rows per tile at most (MMA N <= 64)
-constexpr int QT_RAW_K = 2 * BK;                // codes per raw row: 128 bytes
-constexpr int QT_RAW_BYTES = QT_CH * QT_RAW_K;  // 16 KB
-constexpr int QT_RSTAGES = 10;                  // raw ring: 10 k-pairs of codes in flight
+constexpr int QT_KPAIR = 2 * BK;                // reduction columns per pipeline stage (= an INT4 group)
+
+// Weight formats (the kernel's template argument) and their raw-code rings.
+constexpr int QF_FP8 = 0;
+constexpr int QF_INT4 = 1;
+template <int F>
+struct QFormat;
+template <>
+struct QFormat<QF_FP8> {
+    static constexpr int ROW_BYTES = QT_KPAIR;      // one byte a code
+    static constexpr int RSTAGES = 10;
+};
+template <>
+struct QFormat<QF_INT4> {
+    static constexpr int ROW_BYTES = QT_KPAIR / 2;  // two codes a byte
+    static constexpr int RSTAGES = 20;
+};
+constexpr int QT_RAW_K = QFormat<QF_FP8>::ROW_BYTES;        // FP8 raw row: 128 bytes
+constexpr int QT_RAW_BYTES = QT_CH * QT_RAW_K;                // 16 KB
+constexpr int QT_RSTAGES = QFormat<QF_FP8>::RSTAGES;         // the byte budget of both rings:
+static_assert(QFormat<QF_INT4>::RSTAGES * QT_CH * QFormat<QF_INT4>::ROW_BYTES == QT_RSTAGES * QT_RAW_BYTES,
+              "raw ring budget");
+constexpr int QT_MAX_RSTAGES = QFormat<QF_INT4>::RSTAGES;
 constexpr int QT_TBOX = 16;                     // token rows per TMA box
 constexpr int QT_TBOX_BYTES = QT_TBOX * BK * 2;       // 2 KB (two 1024-byte swizzle atoms)
 constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a full token tile
@@ -80,8 +110,8 @@ constexpr int QT_SMEM_BYTES = QT_RSTAGES * QT_RAW_BYTES + QT_STAGES * QT_TOK_BYT
 static_assert(QT_SMEM_BYTES <= 227 * 1024, "shared memory");
 
 struct QTShared {
-    uint64_t raw_full[QT_RSTAGES];
-    uint64_t raw_empty[QT_RSTAGES];
+    uint64_t raw_full[QT_MAX_RSTAGES];
+    uint64_t raw_empty[QT_MAX_RSTAGES];
     uint64_t a_full[QT_STAGES];    // the 8 converter warps wrote the stage's A columns
     uint64_t tok_full[QT_STAGES];  // the stage's token boxes have landed
     uint64_t empty[QT_STAGES];     // the MMAs reading the stage have completed
@@ -166,6 +196,33 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &in, uint32_t *o) {
     o[7] = e4m3x2_bf16x2(in.w, 0xB3A2u);
 }
 
+// 32 INT4 codes (16 bytes; byte j holds column 2j in its low nibble and
+// 2j + 1 in its high nibble) -> 16 packed bf16 pairs (c - 8) * scale. Each
+// pair is assembled as the bf16 patterns 0x4300 | c (= 128 + c, exact), then
+// 136 is subtracted (exact: c - 8) and one bf16 multiply by the scale rounds
+// the product once (RNE).
+__device__ __forceinline__ void int4x32_to_bf16(const uint4 &in, __nv_bfloat162 scale, uint32_t *o) {
+    const uint32_t words[4] = {in.x, in.y, in.z, in.w};
+    const __nv_bfloat162 k136 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x4308u),
+                                                   __ushort_as_bfloat16((unsigned short)0x4308u));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = words[i] & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 of the word
+        const uint32_t hi = (words[i] >> 4) & 0x0F0F0F0Fu;  // columns 1, 3, 5, 7
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // byte j of lo into byte 0 and byte j of hi into byte 2
+            const uint32_t sel = (uint32_t)(j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12));
+            uint32_t t;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(lo), "r"(hi), "r"(sel));
+            t = (t & 0x00FF00FFu) | 0x43004300u;
+            __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&t), k136);
+            v = __hmul2(v, scale);
+            o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&v);
+        }
+    }
+}
+
 // This thread's lane of 32 consecutive TMEM columns.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -210,21 +267,27 @@ __device__ __forceinline__ Tile qt_tile(const Params &p, int w, int num_m, int n
     return t;
 }
 
+// wscale: FP8, the per-channel fp32 scales [groups * n_out]; gscale: INT4,
+// the bf16 group scales [groups][k_dim / 128][n_out].
+template <int F>
 __global__ void __launch_bounds__(QT_NUM_THREADS, 1)
-grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmBq,
-                         const Params p, const float *__restrict__ wscale) {
+grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmBq,
+                          const Params p, const float *__restrict__ wscale, const uint16_t *__restrict__ gscale) {
+    constexpr int RS = QFormat<F>::RSTAGES;     // raw ring stages
+    constexpr int RB = QFormat<F>::ROW_BYTES;   // bytes of a channel's row per k-pair
+    constexpr int RAWB = QT_CH * RB;            // bytes of a raw stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *rawbuf = smem;
-    uint8_t *tokbuf = rawbuf + QT_RSTAGES * QT_RAW_BYTES;
+    uint8_t *tokbuf = rawbuf + RS * RAWB;
     QTShared *sh = reinterpret_cast<QTShared *>(tokbuf + QT_STAGES * QT_TOK_BYTES);
 
     const int warp = warp_id();
     const int lane = lane_id();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < QT_RSTAGES; ++s) {
+        for (int s = 0; s < RS; ++s) {
             mbar_init(smem_u32(&sh->raw_full[s]), 1);
             mbar_init(smem_u32(&sh->raw_empty[s]), QT_CONVERTERS / 32);
         }
@@ -279,22 +342,21 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
                 const int brow = t.group * p.n_out + t.n0;
                 const int k1 = split_k1(w);
                 for (int kp = split_k0(w); kp < k1; ++kp, ++j) {
-                    const int r = j % QT_RSTAGES;
-                    if (!qt_wait(sh, smem_u32(&sh->raw_empty[r]), ((uint32_t)(j / QT_RSTAGES) & 1u) ^ 1u,
+                    const int r = j % RS;
+                    if (!qt_wait(sh, smem_u32(&sh->raw_empty[r]), ((uint32_t)(j / RS) & 1u) ^ 1u,
                                  WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
                     }
                     // the second half of an odd k count's last pair reads zeros past k_dim;
                     // channels past the tensor's last row read zeros too
-                    mbar_arrive_expect_tx(smem_u32(&sh->raw_full[r]), QT_RAW_BYTES);
-                    tma_load_2d(smem_u32(rawbuf + r * QT_RAW_BYTES), &tmBq, smem_u32(&sh->raw_full[r]),
-                                kp * QT_RAW_K, brow);
+                    mbar_arrive_expect_tx(smem_u32(&sh->raw_full[r]), RAWB);
+                    tma_load_2d(smem_u32(rawbuf + r * RAWB), &tmBq, smem_u32(&sh->raw_full[r]), kp * RB, brow);
                 }
             }
             if (stop) {
-                for (int jj = max(0, j - QT_RSTAGES); jj < j; ++jj)
-                    qt_wait(sh, smem_u32(&sh->raw_full[jj % QT_RSTAGES]), (uint32_t)(jj / QT_RSTAGES) & 1u,
+                for (int jj = max(0, j - RS); jj < j; ++jj)
+                    qt_wait(sh, smem_u32(&sh->raw_full[jj % RS]), (uint32_t)(jj / RS) & 1u,
                             DRAIN_LIMIT_NS, false);
             }
         }
@@ -409,7 +471,7 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
             const bool live = n < p.n_out;
             float scl = 0.f, b = 0.f;
             if (live) {
-                scl = __ldg(wscale + (size_t)t.group * p.n_out + n);
+                scl = F == QF_FP8 ? __ldg(wscale + (size_t)t.group * p.n_out + n) : 1.0f;
                 b = __ldg(p.bias + (size_t)t.group * p.n_out + n);
             }
             uint16_t *outc = p.out + (size_t)t.row0 * p.n_out + n;
@@ -459,29 +521,49 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
         const int q = warp & 3;            // TMEM lane quarter this warp may address
         const int half = (warp - 7) >> 2;  // which k-block of each pair
         const int ch = q * 32 + lane;      // channel = raw row = TMEM lane
-        const uint8_t *rrow = rawbuf + ch * QT_RAW_K;
-        const int sw = ch & 7;             // the 128-byte swizzle of the raw tile
+        const uint8_t *rrow = rawbuf + ch * RB;
+        // the raw tile's swizzle: FP8 rows of 128 bytes (128-byte swizzle: chunk c
+        // of row ch at c ^ (ch % 8)); INT4 rows of 64 bytes (64-byte swizzle:
+        // chunk c at c ^ ((ch / 2) % 4))
+        const int sw = F == QF_FP8 ? (ch & 7) : ((ch >> 1) & 3);
+        const int kgroups = p.k_dim / QT_KPAIR;  // INT4 scale groups per row
         const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + half * (BK / 2);
         int i = 0;  // k-pairs converted (= raw stages consumed)
         bool stop = false;
         for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
             const Tile t = qt_tile(p, w / splits, num_m, num_n);
             if (!t.ok) continue;
-            const int k1 = split_k1(w);
-            for (int kp = split_k0(w); kp < k1; ++kp, ++i) {
-                const int r = i % QT_RSTAGES, s = i % QT_STAGES;
-                if (!qt_wait(sh, smem_u32(&sh->raw_full[r]), (uint32_t)(i / QT_RSTAGES) & 1u, WAIT_LIMIT_NS,
-                             true)) {
+            const int k0 = split_k0(w), k1 = split_k1(w);
+            // INT4: this channel's scales of the item's groups (0 past n_out), each
+            // loaded one k-pair ahead of its use
+            const bool glive = F == QF_INT4 && t.n0 + ch < p.n_out;
+            const uint16_t *grow = gscale + (size_t)t.group * kgroups * p.n_out + t.n0 + ch;
+            uint16_t gnext = glive && k0 < k1 ? __ldg(grow + (size_t)k0 * p.n_out) : (uint16_t)0;
+            for (int kp = k0; kp < k1; ++kp, ++i) {
+                const int r = i % RS, s = i % QT_STAGES;
+                const uint16_t g = gnext;
+                if (glive && kp + 1 < k1) gnext = __ldg(grow + (size_t)(kp + 1) * p.n_out);
+                const __nv_bfloat162 gs = __halves2bfloat162(__ushort_as_bfloat16(g), __ushort_as_bfloat16(g));
+                if (!qt_wait(sh, smem_u32(&sh->raw_full[r]), (uint32_t)(i / RS) & 1u, WAIT_LIMIT_NS, true)) {
                     stop = true;
                     break;
                 }
-                const uint8_t *src = rrow + r * QT_RAW_BYTES;
+                const uint8_t *src = rrow + r * RAWB;
                 uint32_t v[32];
+                if (F == QF_FP8) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = half * 4 + c;  // 16-byte chunks of this k-block in the raw row
-                    const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
-                    e4m3x16_to_bf16(in, v + 8 * c);
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = half * 4 + c;  // 16-byte chunks (16 codes) of this k-block
+                        const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
+                        e4m3x16_to_bf16(in, v + 8 * c);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int chunk = half * 2 + c;  // 16-byte chunks (32 codes) of this k-block
+                        const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
+                        int4x32_to_bf16(in, gs, v + 16 * c);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh->raw_empty[r]));
@@ -509,13 +591,14 @@ grouped_gemm_fp8t_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_c
     }
 }
 
-// Split-K finalize: out[r, n] = epilogue( scale[g(r), n] * sum_s part[s, r, n] + bias[g(r), n] ),
+// Split-K finalize: out[r, n] = epilogue( scale[g(r), n] * sum_s part[s, r, n] + bias[g(r), n] )
+// (scale = nullptr: 1, the INT4 format, whose scales were applied while widening),
 // the splits added in order. Block (x, y) = row x, columns
 // [1024 y, 1024 y + 1024); g(r) from the expert offsets (offsets = nullptr:
 // one group); rows past the last expert's block were not computed and are
 // skipped.
 __global__ void __launch_bounds__(256)
-fp8_split_finalize_kernel(const float *__restrict__ part, int splits, int rows, int n_out,
+quant_split_finalize_kernel(const float *__restrict__ part, int splits, int rows, int n_out,
                           const int32_t *__restrict__ offsets, int groups, const float *__restrict__ scale,
                           const float *__restrict__ bias, int gelu, uint16_t *__restrict__ out) {
     const int r = blockIdx.x;
@@ -533,7 +616,7 @@ fp8_split_finalize_kernel(const float *__restrict__ part, int splits, int rows, 
     }
     const size_t plane = (size_t)rows * n_out;
     const float *pr = part + (size_t)r * n_out;
-    const float *sc = scale + (size_t)g * n_out;
+    const float *sc = scale != nullptr ? scale + (size_t)g * n_out : nullptr;
     const float *bi = bias + (size_t)g * n_out;
     uint16_t *o = out + (size_t)r * n_out;
     const int n = blockIdx.y * 1024 + threadIdx.x * 4;
@@ -546,7 +629,7 @@ fp8_split_finalize_kernel(const float *__restrict__ part, int splits, int rows, 
             acc.z += v.z;
             acc.w += v.w;
         }
-        const float4 c = *reinterpret_cast<const float4 *>(sc + n);
+        const float4 c = sc != nullptr ? *reinterpret_cast<const float4 *>(sc + n) : make_float4(1.f, 1.f, 1.f, 1.f);
         const float4 b = *reinterpret_cast<const float4 *>(bi + n);
         float y0 = fmaf(acc.x, c.x, b.x), y1 = fmaf(acc.y, c.y, b.y);
         float y2 = fmaf(acc.z, c.z, b.z), y3 = fmaf(acc.w, c.w, b.w);

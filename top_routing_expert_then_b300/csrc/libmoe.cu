@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -19,7 +20,7 @@
 #include "route.cuh"
 #include "route_tc.cuh"
 #include "gemm_fp8w.cuh"
-#include "gemm_fp8t.cuh"
+#include "gemm_quant.cuh"
 #include "backward.cuh"
 #include "plan.cuh"
 
@@ -354,7 +355,10 @@ moe_status device_state(DeviceState **out) {
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8w_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::Q_SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_fp8t_kernel,
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_quant_kernel<moe::gg::QF_FP8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::QT_SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_quant_kernel<moe::gg::QF_INT4>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::QT_SMEM_BYTES);
         for (int lpl = 1; lpl <= 8; lpl <<= 1)
             for (int sp = 1; sp <= moe::rtc::kMaxSplits; sp <<= 1)
@@ -427,16 +431,15 @@ bool make_tmap_f32(CUtensorMap *m, const void *base, uint64_t rows, uint64_t col
 // bytes land densely, rows box_cols bytes apart; with swizzle128 (box_cols =
 // 128) the 16-byte chunks of row r are permuted by r % 8 as for bf16 tiles.
 bool make_tmap_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                  uint32_t box_cols, bool swizzle128 = false) {
+                  uint32_t box_cols, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     if (!get_encoder()) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -776,15 +779,22 @@ int fp8_splits(int m_est, int n_tiles, int kpairs, int num_sms) {
     return best;
 }
 
-moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, const void *Bq, uint64_t b_rows,
-                           int k_dim, int n_out, int groups, const float *scale, const float *bias, uint16_t *out,
-                           int out_rows, const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows,
-                           bool gelu, cudaStream_t st, float *part = nullptr, const int32_t *offsets = nullptr) {
-    if (!fp8_token_major()) {
+// The grouped GEMM with quantised expert weights: A bf16 [a_rows, k_dim];
+// FP8 (is_int4 false): codes Bq [groups * n_out, k_dim], scale [groups * n_out];
+// INT4: codes Bq [groups * n_out, k_dim / 2], gscale [groups, k_dim / 128, n_out] bf16.
+moe_status launch_gemm_quant(DeviceState *dev, bool is_int4, const void *A, uint64_t a_rows, const void *Bq,
+                             uint64_t b_rows, int k_dim, int n_out, int groups, const float *scale,
+                             const uint16_t *gscale, const float *bias, uint16_t *out, int out_rows,
+                             const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
+                             cudaStream_t st, float *part = nullptr, const int32_t *offsets = nullptr) {
+    if (is_int4 || !fp8_token_major()) {
         CUtensorMap tt, tb;
         if (!make_tmap(&tt, A, a_rows, (uint64_t)k_dim, moe::gg::QT_TBOX)) return MOE_ERR_CUDA;
-        if (!make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::QT_CH, moe::gg::QT_RAW_K, true))
-            return MOE_ERR_CUDA;
+        const bool ok = is_int4 ? make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim / 2, moe::gg::QT_CH,
+                                            moe::gg::QFormat<moe::gg::QF_INT4>::ROW_BYTES, CU_TENSOR_MAP_SWIZZLE_64B)
+                             : make_tmap_u8(&tb, Bq, b_rows, (uint64_t)k_dim, moe::gg::QT_CH,
+                                            moe::gg::QFormat<moe::gg::QF_FP8>::ROW_BYTES, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return MOE_ERR_CUDA;
         moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles, max_tiles,
                                        dense_rows, gelu);
         const int n_tiles = (n_out + moe::gg::QT_CH - 1) / moe::gg::QT_CH;
@@ -804,13 +814,18 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
         int grid = dev->num_sms;
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
-        moe::gg::grouped_gemm_fp8t_kernel<<<grid, moe::gg::QT_NUM_THREADS, moe::gg::QT_SMEM_BYTES, st>>>(tt, tb, p,
-                                                                                                     scale);
+        if (is_int4)
+            moe::gg::grouped_gemm_quant_kernel<moe::gg::QF_INT4>
+                <<<grid, moe::gg::QT_NUM_THREADS, moe::gg::QT_SMEM_BYTES, st>>>(tt, tb, p, nullptr, gscale);
+        else
+            moe::gg::grouped_gemm_quant_kernel<moe::gg::QF_FP8>
+                <<<grid, moe::gg::QT_NUM_THREADS, moe::gg::QT_SMEM_BYTES, st>>>(tt, tb, p, scale, nullptr);
         count_launch();
         if (splits > 1) {
             const dim3 fgrid((unsigned)out_rows, (unsigned)((n_out + 1023) / 1024));
-            moe::gg::fp8_split_finalize_kernel<<<fgrid, 256, 0, st>>>(part, splits, out_rows, n_out, offsets,
-                                                                         groups, scale, bias, gelu ? 1 : 0, out);
+            moe::gg::quant_split_finalize_kernel<<<fgrid, 256, 0, st>>>(part, splits, out_rows, n_out, offsets,
+                                                                           groups, is_int4 ? nullptr : scale, bias,
+                                                                           gelu ? 1 : 0, out);
             count_launch();
         }
         return MOE_OK;
@@ -839,7 +854,7 @@ moe_status launch_gemm_fp8(DeviceState *dev, const void *A, uint64_t a_rows, con
 // The routed experts' GEMM kernel and its m-tile shape: FP8 (64-row tiles, or
 // 128 token-major), the SM-pair kernel (256) or the single-SM kernel (128).
 struct FfnTiling {
-    bool fp8, pair_routed, pair_routed2, pair_shared;
+    bool fp8, pair_routed, pair_routed2, pair_shared;  // fp8: any quantised format
     int tile_rows, raster;    // first expert GEMM's m-tiles
     int tile_rows2, raster2;  // second's (a second list is built when they differ)
 };
@@ -848,11 +863,11 @@ FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
     int64_t per_expert = (int64_t)s->T * s->K / s->N;
     const int C = capacity_of(s);
     if (per_expert > C) per_expert = C;
-    t.fp8 = wt->format == MOE_WEIGHTS_FP8_E4M3;
+    t.fp8 = wt->format != MOE_WEIGHTS_BF16;
     t.pair_routed = !t.fp8 && !gather && use_pair(per_expert);
     t.pair_routed2 = !t.fp8 && use_pair_gemm2(per_expert, s->d_ff);
     t.pair_shared = !t.fp8 && use_pair(s->T);
-    t.tile_rows = t.fp8 ? (fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
+    t.tile_rows = t.fp8 ? (wt->format == MOE_WEIGHTS_FP8_E4M3 && fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
                         : (t.pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
     t.raster = t.pair_routed ? kRasterPair : kRasterSingle;
     t.tile_rows2 = t.fp8 ? t.tile_rows : (t.pair_routed2 ? moe::gg::PAIR_BM : moe::gg::BM);
@@ -886,22 +901,23 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     }
     moe_status r;
     if (fp8) {
-        // the same four GEMMs with FP8 expert weights and per-channel scales
-        r = launch_gemm_fp8(dev, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->b1, w.H, rows, w.mtiles,
-                            w.num_mtiles, mt, 0, true, st, w.part, offsets);
+        // the same four GEMMs with quantised expert weights (FP8 per-channel or INT4 group-wise scales)
+        const bool i4 = wt->format == MOE_WEIGHTS_INT4_G128;
+        r = launch_gemm_quant(dev, i4, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->g1, wt->b1, w.H,
+                              rows, w.mtiles, w.num_mtiles, mt, 0, true, st, w.part, offsets);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
-            r = launch_gemm_fp8(dev, x, T, wt->Ws1q, f, d, f, 1, wt->ss1, wt->bs1, w.Hs, T, nullptr, nullptr, 0, T,
-                                true, st, w.part);
+            r = launch_gemm_quant(dev, i4, x, T, wt->Ws1q, f, d, f, 1, wt->ss1, wt->gs1, wt->bs1, w.Hs, T, nullptr,
+                                  nullptr, 0, T, true, st, w.part);
             if (r != MOE_OK) return r;
         }
         if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
-        r = launch_gemm_fp8(dev, w.H, rows, wt->W2q, (uint64_t)N * d, f, d, N, wt->s2, wt->b2, y_perm, rows, w.mtiles,
-                            w.num_mtiles, mt, 0, false, st, w.part, offsets);
+        r = launch_gemm_quant(dev, i4, w.H, rows, wt->W2q, (uint64_t)N * d, f, d, N, wt->s2, wt->g2, wt->b2, y_perm,
+                              rows, w.mtiles, w.num_mtiles, mt, 0, false, st, w.part, offsets);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
-            r = launch_gemm_fp8(dev, w.Hs, T, wt->Ws2q, d, f, d, 1, wt->ss2, wt->bs2, z, T, nullptr, nullptr, 0, T,
-                                false, st, w.part);
+            r = launch_gemm_quant(dev, i4, w.Hs, T, wt->Ws2q, d, f, d, 1, wt->ss2, wt->gs2, wt->bs2, z, T, nullptr,
+                                  nullptr, 0, T, false, st, w.part);
             if (r != MOE_OK) return r;
         }
         return launch_status();
@@ -1100,24 +1116,28 @@ moe_status run_backward(const moe_shape *s, DeviceState *dev, const moe_weights 
 
 bool weights_ok(const moe_shape *s, const moe_weights *w, bool need_gate) {
     if (w == nullptr) return false;
-    if (w->format != MOE_WEIGHTS_BF16 && w->format != MOE_WEIGHTS_FP8_E4M3) return false;
-    const bool q = w->format == MOE_WEIGHTS_FP8_E4M3;
+    const int fmt = w->format;
+    if (fmt != MOE_WEIGHTS_BF16 && fmt != MOE_WEIGHTS_FP8_E4M3 && fmt != MOE_WEIGHTS_INT4_G128) return false;
     if (need_gate && (w->Wg == nullptr || !aligned16(w->Wg))) return false;
-    const void *req_bf[] = {w->W1, w->b1, w->W2, w->b2};
-    const void *req_q[] = {w->W1q, w->s1, w->b1, w->W2q, w->s2, w->b2};
-    for (const void *p : req_bf)
-        if (!q && (p == nullptr || !aligned16(p))) return false;
-    for (const void *p : req_q)
-        if (q && (p == nullptr || !aligned16(p))) return false;
-    if (s->has_shared) {
-        const void *sh_bf[] = {w->Ws1, w->bs1, w->Ws2, w->bs2};
-        const void *sh_q[] = {w->Ws1q, w->ss1, w->bs1, w->Ws2q, w->ss2, w->bs2};
-        for (const void *p : sh_bf)
-            if (!q && (p == nullptr || !aligned16(p))) return false;
-        for (const void *p : sh_q)
-            if (q && (p == nullptr || !aligned16(p))) return false;
-    }
-    return true;
+    auto all = [](std::initializer_list<const void *> ps) {
+        for (const void *p : ps)
+            if (p == nullptr || !aligned16(p)) return false;
+        return true;
+    };
+    bool ok = fmt == MOE_WEIGHTS_BF16        ? all({w->W1, w->b1, w->W2, w->b2})
+              : fmt == MOE_WEIGHTS_FP8_E4M3 ? all({w->W1q, w->s1, w->b1, w->W2q, w->s2, w->b2})
+                                             : all({w->W1q, w->g1, w->b1, w->W2q, w->g2, w->b2});
+    if (ok && s->has_shared)
+        ok = fmt == MOE_WEIGHTS_BF16        ? all({w->Ws1, w->bs1, w->Ws2, w->bs2})
+             : fmt == MOE_WEIGHTS_FP8_E4M3 ? all({w->Ws1q, w->ss1, w->bs1, w->Ws2q, w->ss2, w->bs2})
+                                            : all({w->Ws1q, w->gs1, w->bs1, w->Ws2q, w->gs2, w->bs2});
+    return ok;
+}
+
+// INT4 scales come in groups of 128 reduction columns: both reductions (d_model
+// for the first Linear, d_ff for the second) must hold whole groups.
+bool weights_shape_supported(const moe_shape *s, const moe_weights *w) {
+    return w->format != MOE_WEIGHTS_INT4_G128 || (s->d_model % 128 == 0 && s->d_ff % 128 == 0);
 }
 
 }  // namespace
@@ -1249,6 +1269,7 @@ moe_status moe_expert_ffn(const moe_shape *shape, const moe_bf16 *x_perm, const 
     moe_status r = check_shape(shape);
     if (r != MOE_OK) return r;
     if (!x_perm || !expert_offsets || !y_perm || !weights_ok(shape, weights, false)) return MOE_ERR_INVALID_ARG;
+    if (!weights_shape_supported(shape, weights)) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
     if (shape->has_shared && (!x || !z_shared || !aligned16(x) || !aligned16(z_shared)))
         return MOE_ERR_INVALID_ARG;
@@ -1287,6 +1308,7 @@ moe_status forward_impl(const moe_shape *shape, const moe_weights *weights, cons
     moe_status r = check_shape(shape);
     if (r != MOE_OK) return r;
     if (!x || !y || !aligned16(x) || !aligned16(y) || !weights_ok(shape, weights, true)) return MOE_ERR_INVALID_ARG;
+    if (!weights_shape_supported(shape, weights)) return MOE_ERR_UNSUPPORTED;
     if ((r = check_ws(shape, MOE_WS_FORWARD, workspace, workspace_bytes)) != MOE_OK) return r;
     DeviceState *dev;
     if ((r = device_state(&dev)) != MOE_OK) return r;
@@ -1392,6 +1414,7 @@ moe_status moe_forward_hostio_batches(const moe_shape *shape, const moe_weights 
     if (nbatch < 1 || !x_host || !y_host || !x_dev || !y_dev || !aligned16(x_dev) || !aligned16(y_dev))
         return MOE_ERR_INVALID_ARG;
     if (!weights_ok(shape, weights, true)) return MOE_ERR_INVALID_ARG;
+    if (!weights_shape_supported(shape, weights)) return MOE_ERR_UNSUPPORTED;
     if ((r = check_ws(shape, MOE_WS_FORWARD, workspace, workspace_bytes)) != MOE_OK) return r;
     DeviceState *dev;
     if ((r = device_state(&dev)) != MOE_OK) return r;

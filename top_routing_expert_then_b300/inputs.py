@@ -52,7 +52,8 @@ class MoEConfig:
     z_beta: float = 1e-3
     rank_major: bool = False   # capacity priority: earlier ranks first instead of earlier tokens
     kl_coef: float = 0.02      # KL-to-uniform balance-loss variant
-    weights: str = "bf16"      # expert weight format: "bf16" or "fp8_e4m3" (per-output-channel scales)
+    weights: str = "bf16"      # expert weight format: "bf16", "fp8_e4m3" (per-output-channel scales)
+                               # or "int4_g128" (4-bit codes, a bf16 scale per 128 reduction columns)
     note: str = ""
 
     def with_(self, **kw) -> "MoEConfig":
@@ -85,6 +86,10 @@ CONFIGS: Dict[str, MoEConfig] = {
                               note="64 experts of the DeepSeek-V3 shape, 128 rows per expert"),
     "mixtral_decode16_fp8": MoEConfig("mixtral_decode16_fp8", 16, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
                                       note="Mixtral-shaped decode, 16 tokens, FP8 E4M3 expert weights"),
+    "mixtral_decode16_int4": MoEConfig("mixtral_decode16_int4", 16, 4096, 14336, 8, 2, 0.0, weights="int4_g128",
+                                       note="Mixtral-shaped decode, 16 tokens, INT4 group-wise expert weights"),
+    "mixtral_decode64_int4": MoEConfig("mixtral_decode64_int4", 64, 4096, 14336, 8, 2, 0.0, weights="int4_g128",
+                                       note="Mixtral-shaped decode, 64 tokens, INT4 group-wise expert weights"),
     "mixtral_decode64_fp8": MoEConfig("mixtral_decode64_fp8", 64, 4096, 14336, 8, 2, 0.0, weights="fp8_e4m3",
                                       note="Mixtral-shaped decode, 64 tokens, FP8 E4M3 expert weights"),
 }
@@ -105,7 +110,7 @@ class MoEInputs:
     Ws2: Optional[torch.Tensor] = None       # [d, f] bf16
     bs2: Optional[torch.Tensor] = None       # [d] fp32
     extra: Dict[str, torch.Tensor] = field(default_factory=dict)
-    quant: Optional["QuantWeights"] = None   # FP8 expert weights (cfg.weights == "fp8_e4m3")
+    quant: Optional["QuantWeights"] = None   # quantised expert weights (cfg.weights != "bf16")
 
     def to(self, device) -> "MoEInputs":
         def mv(t):
@@ -119,22 +124,33 @@ class MoEInputs:
 
 @dataclass
 class QuantWeights:
-    """FP8 E4M3 expert weights: uint8 codes in nn.Linear layout and one fp32
-    scale per output channel (dequantised weight = code value * scale)."""
-    W1q: torch.Tensor                      # [N, f, d] uint8
-    s1: torch.Tensor                       # [N, f] fp32
-    W2q: torch.Tensor                      # [N, d, f] uint8
-    s2: torch.Tensor                       # [N, d] fp32
-    Ws1q: Optional[torch.Tensor] = None    # [f, d] uint8
-    ss1: Optional[torch.Tensor] = None     # [f] fp32
-    Ws2q: Optional[torch.Tensor] = None    # [d, f] uint8
-    ss2: Optional[torch.Tensor] = None     # [d] fp32
+    """Quantised expert weights.
+
+    format "fp8_e4m3": uint8 E4M3 codes in nn.Linear layout and one fp32 scale
+    per output channel (dequantised weight = code value * scale):
+    W1q [N, f, d], s1 [N, f], W2q [N, d, f], s2 [N, d] (shared: [f, d], [f],
+    [d, f], [d]).
+    format "int4_g128": 4-bit codes packed two per byte along the reduction
+    dimension (even column in the low nibble; code c stands for c - 8) and one
+    bf16 scale per output channel and group of 128 reduction columns, stored
+    group-major (dequantised weight = bf16(RNE) of (c - 8) * scale):
+    W1q [N, f, d / 2], s1 [N, d / 128, f], W2q [N, d, f / 2], s2 [N, f / 128, d]
+    (shared: [f, d / 2], [d / 128, f], [d, f / 2], [f / 128, d])."""
+    W1q: torch.Tensor
+    s1: torch.Tensor
+    W2q: torch.Tensor
+    s2: torch.Tensor
+    Ws1q: Optional[torch.Tensor] = None
+    ss1: Optional[torch.Tensor] = None
+    Ws2q: Optional[torch.Tensor] = None
+    ss2: Optional[torch.Tensor] = None
+    format: str = "fp8_e4m3"
 
     def to(self, device) -> "QuantWeights":
         def mv(t):
             return None if t is None else t.to(device)
         return QuantWeights(mv(self.W1q), mv(self.s1), mv(self.W2q), mv(self.s2), mv(self.Ws1q),
-                            mv(self.ss1), mv(self.Ws2q), mv(self.ss2))
+                            mv(self.ss1), mv(self.Ws2q), mv(self.ss2), self.format)
 
 
 FP8_E4M3_MAX = 448.0
@@ -150,6 +166,26 @@ def fp8_codes(W: torch.Tensor):
     scale = (amax / FP8_E4M3_MAX).to(torch.float32)
     q = (w / scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
     return q.contiguous(), scale.contiguous()
+
+
+INT4_GROUP = 128
+
+
+def int4_codes(W: torch.Tensor):
+    """Synthetic INT4 group-wise weights for a stack of nn.Linear matrices
+    [..., out, in] (in a multiple of 128): per output row and group of 128
+    reduction columns, scale = bf16(largest magnitude / 7) and code = clamp(
+    round(W / scale), -8, 7) + 8, packed two per byte (even column in the
+    low nibble); scales returned group-major [..., in / 128, out]. (Data
+    preparation only: calibrated quantisers need real data.)"""
+    w = W.to(torch.float32)
+    *lead, out, inn = w.shape
+    g = w.reshape(*lead, out, inn // INT4_GROUP, INT4_GROUP)
+    scale = (g.abs().amax(dim=-1).clamp_min(1e-30) / 7.0).to(torch.bfloat16)
+    q = torch.round(g / scale.to(torch.float32)[..., None]).clamp(-8, 7).to(torch.int32) + 8
+    q = q.reshape(*lead, out, inn)
+    packed = (q[..., 0::2] | (q[..., 1::2] << 4)).to(torch.uint8)
+    return packed.contiguous(), scale.transpose(-1, -2).contiguous()
 
 
 ZIPF_AMPLITUDE_64THS = 16
@@ -212,6 +248,13 @@ def make_inputs(cfg: MoEConfig | str, seed: int = 0, device="cpu") -> MoEInputs:
         bs2 = torch.randn((d,), generator=g, device=device, dtype=torch.float32) * 0.02
 
     quant = None
+    if cfg.weights == "int4_g128":
+        W1q, s1 = int4_codes(W1)
+        W2q, s2 = int4_codes(W2)
+        quant = QuantWeights(W1q, s1, W2q, s2, format="int4_g128")
+        if cfg.has_shared:
+            quant.Ws1q, quant.ss1 = int4_codes(Ws1)
+            quant.Ws2q, quant.ss2 = int4_codes(Ws2)
     if cfg.weights == "fp8_e4m3":
         W1q, s1 = fp8_codes(W1)
         W2q, s2 = fp8_codes(W2)
@@ -219,7 +262,7 @@ def make_inputs(cfg: MoEConfig | str, seed: int = 0, device="cpu") -> MoEInputs:
         if cfg.has_shared:
             quant.Ws1q, quant.ss1 = fp8_codes(Ws1)
             quant.Ws2q, quant.ss2 = fp8_codes(Ws2)
-    elif cfg.weights != "bf16":
+    elif cfg.weights not in ("bf16", "int4_g128"):
         raise ValueError(f"unknown weight format {cfg.weights!r}")
 
     return MoEInputs(cfg, x, Wg, W1, b1, W2, b2, sel_bias, Ws1, bs1, Ws2, bs2, quant=quant)

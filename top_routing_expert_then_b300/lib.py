@@ -42,13 +42,14 @@ class MoeShape(ctypes.Structure):
                 ("drop_policy", ctypes.c_int32), ("kl_coef", ctypes.c_float)]
 
 
-MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3 = 0, 1
+MOE_WEIGHTS_BF16, MOE_WEIGHTS_FP8_E4M3, MOE_WEIGHTS_INT4_G128 = 0, 1, 2
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_void_p) for n in ("Wg", "W1", "b1", "W2", "b2", "Ws1", "bs1", "Ws2", "bs2")]
                 + [("format", ctypes.c_int32)]
-                + [(n, ctypes.c_void_p) for n in ("W1q", "s1", "W2q", "s2", "Ws1q", "ss1", "Ws2q", "ss2")])
+                + [(n, ctypes.c_void_p) for n in ("W1q", "s1", "W2q", "s2", "Ws1q", "ss1", "Ws2q", "ss2")]
+                + [(n, ctypes.c_void_p) for n in ("g1", "g2", "gs1", "gs2")])
 
 
 class MoeGrads(ctypes.Structure):
@@ -234,13 +235,20 @@ def dispatch(shape: MoeShape, topk_idx, x, ws=None, stream=None):
 
 
 def weights_struct(W1, b1, W2, b2, Wg=None, Ws1=None, bs1=None, Ws2=None, bs2=None, quant=None) -> MoeWeights:
-    """The C struct; with ``quant`` (FP8 codes and scales: W1q, s1, W2q, s2 and
-    the shared expert's Ws1q, ss1, Ws2q, ss2) the expert matrices are FP8."""
+    """The C struct; with ``quant`` (codes and scales W1q, s1, W2q, s2 and the
+    shared expert's Ws1q, ss1, Ws2q, ss2) the expert matrices are FP8 with fp32
+    channel scales, or (quant.format == "int4_g128") INT4 with bf16 group
+    scales (passed as g1, g2, gs1, gs2)."""
     bf, f32, u8 = torch.bfloat16, torch.float32, torch.uint8
     w = MoeWeights(_ptr(Wg, bf, "Wg"), _ptr(W1, bf, "W1"), _ptr(b1, f32, "b1"), _ptr(W2, bf, "W2"),
                    _ptr(b2, f32, "b2"), _ptr(Ws1, bf, "Ws1"), _ptr(bs1, f32, "bs1"), _ptr(Ws2, bf, "Ws2"),
                    _ptr(bs2, f32, "bs2"), MOE_WEIGHTS_BF16)
-    if quant is not None:
+    if quant is not None and getattr(quant, "format", "fp8_e4m3") == "int4_g128":
+        w.format = MOE_WEIGHTS_INT4_G128
+        for n, dt, field in (("W1q", u8, "W1q"), ("s1", bf, "g1"), ("W2q", u8, "W2q"), ("s2", bf, "g2"),
+                             ("Ws1q", u8, "Ws1q"), ("ss1", bf, "gs1"), ("Ws2q", u8, "Ws2q"), ("ss2", bf, "gs2")):
+            setattr(w, field, _ptr(getattr(quant, n), dt, n))
+    elif quant is not None:
         w.format = MOE_WEIGHTS_FP8_E4M3
         for n, dt in (("W1q", u8), ("s1", f32), ("W2q", u8), ("s2", f32), ("Ws1q", u8), ("ss1", f32),
                       ("Ws2q", u8), ("ss2", f32)):
@@ -251,8 +259,12 @@ def weights_struct(W1, b1, W2, b2, Wg=None, Ws1=None, bs1=None, Ws2=None, bs2=No
 def _check_weights(shape: MoeShape, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None, bs2=None, Wg=None, quant=None):
     N, d, f = shape.N, shape.d_model, shape.d_ff
     want = {"b1": (b1, (N, f)), "b2": (b2, (N, d))}
+    int4 = quant is not None and getattr(quant, "format", "fp8_e4m3") == "int4_g128"
     if quant is None:
         want.update({"W1": (W1, (N, f, d)), "W2": (W2, (N, d, f))})
+    elif int4:
+        want.update({"W1q": (quant.W1q, (N, f, d // 2)), "s1": (quant.s1, (N, d // 128, f)),
+                     "W2q": (quant.W2q, (N, d, f // 2)), "s2": (quant.s2, (N, f // 128, d))})
     else:
         want.update({"W1q": (quant.W1q, (N, f, d)), "s1": (quant.s1, (N, f)), "W2q": (quant.W2q, (N, d, f)),
                      "s2": (quant.s2, (N, d))})
@@ -262,6 +274,9 @@ def _check_weights(shape: MoeShape, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None
         want.update({"bs1": (bs1, (f,)), "bs2": (bs2, (d,))})
         if quant is None:
             want.update({"Ws1": (Ws1, (f, d)), "Ws2": (Ws2, (d, f))})
+        elif int4:
+            want.update({"Ws1q": (quant.Ws1q, (f, d // 2)), "ss1": (quant.ss1, (d // 128, f)),
+                         "Ws2q": (quant.Ws2q, (d, f // 2)), "ss2": (quant.ss2, (f // 128, d))})
         else:
             want.update({"Ws1q": (quant.Ws1q, (f, d)), "ss1": (quant.ss1, (f,)), "Ws2q": (quant.Ws2q, (d, f)),
                          "ss2": (quant.ss2, (d,))})
@@ -272,7 +287,7 @@ def _check_weights(shape: MoeShape, W1, b1, W2, b2, Ws1=None, bs1=None, Ws2=None
 
 def expert_ffn(shape: MoeShape, x_perm, expert_offsets, W1, b1, W2, b2, x=None, Ws1=None, bs1=None, Ws2=None,
                bs2=None, ws=None, stream=None, quant=None):
-    """-> (y_perm [T*K, d], z [T, d] or None); ``quant``: FP8 expert weights."""
+    """-> (y_perm [T*K, d], z [T, d] or None); ``quant``: quantised expert weights."""
     T, K, d = shape.T, shape.K, shape.d_model
     _check_weights(shape, W1, b1, W2, b2, Ws1, bs1, Ws2, bs2, quant=quant)
     dev = x_perm.device
