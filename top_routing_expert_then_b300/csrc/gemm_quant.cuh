@@ -84,12 +84,14 @@ struct QFormat<QF_FP8> {
 template <>
 struct QFormat<QF_INT4> {
     static constexpr int ROW_BYTES = QT_KPAIR / 2;  // two codes a byte
-    static constexpr int RSTAGES = 20;
+    static constexpr int RSTAGES = 18;
 };
 constexpr int QT_RAW_K = QFormat<QF_FP8>::ROW_BYTES;        // FP8 raw row: 128 bytes
 constexpr int QT_RAW_BYTES = QT_CH * QT_RAW_K;                // 16 KB
-constexpr int QT_RSTAGES = QFormat<QF_FP8>::RSTAGES;         // the byte budget of both rings:
-static_assert(QFormat<QF_INT4>::RSTAGES * QT_CH * QFormat<QF_INT4>::ROW_BYTES == QT_RSTAGES * QT_RAW_BYTES,
+constexpr int QT_RSTAGES = QFormat<QF_FP8>::RSTAGES;         // the raw-ring budget (160 KB) both use:
+constexpr int QT_SCALE_BYTES = QT_CH * 2;                    // INT4: a stage's 128 bf16 group scales
+static_assert(QFormat<QF_INT4>::RSTAGES * (QT_CH * QFormat<QF_INT4>::ROW_BYTES + QT_SCALE_BYTES) <=
+                  QT_RSTAGES * QT_RAW_BYTES,
               "raw ring budget");
 constexpr int QT_MAX_RSTAGES = QFormat<QF_INT4>::RSTAGES;
 constexpr int QT_TBOX = 16;                     // token rows per TMA box
@@ -267,6 +269,14 @@ __device__ __forceinline__ Tile qt_tile(const Params &p, int w, int num_m, int n
     return t;
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, a multiple of 16
+// bytes) that completes on the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // wscale: FP8, the per-channel fp32 scales [groups * n_out]; gscale: INT4,
 // the bf16 group scales [groups][k_dim / 128][n_out].
 template <int F>
@@ -280,7 +290,8 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *rawbuf = smem;
-    uint8_t *tokbuf = rawbuf + RS * RAWB;
+    uint8_t *scalebuf = rawbuf + RS * RAWB;  // INT4: each raw stage's 128 group scales
+    uint8_t *tokbuf = rawbuf + QT_RSTAGES * QT_RAW_BYTES;
     QTShared *sh = reinterpret_cast<QTShared *>(tokbuf + QT_STAGES * QT_TOK_BYTES);
 
     const int warp = warp_id();
@@ -326,6 +337,7 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
     const int total = num_m * num_n * splits;
     const int kblocks = p.k_dim / BK;
     const int kpairs = (kblocks + 1) / 2;
+    const int kgroups = p.k_dim / QT_KPAIR;  // INT4: scale groups per row (= k-pairs)
     // work item w: tile w / splits, k-pairs [split_k0(w), split_k0(w + 1)) of it
     // (the last split of a tile ends at kpairs); kpairs * splits < 2^31
     auto split_k0 = [&](int w) { return (w % splits) * kpairs / splits; };
@@ -350,8 +362,12 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                     }
                     // the second half of an odd k count's last pair reads zeros past k_dim;
                     // channels past the tensor's last row read zeros too
-                    mbar_arrive_expect_tx(smem_u32(&sh->raw_full[r]), RAWB);
+                    mbar_arrive_expect_tx(smem_u32(&sh->raw_full[r]), RAWB + (F == QF_INT4 ? QT_SCALE_BYTES : 0));
                     tma_load_2d(smem_u32(rawbuf + r * RAWB), &tmBq, smem_u32(&sh->raw_full[r]), kp * RB, brow);
+                    if (F == QF_INT4)  // the tile's 128 channel scales of this k-pair's group (contiguous)
+                        bulk_g2s(smem_u32(scalebuf + r * QT_SCALE_BYTES),
+                                 gscale + ((size_t)t.group * kgroups + kp) * p.n_out + t.n0, QT_SCALE_BYTES,
+                                 smem_u32(&sh->raw_full[r]));
                 }
             }
             if (stop) {
@@ -526,24 +542,15 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
         // of row ch at c ^ (ch % 8)); INT4 rows of 64 bytes (64-byte swizzle:
         // chunk c at c ^ ((ch / 2) % 4))
         const int sw = F == QF_FP8 ? (ch & 7) : ((ch >> 1) & 3);
-        const int kgroups = p.k_dim / QT_KPAIR;  // INT4 scale groups per row
         const uint32_t tlane = tmem_base + ((uint32_t)(q * 32) << 16) + half * (BK / 2);
         int i = 0;  // k-pairs converted (= raw stages consumed)
         bool stop = false;
         for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
             const Tile t = qt_tile(p, w / splits, num_m, num_n);
             if (!t.ok) continue;
-            const int k0 = split_k0(w), k1 = split_k1(w);
-            // INT4: this channel's scales of the item's groups (0 past n_out), each
-            // loaded one k-pair ahead of its use
-            const bool glive = F == QF_INT4 && t.n0 + ch < p.n_out;
-            const uint16_t *grow = gscale + (size_t)t.group * kgroups * p.n_out + t.n0 + ch;
-            uint16_t gnext = glive && k0 < k1 ? __ldg(grow + (size_t)k0 * p.n_out) : (uint16_t)0;
-            for (int kp = k0; kp < k1; ++kp, ++i) {
+            const int k1 = split_k1(w);
+            for (int kp = split_k0(w); kp < k1; ++kp, ++i) {
                 const int r = i % RS, s = i % QT_STAGES;
-                const uint16_t g = gnext;
-                if (glive && kp + 1 < k1) gnext = __ldg(grow + (size_t)(kp + 1) * p.n_out);
-                const __nv_bfloat162 gs = __halves2bfloat162(__ushort_as_bfloat16(g), __ushort_as_bfloat16(g));
                 if (!qt_wait(sh, smem_u32(&sh->raw_full[r]), (uint32_t)(i / RS) & 1u, WAIT_LIMIT_NS, true)) {
                     stop = true;
                     break;
@@ -558,6 +565,9 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                         e4m3x16_to_bf16(in, v + 8 * c);
                     }
                 } else {
+                    // this channel's scale for the k-pair's group (landed with the codes)
+                    const uint16_t g = reinterpret_cast<const uint16_t *>(scalebuf + r * QT_SCALE_BYTES)[ch];
+                    const __nv_bfloat162 gs = __halves2bfloat162(__ushort_as_bfloat16(g), __ushort_as_bfloat16(g));
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const int chunk = half * 2 + c;  // 16-byte chunks (32 codes) of this k-block
