@@ -96,8 +96,11 @@ static_assert(QFormat<QF_INT4>::RSTAGES * (QT_CH * QFormat<QF_INT4>::ROW_BYTES +
 constexpr int QT_MAX_RSTAGES = QFormat<QF_INT4>::RSTAGES;
 constexpr int QT_TBOX = 16;                     // token rows per TMA box
 constexpr int QT_TBOX_BYTES = QT_TBOX * BK * 2;       // 2 KB (two 1024-byte swizzle atoms)
-constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a full token tile
+constexpr int QT_TOK_HALF = QT_ROWS * BK * 2;         // 8 KB: one k-block of a 64-row token tile
 constexpr int QT_TOK_BYTES = 2 * QT_TOK_HALF;         // a k-pair
+constexpr int QT_NARROW_ROWS = 32;                    // launches whose tiles have at most 32 rows ...
+constexpr int QT_NARROW_TSTAGES = 8;                  // ... keep twice as many (half-size) token stages
+constexpr int QT_MAX_TSTAGES = QT_NARROW_TSTAGES;
 constexpr int QT_STAGES = 4;                    // A (TMEM) + token (shared) stages
 constexpr int QT_A_COLS = BK;                   // 128 bf16 per lane = 64 columns
 constexpr int QT_ACC_COL0 = QT_STAGES * QT_A_COLS;    // 256
@@ -107,7 +110,7 @@ static_assert(QT_ACC_COL0 + 4 * QT_ACC_COLS <= QT_TMEM_COLS, "TMEM budget");
 constexpr int QT_CONVERTERS = 256;              // warps 7-14
 constexpr int QT_ISSUER2 = 15;                  // the second MMA issuer warp
 constexpr int QT_NUM_THREADS = 16 * 32;
-constexpr int QT_BAR_BYTES = 512;
+constexpr int QT_BAR_BYTES = 1024;
 constexpr int QT_SMEM_BYTES = QT_RSTAGES * QT_RAW_BYTES + QT_STAGES * QT_TOK_BYTES + QT_BAR_BYTES + 1024;
 static_assert(QT_SMEM_BYTES <= 227 * 1024, "shared memory");
 
@@ -115,8 +118,9 @@ struct QTShared {
     uint64_t raw_full[QT_MAX_RSTAGES];
     uint64_t raw_empty[QT_MAX_RSTAGES];
     uint64_t a_full[QT_STAGES];    // the 8 converter warps wrote the stage's A columns
-    uint64_t tok_full[QT_STAGES];  // the stage's token boxes have landed
-    uint64_t empty[QT_STAGES];     // the MMAs reading the stage have completed
+    uint64_t tok_full[QT_MAX_TSTAGES];   // the token stage's boxes have landed
+    uint64_t tok_empty[QT_MAX_TSTAGES];  // the MMAs reading the token stage have completed
+    uint64_t empty[QT_STAGES];           // the MMAs reading the A stage have completed
     uint64_t tfull[2][2];          // [accumulator buffer][issuer]
     uint64_t tempty[2];
     uint64_t drain[2];
@@ -261,11 +265,27 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Position in a ring of n stages (n known only at run time): stage index
+// and phase parity, advanced one fill at a time, so no division.
+struct RingPos {
+    int n, s;
+    uint32_t ph;
+    __device__ __forceinline__ void next() {
+        if (++s == n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 // Work item -> tile: the bf16 kernels' raster order with 128-channel n-tiles
 // (tile_of numbers n-tiles in units of its own 256-column width).
+// A tile with more rows than the launch's token stages hold is invalid
+// (every role skips it; the epilogue flags it).
 __device__ __forceinline__ Tile qt_tile(const Params &p, int w, int num_m, int num_n) {
     Tile t = tile_of<QT_ROWS>(p, w, num_m, num_n);
     t.n0 = (t.n0 / BN) * QT_CH;
+    if (p.q_rows > 0 && p.q_rows <= QT_NARROW_ROWS && t.rows > QT_NARROW_ROWS) t.ok = false;
     return t;
 }
 
@@ -293,6 +313,14 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
     uint8_t *scalebuf = rawbuf + RS * RAWB;  // INT4: each raw stage's 128 group scales
     uint8_t *tokbuf = rawbuf + QT_RSTAGES * QT_RAW_BYTES;
     QTShared *sh = reinterpret_cast<QTShared *>(tokbuf + QT_STAGES * QT_TOK_BYTES);
+    // Token ring: the MMA reads each k-pair's token tile from it. It is
+    // decoupled from the A ring, and launches whose tiles have at most 32 rows
+    // (decode) split its bytes into twice as many stages, so the token loads
+    // run further ahead of the MMAs.
+    const bool narrow = p.q_rows > 0 && p.q_rows <= QT_NARROW_ROWS;
+    const int tstages = narrow ? QT_NARROW_TSTAGES : QT_STAGES;
+    const int tok_half = (narrow ? QT_NARROW_ROWS : QT_ROWS) * BK * 2;
+    const int tok_bytes = 2 * tok_half;
 
     const int warp = warp_id();
     const int lane = lane_id();
@@ -304,8 +332,11 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
         }
         for (int s = 0; s < QT_STAGES; ++s) {
             mbar_init(smem_u32(&sh->a_full[s]), QT_CONVERTERS / 32);
-            mbar_init(smem_u32(&sh->tok_full[s]), 1);
             mbar_init(smem_u32(&sh->empty[s]), 1);
+        }
+        for (int s = 0; s < QT_MAX_TSTAGES; ++s) {
+            mbar_init(smem_u32(&sh->tok_full[s]), 1);
+            mbar_init(smem_u32(&sh->tok_empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&sh->tfull[a][0]), 1);
@@ -380,17 +411,18 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
     } else if (warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------ token producer
-            int i = 0;
+            RingPos tp{tstages, 0, 0u};
+            int issued_phase[QT_MAX_TSTAGES];
+            for (int s = 0; s < QT_MAX_TSTAGES; ++s) issued_phase[s] = -1;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
                 const Tile t = qt_tile(p, w / splits, num_m, num_n);
                 if (!t.ok) continue;
                 const int boxes = (t.rows + QT_TBOX - 1) / QT_TBOX;
                 const int k1 = split_k1(w);
-                for (int kp = split_k0(w); kp < k1; ++kp, ++i) {
-                    const int s = i % QT_STAGES;
-                    if (!qt_wait(sh, smem_u32(&sh->empty[s]), ((uint32_t)(i / QT_STAGES) & 1u) ^ 1u,
-                                 WAIT_LIMIT_NS, true)) {
+                for (int kp = split_k0(w); kp < k1; ++kp, tp.next()) {
+                    const int s = tp.s;
+                    if (!qt_wait(sh, smem_u32(&sh->tok_empty[s]), tp.ph ^ 1u, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
                     }
@@ -398,14 +430,15 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                     mbar_arrive_expect_tx(smem_u32(&sh->tok_full[s]), (uint32_t)(halves * boxes * QT_TBOX_BYTES));
                     for (int h = 0; h < halves; ++h)
                         for (int b = 0; b < boxes; ++b)
-                            tma_load_2d(smem_u32(tokbuf + s * QT_TOK_BYTES + h * QT_TOK_HALF + b * QT_TBOX_BYTES),
+                            tma_load_2d(smem_u32(tokbuf + s * tok_bytes + h * tok_half + b * QT_TBOX_BYTES),
                                         &tmT, smem_u32(&sh->tok_full[s]), (2 * kp + h) * BK, t.row0 + b * QT_TBOX);
+                    issued_phase[s] = (int)tp.ph;
                 }
             }
-            if (stop) {
-                for (int ii = max(0, i - QT_STAGES); ii < i; ++ii)
-                    qt_wait(sh, smem_u32(&sh->tok_full[ii % QT_STAGES]), (uint32_t)(ii / QT_STAGES) & 1u,
-                            DRAIN_LIMIT_NS, false);
+            if (stop) {  // let this block's copies in flight land before it exits
+                for (int s = 0; s < tstages; ++s)
+                    if (issued_phase[s] >= 0)
+                        qt_wait(sh, smem_u32(&sh->tok_full[s]), (uint32_t)issued_phase[s], DRAIN_LIMIT_NS, false);
             }
         }
         __syncwarp();
@@ -417,6 +450,7 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
             // time than the tensor core, and two issuers overlap.
             const int e = warp == 1 ? 0 : 1;
             int i = 0;
+            RingPos tp{tstages, 0, 0u};  // token stage of k-pair i
             uint32_t acc = 0, acc_phase = 0;
             bool stop = false;
             for (int w = blockIdx.x; w < total && !stop; w += gridDim.x) {
@@ -429,23 +463,23 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + QT_ACC_COL0 + (2 * acc + e) * QT_ACC_COLS;
                 const int k0 = split_k0(w), k1 = split_k1(w);
-                for (int kp = k0; kp < k1; ++kp, ++i) {
+                for (int kp = k0; kp < k1; ++kp, ++i, tp.next()) {
                     if (((kp - k0) & 1) != e) continue;
                     const int s = i % QT_STAGES;
                     const uint32_t ph = (uint32_t)(i / QT_STAGES) & 1u;
                     if (!qt_wait(sh, smem_u32(&sh->a_full[s]), ph, WAIT_LIMIT_NS, true) ||
-                        !qt_wait(sh, smem_u32(&sh->tok_full[s]), ph, WAIT_LIMIT_NS, true)) {
+                        !qt_wait(sh, smem_u32(&sh->tok_full[tp.s]), tp.ph, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_tmem = tmem_base + s * QT_A_COLS;
-                    const uint32_t b_addr = smem_u32(tokbuf + s * QT_TOK_BYTES);
+                    const uint32_t b_addr = smem_u32(tokbuf + tp.s * tok_bytes);
                     if (2 * kp + 1 < kblocks) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_bf16_ta(d_tmem, a_tmem + kk * (UMMA_K / 2),
-                                        sdesc(b_addr + (kk >> 2) * QT_TOK_HALF + (kk & 3) * UMMA_K * 2), idesc,
+                                        sdesc(b_addr + (kk >> 2) * tok_half + (kk & 3) * UMMA_K * 2), idesc,
                                         (kp != k0 + e || kk != 0) ? 1u : 0u);
                     } else {  // an odd k count's last pair: its first k-block only
 #pragma unroll
@@ -454,6 +488,7 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                                         (kp != k0 + e || kk != 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&sh->empty[s]));
+                    mma_commit(smem_u32(&sh->tok_empty[tp.s]));
                 }
                 if (stop) break;
                 // (an issuer without pairs in this tile commits nothing new: the arrival is immediate)

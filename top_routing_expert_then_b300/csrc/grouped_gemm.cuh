@@ -122,6 +122,8 @@ struct Params {
                               // copy warp; tmA is not read), [out_rows] device ints
     const uint16_t *a_ptr;    // the gathered tensor, [a_rows_limit, k_dim] bf16 row-major
     int a_rows_limit;         // rows of the gathered tensor (bounds check of a_rows)
+    int q_rows;               // quantised channel-major kernel: the most rows any tile of the launch
+                              // has (<= 32: half-size token stages, twice as many)
 };
 
 // ---------------------------------------------------------------- PTX wrappers

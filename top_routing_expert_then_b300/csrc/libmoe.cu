@@ -85,8 +85,10 @@ int capacity_of(const moe_shape *s) {
 
 // Capacity of the device tile list: m-tiles of 64 rows (the FP8 kernel's
 // height; the bf16 kernels' 128- and 256-row tiles need fewer).
+// m-tiles of the smallest height any kernel uses (32 rows): an expert's block
+// of r rows takes at most r / 32 + 1 of them
 int max_mtiles(const moe_shape *s) {
-    return (int)(((int64_t)s->T * s->K + 63) / 64) + s->N;
+    return (int)(((int64_t)s->T * s->K + 31) / 32) + s->N;
 }
 
 // ------------------------------------------------------------------ workspace layouts
@@ -786,7 +788,8 @@ moe_status launch_gemm_quant(DeviceState *dev, bool is_int4, const void *A, uint
                              uint64_t b_rows, int k_dim, int n_out, int groups, const float *scale,
                              const uint16_t *gscale, const float *bias, uint16_t *out, int out_rows,
                              const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                             cudaStream_t st, float *part = nullptr, const int32_t *offsets = nullptr) {
+                             cudaStream_t st, float *part = nullptr, const int32_t *offsets = nullptr,
+                             int tile_rows = moe::gg::QT_ROWS) {
     if (is_int4 || !fp8_token_major()) {
         CUtensorMap tt, tb;
         if (!make_tmap(&tt, A, a_rows, (uint64_t)k_dim, moe::gg::QT_TBOX)) return MOE_ERR_CUDA;
@@ -797,6 +800,8 @@ moe_status launch_gemm_quant(DeviceState *dev, bool is_int4, const void *A, uint
         if (!ok) return MOE_ERR_CUDA;
         moe::gg::Params p = fp8_params(k_dim, n_out, groups, bias, out, out_rows, mtiles, num_mtiles, max_tiles,
                                        dense_rows, gelu);
+        // the most rows of any tile: the list's tile height, or the dense rows' (64-row tiles)
+        p.q_rows = mtiles ? tile_rows : std::min(dense_rows, moe::gg::QT_ROWS);
         const int n_tiles = (n_out + moe::gg::QT_CH - 1) / moe::gg::QT_CH;
         const int kpairs = (k_dim / moe::gg::BK + 1) / 2;
         const int m_upper = mtiles ? max_tiles : (dense_rows + moe::gg::QT_ROWS - 1) / moe::gg::QT_ROWS;
@@ -867,7 +872,10 @@ FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
     t.pair_routed = !t.fp8 && !gather && use_pair(per_expert);
     t.pair_routed2 = !t.fp8 && use_pair_gemm2(per_expert, s->d_ff);
     t.pair_shared = !t.fp8 && use_pair(s->T);
-    t.tile_rows = t.fp8 ? (wt->format == MOE_WEIGHTS_FP8_E4M3 && fp8_token_major() ? moe::gg::BM : moe::gg::QT_ROWS)
+    // quantised channel-major kernel: 32-row tiles (more, half-size token
+    // stages) when the experts get at most 32 rows each on average (decode)
+    const int qt_rows = per_expert <= moe::gg::QT_NARROW_ROWS ? moe::gg::QT_NARROW_ROWS : moe::gg::QT_ROWS;
+    t.tile_rows = t.fp8 ? (wt->format == MOE_WEIGHTS_FP8_E4M3 && fp8_token_major() ? moe::gg::BM : qt_rows)
                         : (t.pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
     t.raster = t.pair_routed ? kRasterPair : kRasterSingle;
     t.tile_rows2 = t.fp8 ? t.tile_rows : (t.pair_routed2 ? moe::gg::PAIR_BM : moe::gg::BM);
@@ -904,7 +912,7 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
         // the same four GEMMs with quantised expert weights (FP8 per-channel or INT4 group-wise scales)
         const bool i4 = wt->format == MOE_WEIGHTS_INT4_G128;
         r = launch_gemm_quant(dev, i4, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->g1, wt->b1, w.H,
-                              rows, w.mtiles, w.num_mtiles, mt, 0, true, st, w.part, offsets);
+                              rows, w.mtiles, w.num_mtiles, mt, 0, true, st, w.part, offsets, tl.tile_rows);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
             r = launch_gemm_quant(dev, i4, x, T, wt->Ws1q, f, d, f, 1, wt->ss1, wt->gs1, wt->bs1, w.Hs, T, nullptr,
@@ -913,7 +921,7 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
         }
         if (mid != nullptr && cudaEventRecord(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
         r = launch_gemm_quant(dev, i4, w.H, rows, wt->W2q, (uint64_t)N * d, f, d, N, wt->s2, wt->g2, wt->b2, y_perm,
-                              rows, w.mtiles, w.num_mtiles, mt, 0, false, st, w.part, offsets);
+                              rows, w.mtiles, w.num_mtiles, mt, 0, false, st, w.part, offsets, tl.tile_rows);
         if (r != MOE_OK) return r;
         if (s->has_shared) {
             r = launch_gemm_quant(dev, i4, w.Hs, T, wt->Ws2q, d, f, d, 1, wt->ss2, wt->gs2, wt->bs2, z, T, nullptr,
