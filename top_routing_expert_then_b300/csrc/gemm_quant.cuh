@@ -289,6 +289,23 @@ __device__ __forceinline__ Tile qt_tile(const Params &p, int w, int num_m, int n
     return t;
 }
 
+// 16 bytes from shared memory (a .shared address: the converters' reads of
+// the raw stages stay on the shared-memory path)
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t saddr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(saddr) : "memory");
+    return v;
+}
+
 // 1-D bulk copy global -> shared (both 16-byte aligned, a multiple of 16
 // bytes) that completes on the mbarrier as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -572,7 +589,7 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
         const int q = warp & 3;            // TMEM lane quarter this warp may address
         const int half = (warp - 7) >> 2;  // which k-block of each pair
         const int ch = q * 32 + lane;      // channel = raw row = TMEM lane
-        const uint8_t *rrow = rawbuf + ch * RB;
+        const uint32_t rrow = smem_u32(rawbuf) + (uint32_t)(ch * RB);
         // the raw tile's swizzle: FP8 rows of 128 bytes (128-byte swizzle: chunk c
         // of row ch at c ^ (ch % 8)); INT4 rows of 64 bytes (64-byte swizzle:
         // chunk c at c ^ ((ch / 2) % 4))
@@ -590,23 +607,23 @@ grouped_gemm_quant_kernel(const __grid_constant__ CUtensorMap tmT, const __grid_
                     stop = true;
                     break;
                 }
-                const uint8_t *src = rrow + r * RAWB;
+                const uint32_t src = rrow + (uint32_t)(r * RAWB);
                 uint32_t v[32];
                 if (F == QF_FP8) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int chunk = half * 4 + c;  // 16-byte chunks (16 codes) of this k-block
-                        const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
+                        const uint4 in = lds128(src + (uint32_t)((chunk ^ sw) << 4));
                         e4m3x16_to_bf16(in, v + 8 * c);
                     }
                 } else {
                     // this channel's scale for the k-pair's group (landed with the codes)
-                    const uint16_t g = reinterpret_cast<const uint16_t *>(scalebuf + r * QT_SCALE_BYTES)[ch];
+                    const uint16_t g = lds16(smem_u32(scalebuf) + r * QT_SCALE_BYTES + ch * 2);
                     const __nv_bfloat162 gs = __halves2bfloat162(__ushort_as_bfloat16(g), __ushort_as_bfloat16(g));
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const int chunk = half * 2 + c;  // 16-byte chunks (32 codes) of this k-block
-                        const uint4 in = *reinterpret_cast<const uint4 *>(src + ((chunk ^ sw) << 4));
+                        const uint4 in = lds128(src + (uint32_t)((chunk ^ sw) << 4));
                         int4x32_to_bf16(in, gs, v + 16 * c);
                     }
                 }
