@@ -55,6 +55,10 @@ SMALL = [
     # >= 1024 rows per expert and a long second reduction: the second expert
     # GEMM runs on the SM-pair kernel (256-row tiles, ragged last tiles)
     MoEConfig("pair_gemm2", 1100, 256, 8192, 2, 2, 0.0),
+    # decode-sized bf16 batches (a few rows per expert, x rows gathered): a
+    # shared expert; odd k-block counts and a ragged n tile
+    MoEConfig("bf16_decode_split", 24, 256, 384, 8, 2, 0.0, has_shared=True),
+    MoEConfig("bf16_decode_odd", 40, 192, 320, 6, 2, 0.0, sel_bias=True),
     # FP8 E4M3 expert weights (per-output-channel scales): several n-tiles, a
     # ragged expert, the shared expert, drops
     MoEConfig("fp8_experts", 700, 256, 640, 8, 2, 1.25, weights="fp8_e4m3"),
