@@ -38,11 +38,14 @@
 // Block = 16 warps, one block per SM, persistent over the tile list:
 //   warp 0     raw producer (one lane): TMA of 128 channels x one k-pair of
 //              codes (FP8: 128 bytes a row, 128-byte swizzle, 10-deep ring;
-//              INT4: 64 bytes a row, 64-byte swizzle, 20-deep ring)
+//              INT4: 64 bytes a row, 64-byte swizzle, 18-deep ring, each
+//              stage also receiving the tile's 128 group scales by a bulk copy)
 //   warps 1,15 TMEM allocator (warp 1) + two MMA issuers (one lane each):
 //              even k-pairs into one accumulator, odd into another
 //   warp 2     token producer (one lane): TMA of the tile's rows (16-row
-//              boxes, only the boxes that hold rows) x 64 bf16, two per stage
+//              boxes, only the boxes that hold rows) x 64 bf16, two per stage,
+//              into a token ring of its own: 4 stages, or 8 half-size stages
+//              when the launch's tiles have at most 32 rows (decode)
 //   warps 3-6  epilogue: accumulator lane = channel, column = row; scale,
 //              bias, GELU, bf16, stores (one 64-byte segment per row and warp)
 //   warps 7-14 converters: warp w owns TMEM lanes 32 (w % 4) .. +31 (the
