@@ -859,7 +859,7 @@ moe_status launch_gemm_quant(DeviceState *dev, bool is_int4, const void *A, uint
 // The routed experts' GEMM kernel and its m-tile shape: FP8 (64-row tiles, or
 // 128 token-major), the SM-pair kernel (256) or the single-SM kernel (128).
 struct FfnTiling {
-    bool fp8, pair_routed, pair_routed2, pair_shared;  // fp8: any quantised format
+    bool quant, pair_routed, pair_routed2, pair_shared;  // quant: FP8 or INT4 expert weights
     int tile_rows, raster;    // first expert GEMM's m-tiles
     int tile_rows2, raster2;  // second's (a second list is built when they differ)
 };
@@ -868,18 +868,18 @@ FfnTiling ffn_tiling(const moe_shape *s, const moe_weights *wt, bool gather) {
     int64_t per_expert = (int64_t)s->T * s->K / s->N;
     const int C = capacity_of(s);
     if (per_expert > C) per_expert = C;
-    t.fp8 = wt->format != MOE_WEIGHTS_BF16;
-    t.pair_routed = !t.fp8 && !gather && use_pair(per_expert);
-    t.pair_routed2 = !t.fp8 && use_pair_gemm2(per_expert, s->d_ff);
-    t.pair_shared = !t.fp8 && use_pair(s->T);
+    t.quant = wt->format != MOE_WEIGHTS_BF16;
+    t.pair_routed = !t.quant && !gather && use_pair(per_expert);
+    t.pair_routed2 = !t.quant && use_pair_gemm2(per_expert, s->d_ff);
+    t.pair_shared = !t.quant && use_pair(s->T);
     // quantised channel-major kernel: 32-row tiles (more, half-size token
     // stages) when the experts get at most 32 rows each on average (decode)
     const int qt_rows = per_expert <= moe::gg::QT_NARROW_ROWS ? moe::gg::QT_NARROW_ROWS : moe::gg::QT_ROWS;
-    t.tile_rows = t.fp8 ? (wt->format == MOE_WEIGHTS_FP8_E4M3 && fp8_token_major() ? moe::gg::BM : qt_rows)
+    t.tile_rows = t.quant ? (wt->format == MOE_WEIGHTS_FP8_E4M3 && fp8_token_major() ? moe::gg::BM : qt_rows)
                         : (t.pair_routed ? moe::gg::PAIR_BM : moe::gg::BM);
     t.raster = t.pair_routed ? kRasterPair : kRasterSingle;
-    t.tile_rows2 = t.fp8 ? t.tile_rows : (t.pair_routed2 ? moe::gg::PAIR_BM : moe::gg::BM);
-    t.raster2 = t.fp8 ? t.raster : (t.pair_routed2 ? kRasterPair : kRasterSingle);
+    t.tile_rows2 = t.quant ? t.tile_rows : (t.pair_routed2 ? moe::gg::PAIR_BM : moe::gg::BM);
+    t.raster2 = t.quant ? t.raster : (t.pair_routed2 ? kRasterPair : kRasterSingle);
     return t;
 }
 
@@ -893,7 +893,7 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
     const int rows = T * K;
     const int mt = max_mtiles(s);
     const FfnTiling tl = ffn_tiling(s, wt, gather_rows != nullptr);
-    const bool fp8 = tl.fp8, pair_routed = tl.pair_routed, pair_shared = tl.pair_shared;
+    const bool quant = tl.quant, pair_routed = tl.pair_routed, pair_shared = tl.pair_shared;
     const bool two_lists = tl.tile_rows2 != tl.tile_rows;
     const int4 *mtiles2 = two_lists ? w.mtiles2 : w.mtiles;
     const int *num_mtiles2 = two_lists ? w.num_mtiles2 : w.num_mtiles;
@@ -908,7 +908,7 @@ moe_status run_ffn(const moe_shape *s, DeviceState *dev, const uint16_t *x_perm,
         }
     }
     moe_status r;
-    if (fp8) {
+    if (quant) {
         // the same four GEMMs with quantised expert weights (FP8 per-channel or INT4 group-wise scales)
         const bool i4 = wt->format == MOE_WEIGHTS_INT4_G128;
         r = launch_gemm_quant(dev, i4, x_perm, rows, wt->W1q, (uint64_t)N * f, d, f, N, wt->s1, wt->g1, wt->b1, w.H,
