@@ -133,10 +133,13 @@ typedef struct {
      * supported.
      * MOE_WEIGHTS_INT4_G128: weight-only 4-bit experts (the 4-bit expert
      * weights of lmnt.cn/news/351908 sec. 4.3; the yunthe.com page measures a
-     * 4-bit Mixtral): W1q / W2q / Ws1q / Ws2q hold 4-bit codes packed two per
-     * byte along the reduction dimension (byte j of a row holds column 2j in
-     * its low nibble and 2j + 1 in its high nibble; code c stands for the
-     * integer c - 8), i.e. [N, d_ff, d_model / 2], [N, d_model, d_ff / 2],
+     * 4-bit Mixtral): W1q / W2q / Ws1q / Ws2q hold 4-bit codes along the
+     * reduction dimension, half a byte each: the eight columns 8m .. 8m + 7
+     * of a row form one little-endian 32-bit word (bytes 4m .. 4m + 3 of the
+     * row) with column 8m + 2j in bits 4j .. 4j + 3 and column 8m + 2j + 1 in
+     * bits 16 + 4j .. 19 + 4j, j = 0 .. 3 (so the bytes hold the column pairs
+     * (0, 2), (4, 6), (1, 3), (5, 7), low nibble first); code c stands for the
+     * integer c - 8. Shapes [N, d_ff, d_model / 2], [N, d_model, d_ff / 2],
      * [d_ff, d_model / 2], [d_model, d_ff / 2]; g1 / g2 / gs1 / gs2 hold one
      * bf16 scale per output channel and group of 128 consecutive reduction
      * columns, group-major: [N, d_model / 128, d_ff], [N, d_ff / 128, d_model],

@@ -263,7 +263,8 @@ class Oracle:
 
     def expert_ffn_int4(self, x, offsets, row_token, W1q4, g1, b1, W2q4, g2, b2, want=None) -> np.ndarray:
         """expert_ffn with INT4 group-wise weights: packed codes [N, out, in / 2]
-        (even column in the low nibble) and bf16 group scales [N, in / 128, out]."""
+        (eight columns to a little-endian 32-bit word, column 2j of the run in
+        bits 4j.., 2j + 1 in bits 16 + 4j..) and bf16 group scales [N, in / 128, out]."""
         x = _np(x, np.uint16)
         offsets, row_token = _np(offsets, np.int32), _np(row_token, np.int32)
         W1q4, W2q4 = _np(W1q4, np.uint8), _np(W2q4, np.uint8)

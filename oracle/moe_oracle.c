@@ -283,11 +283,13 @@ static double fp8e4m3_val(uint8_t q)
 double oracle_fp8_value(uint8_t q) { return fp8e4m3_val(q); }
 
 /* INT4 group-wise (the 4-bit expert weights of the lmnt.cn/news/351908 sec.
- * 4.3 remark; the yunthe.com page measures a 4-bit Mixtral): codes packed two
- * per byte along the reduction dimension, the even column in the low nibble;
- * code c stands for the integer c - 8; one bf16 scale per output row and
- * group of 128 consecutive reduction columns. The dequantised weight is
- * (c - 8) * scale rounded to bf16 (RNE): the bf16 value the matrix product
+ * 4.3 remark; the yunthe.com page measures a 4-bit Mixtral): 4-bit codes, the
+ * eight reduction columns 8m .. 8m + 7 of a row in one little-endian 32-bit
+ * word (bytes 4m .. 4m + 3 of the row's packed bytes) whose nibble j (bits
+ * 4j .. 4j + 3) holds column 8m + 2j and nibble j + 4 holds column
+ * 8m + 2j + 1; code c stands for the integer c - 8; one bf16 scale per output
+ * row and group of 128 consecutive reduction columns. The dequantised weight
+ * is (c - 8) * scale rounded to bf16 (RNE): the bf16 value the matrix product
  * consumes. */
 static double int4_dequant(int code, uint16_t scale)
 {
@@ -316,8 +318,10 @@ static double wval(const wmat *m, size_t row, size_t col, size_t cols)
     if (m->q)
         return fp8e4m3_val(m->q[row * cols + col]) * (double)m->scale[row];
     if (m->q4) {
-        const uint8_t byte = m->q4[row * (cols / 2) + col / 2];
-        const int code = (col & 1) ? (byte >> 4) : (byte & 15);
+        const size_t word = col / 8, in_word = col % 8;
+        const size_t nibble = in_word / 2 + 4 * (in_word % 2);
+        const uint8_t byte = m->q4[row * (cols / 2) + 4 * word + nibble / 2];
+        const int code = (nibble & 1) ? (byte >> 4) : (byte & 15);
         return int4_dequant(code, m->gscale[(col / 128) * m->rows + row]);
     }
     return bf16_val(m->bf[row * cols + col]);

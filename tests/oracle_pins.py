@@ -536,12 +536,25 @@ def pin_int4_dequant(orc):
     assert orc.int4_dequant(8, half_bits) == 0.0 and orc.int4_dequant(0, 0x3F80) == -8.0
 
 
+def _int4_pack(codes):
+    """The INT4 byte layout written out bit by bit: each run of eight columns
+    becomes one little-endian 32-bit word whose bits 4j .. 4j + 3 take column
+    2j of the run and bits 16 + 4j .. 19 + 4j column 2j + 1."""
+    *lead, inn = codes.shape
+    runs = codes.reshape(*lead, inn // 8, 8).astype(np.uint32)
+    word = np.zeros(runs.shape[:-1], np.uint32)
+    for j in range(4):
+        word |= runs[..., 2 * j] << np.uint32(4 * j)
+        word |= runs[..., 2 * j + 1] << np.uint32(16 + 4 * j)
+    return word.astype("<u4").view(np.uint8).reshape(*lead, inn // 2)
+
+
 def _int4_weights(rng, out, inn, lead=()):
-    """Random INT4 codes packed two per byte (even column low) and random bf16
-    group scales [..., inn / 128, out]; returns them with the dequantised bf16
-    weights [..., out, inn] computed independently in torch."""
+    """Random INT4 codes in the packed layout and random bf16 group scales
+    [..., inn / 128, out]; returns them with the dequantised bf16 weights
+    [..., out, inn] computed independently in torch."""
     codes = rng.integers(0, 16, size=lead + (out, inn)).astype(np.uint8)
-    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    packed = _int4_pack(codes)
     sc = torch.from_numpy(rng.uniform(0.004, 0.06, size=lead + (inn // 128, out))).to(torch.bfloat16)
     s_full = sc.to(torch.float32).transpose(-1, -2).repeat_interleave(128, dim=-1)   # [..., out, inn]
     w = ((torch.from_numpy(codes.astype(np.float32)) - 8.0) * s_full).to(torch.bfloat16)

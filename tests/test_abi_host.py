@@ -146,3 +146,20 @@ def test_product_path_has_no_fallback():
     assert "oracle" not in src.replace("no CPU", "")
     for forbidden in ("torch.matmul", "F.linear", "torch.topk", "softmax(", "gelu("):
         assert forbidden not in src
+
+
+def test_int4_pack_layout():
+    """The input generator's INT4 packing: codes 0..7 of one run of eight
+    columns form the little-endian word 0x75316420 (column 2j in bits 4j ..,
+    column 2j + 1 in bits 16 + 4j ..), the same bytes the oracle's pins pack
+    bit by bit, and a second run continues at byte 4."""
+    import numpy as np
+    import torch
+    from top_routing_expert_then_b300.inputs import int4_pack
+    from oracle_pins import _int4_pack
+    codes = torch.arange(16, dtype=torch.int32).remainder(16).reshape(1, 16)
+    got = int4_pack(codes).numpy()
+    assert got.tolist() == [[0x20, 0x64, 0x31, 0x75, 0xA8, 0xEC, 0xB9, 0xFD]]
+    rng = np.random.default_rng(5)
+    c = rng.integers(0, 16, size=(3, 5, 256)).astype(np.uint8)
+    assert np.array_equal(int4_pack(torch.from_numpy(c)).numpy(), _int4_pack(c))

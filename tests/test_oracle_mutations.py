@@ -10,8 +10,12 @@ import oracle_pins as pins
 
 # (name, [(exact text in moe_oracle.c, replacement)])
 MUTATIONS = [
-    ("int4_nibble_order_swapped", [("const int code = (col & 1) ? (byte >> 4) : (byte & 15);",
-                                    "const int code = (col & 1) ? (byte & 15) : (byte >> 4);")]),
+    ("int4_nibble_order_swapped", [("const int code = (nibble & 1) ? (byte >> 4) : (byte & 15);",
+                                    "const int code = (nibble & 1) ? (byte & 15) : (byte >> 4);")]),
+    ("int4_two_per_byte_order", [("const size_t nibble = in_word / 2 + 4 * (in_word % 2);",
+                                  "const size_t nibble = in_word;")]),
+    ("int4_pairs_not_split", [("const size_t nibble = in_word / 2 + 4 * (in_word % 2);",
+                               "const size_t nibble = (in_word % 4) * 2 + in_word / 4;")]),
     ("int4_code_offset", [("return bf16_val(bf16_round((double)(code - 8) * bf16_val(scale)));",
                            "return bf16_val(bf16_round((double)(code - 7) * bf16_val(scale)));")]),
     ("int4_dequant_unrounded", [("return bf16_val(bf16_round((double)(code - 8) * bf16_val(scale)));",

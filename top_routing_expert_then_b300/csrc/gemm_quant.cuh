@@ -6,9 +6,10 @@
 //
 //   FP8  E4M3 codes, one fp32 scale per output channel:
 //        out[r, n] = epilogue( scale[g(r), n] * sum_k code(B[g(r) n_out + n, k]) A[r, k] + bias )
-//   INT4 4-bit codes two per byte along k (even column in the low nibble,
-//        code c stands for c - 8), one bf16 scale per output channel and
-//        group of 128 reduction columns:
+//   INT4 4-bit codes along k, eight columns 8m .. 8m + 7 to a little-endian
+//        32-bit word (column 8m + 2j in bits 4j .. 4j + 3, column 8m + 2j + 1
+//        in bits 16 + 4j .. 19 + 4j; code c stands for c - 8), one bf16 scale
+//        per output channel and group of 128 reduction columns:
 //        out[r, n] = epilogue( sum_k bf16((c - 8) * scale[g(r), k / 128, n]) A[r, k] + bias )
 //
 // A decode batch gives each expert a handful of rows, so a token-major tile
@@ -205,26 +206,21 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &in, uint32_t *o) {
     o[7] = e4m3x2_bf16x2(in.w, 0xB3A2u);
 }
 
-// 32 INT4 codes (16 bytes; byte j holds column 2j in its low nibble and
-// 2j + 1 in its high nibble) -> 16 packed bf16 pairs (c - 8) * scale. Each
-// pair is assembled as the bf16 patterns 0x4300 | c (= 128 + c, exact), then
-// 136 is subtracted (exact: c - 8) and one bf16 multiply by the scale rounds
-// the product once (RNE).
+// 32 INT4 codes (16 bytes = four words of eight columns) -> 16 packed bf16
+// pairs (c - 8) * scale. The layout puts a word's columns 2j and 2j + 1 at
+// bits 4j and 16 + 4j, so ((w >> 4j) & 0x000F000F) | 0x43004300 (one shift
+// and one three-input logic op) is the pair as the bf16 patterns 0x4300 | c
+// (= 128 + c, exact); 136 is subtracted (exact: c - 8) and one bf16 multiply
+// by the scale rounds the product once (RNE).
 __device__ __forceinline__ void int4x32_to_bf16(const uint4 &in, __nv_bfloat162 scale, uint32_t *o) {
     const uint32_t words[4] = {in.x, in.y, in.z, in.w};
     const __nv_bfloat162 k136 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x4308u),
                                                    __ushort_as_bfloat16((unsigned short)0x4308u));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = words[i] & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 of the word
-        const uint32_t hi = (words[i] >> 4) & 0x0F0F0F0Fu;  // columns 1, 3, 5, 7
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // byte j of lo into byte 0 and byte j of hi into byte 2
-            const uint32_t sel = (uint32_t)(j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12));
-            uint32_t t;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(lo), "r"(hi), "r"(sel));
-            t = (t & 0x00FF00FFu) | 0x43004300u;
+            const uint32_t t = ((words[i] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;  // columns 8i + 2j, 8i + 2j + 1
             __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&t), k136);
             v = __hmul2(v, scale);
             o[4 * i + j] = *reinterpret_cast<const uint32_t *>(&v);

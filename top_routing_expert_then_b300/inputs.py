@@ -130,10 +130,12 @@ class QuantWeights:
     per output channel (dequantised weight = code value * scale):
     W1q [N, f, d], s1 [N, f], W2q [N, d, f], s2 [N, d] (shared: [f, d], [f],
     [d, f], [d]).
-    format "int4_g128": 4-bit codes packed two per byte along the reduction
-    dimension (even column in the low nibble; code c stands for c - 8) and one
-    bf16 scale per output channel and group of 128 reduction columns, stored
-    group-major (dequantised weight = bf16(RNE) of (c - 8) * scale):
+    format "int4_g128": 4-bit codes, eight consecutive reduction columns
+    8m .. 8m + 7 of a row in one little-endian 32-bit word (bytes 4m .. 4m + 3
+    of the row), column 8m + 2j in bits 4j .. 4j + 3 and column 8m + 2j + 1 in
+    bits 16 + 4j .. 19 + 4j (code c stands for c - 8), and one bf16 scale per
+    output channel and group of 128 reduction columns, stored group-major
+    (dequantised weight = bf16(RNE) of (c - 8) * scale):
     W1q [N, f, d / 2], s1 [N, d / 128, f], W2q [N, d, f / 2], s2 [N, f / 128, d]
     (shared: [f, d / 2], [d / 128, f], [d, f / 2], [f / 128, d])."""
     W1q: torch.Tensor
@@ -175,17 +177,30 @@ def int4_codes(W: torch.Tensor):
     """Synthetic INT4 group-wise weights for a stack of nn.Linear matrices
     [..., out, in] (in a multiple of 128): per output row and group of 128
     reduction columns, scale = bf16(largest magnitude / 7) and code = clamp(
-    round(W / scale), -8, 7) + 8, packed two per byte (even column in the
-    low nibble); scales returned group-major [..., in / 128, out]. (Data
+    round(W / scale), -8, 7) + 8, packed eight to a 32-bit word as
+    `int4_pack` says; scales returned group-major [..., in / 128, out]. (Data
     preparation only: calibrated quantisers need real data.)"""
     w = W.to(torch.float32)
     *lead, out, inn = w.shape
     g = w.reshape(*lead, out, inn // INT4_GROUP, INT4_GROUP)
     scale = (g.abs().amax(dim=-1).clamp_min(1e-30) / 7.0).to(torch.bfloat16)
     q = torch.round(g / scale.to(torch.float32)[..., None]).clamp(-8, 7).to(torch.int32) + 8
-    q = q.reshape(*lead, out, inn)
-    packed = (q[..., 0::2] | (q[..., 1::2] << 4)).to(torch.uint8)
-    return packed.contiguous(), scale.transpose(-1, -2).contiguous()
+    return int4_pack(q.reshape(*lead, out, inn)), scale.transpose(-1, -2).contiguous()
+
+
+def int4_pack(codes: torch.Tensor) -> torch.Tensor:
+    """Pack 4-bit codes [..., in] (in a multiple of 8, values 0..15) into the
+    int4_g128 byte layout [..., in / 2]: columns 8m .. 8m + 7 form one
+    little-endian 32-bit word whose bits 4j .. 4j + 3 hold column 8m + 2j and
+    bits 16 + 4j .. 19 + 4j hold column 8m + 2j + 1 (j = 0 .. 3), so that
+    (word >> 4j) & 0x000F000F is the pair (2j, 2j + 1) in two 16-bit halves."""
+    q = codes.to(torch.int32)
+    *lead, inn = q.shape
+    g = q.reshape(*lead, inn // 8, 8)
+    # byte b of the word: bits 8b .. 8b + 7, i.e. nibbles 2b (low) and 2b + 1
+    word_bytes = [g[..., 0] | (g[..., 2] << 4), g[..., 4] | (g[..., 6] << 4),
+                  g[..., 1] | (g[..., 3] << 4), g[..., 5] | (g[..., 7] << 4)]
+    return torch.stack(word_bytes, dim=-1).to(torch.uint8).reshape(*lead, inn // 2).contiguous()
 
 
 ZIPF_AMPLITUDE_64THS = 16
