@@ -607,10 +607,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
 
     // -------------------------------------------------------- single tile: the plan here
-    // Every CTA's rows, routing weights and expert ids are visible to CTA 0
-    // after the cluster barrier above (release / acquire at cluster scope);
-    // the operand ring is free, so its shared memory is the scratch.
-    if (p.fuse_plan && rank == 0) {
+    // Every CTA's rows, routing weights and expert ids are visible to the
+    // cluster after the barrier above (release / acquire at cluster scope);
+    // the operand ring is free, so its shared memory is the scratch. CTA 0
+    // forms the dispatch plan and the tile lists the GEMMs wait for; the
+    // statistics and losses feed no later kernel, so with a cluster of two or
+    // more CTAs rank 1 forms them at the same time.
+    const uint32_t loss_rank = S > 1 ? 1u : 0u;
+    if (p.fuse_plan && (rank == 0 || rank == loss_rank)) {
         __syncthreads();  // (one CTA: its own row writes)
         int *s_dem = reinterpret_cast<int *>(smem);
         float *s_prob = reinterpret_cast<float *>(s_dem + kMaxN);
@@ -619,29 +623,44 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         float *t_aux = reinterpret_cast<float *>(sc + kThreads);
         float *t_kl = t_aux + kMaxN, *t_var = t_kl + kMaxN;
         unsigned *bits = reinterpret_cast<unsigned *>(t_var + kMaxN);  // kWarps x N
+        const bool stats_here = rank == loss_rank;
         for (int e = threadIdx.x; e < N; e += kThreads) {
             const int dem = __ldcg(p.tile_hist + e);
-            const float prob = __ull2float_rn(__ldcg(p.tile_prob + e)) * plan::kFixUnit;
             s_dem[e] = dem;
-            s_prob[e] = prob;
-            p.st.demand[e] = dem;
-            p.st.prob_sum[e] = prob;
-            if (p.st.mean_weight != nullptr)
-                p.st.mean_weight[e] =
-                    dem > 0 ? __ull2float_rn(__ldcg(p.tile_w + e)) * plan::kFixUnit / (float)dem : 0.f;
+            if (stats_here) {
+                const float prob = __ull2float_rn(__ldcg(p.tile_prob + e)) * plan::kFixUnit;
+                s_prob[e] = prob;
+                p.st.demand[e] = dem;
+                p.st.prob_sum[e] = prob;
+                if (p.st.mean_weight != nullptr)
+                    p.st.mean_weight[e] =
+                        dem > 0 ? __ull2float_rn(__ldcg(p.tile_w + e)) * plan::kFixUnit / (float)dem : 0.f;
+            }
         }
         __syncthreads();
-        plan::expert_offsets(s_dem, N, p.dp.C, s_off, sc, p.dp.kept, p.dp.offsets);
-        plan::assign_tokens(p.topk_idx, p.T, K, N, p.dp.C, s_off, bits, p.dp.slot_of, p.dp.row_token, p.T * K);
-        __syncthreads();
-        if (p.dp.mtiles != nullptr)
-            gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles, p.dp.mtiles,
-                                   p.dp.num_mtiles, sc);
-        __syncthreads();
-        if (p.dp.mtiles2 != nullptr)
-            gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows2, p.dp.raster2, p.dp.max_tiles, p.dp.mtiles2,
-                                   p.dp.num_mtiles2, sc);
-        plan::losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, s_off[N]);
+        int kept_rows = -1;
+        if (rank == 0) {
+            plan::expert_offsets(s_dem, N, p.dp.C, s_off, sc, p.dp.kept, p.dp.offsets);
+            plan::assign_tokens(p.topk_idx, p.T, K, N, p.dp.C, s_off, bits, p.dp.slot_of, p.dp.row_token,
+                                p.T * K);
+            __syncthreads();
+            if (p.dp.mtiles != nullptr)
+                gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows, p.dp.raster, p.dp.max_tiles, p.dp.mtiles,
+                                       p.dp.num_mtiles, sc);
+            __syncthreads();
+            if (p.dp.mtiles2 != nullptr)
+                gg::build_mtiles_block(s_off, N, p.T * K, p.dp.tile_rows2, p.dp.raster2, p.dp.max_tiles,
+                                       p.dp.mtiles2, p.dp.num_mtiles2, sc);
+            kept_rows = s_off[N];
+        } else {  // rows kept = sum of min(demand, C), an integer sum (any order)
+            int v = threadIdx.x < N ? min(s_dem[threadIdx.x], p.dp.C) : 0;
+            v = __reduce_add_sync(0xffffffffu, v);
+            if ((threadIdx.x & 31) == 0) sc[threadIdx.x >> 5] = v;
+            __syncthreads();
+            kept_rows = 0;
+            for (int w = 0; w < kWarps; ++w) kept_rows += sc[w];
+        }
+        if (stats_here) plan::losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, kept_rows);
     }
 }
 
