@@ -1149,7 +1149,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N, int total_rows, int tile_rows,
                                                    int raster, int max_tiles, int4 *__restrict__ mtiles,
                                                    int *__restrict__ num_mtiles, int *sc) {
-    const int e = threadIdx.x, nthr = blockDim.x;
+    const int e = threadIdx.x;
     int cnt = 0, r0 = 0, r1 = 0;
     bool bad = false;
     if (e < N) {
@@ -1164,8 +1164,9 @@ __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N
     if (bad) flag_error(MOE_DEVERR_TILE_LIST);
     sc[e] = cnt;
     __syncthreads();
+    // inclusive scan over the N experts (threads past N hold no tiles)
     int v = cnt;
-    for (int o = 1; o < nthr; o <<= 1) {
+    for (int o = 1; o < N; o <<= 1) {
         int add = (e >= o) ? sc[e - o] : 0;
         __syncthreads();
         sc[e] = v = v + add;
@@ -1187,7 +1188,7 @@ __device__ __forceinline__ void build_mtiles_block(const int32_t *offsets, int N
             mtiles[m] = make_int4(rr, rows, e, ((start + lo) << 16) | (hi - lo));
         }
     }
-    if (e == nthr - 1) *num_mtiles = v < max_tiles ? v : max_tiles;
+    if (e == N - 1) *num_mtiles = v < max_tiles ? v : max_tiles;
 }
 
 __global__ void __launch_bounds__(1024)

@@ -533,8 +533,8 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
             return MOE_ERR_CUDA;
         }
         if (in_router) return launch_status();
-        // one block: statistics and losses from the per-tile rows (and, on the
-        // forward path, the dispatch plan and the m-tile list)
+        // statistics and losses from the per-tile rows; on the forward path a
+        // second block forms the dispatch plan and the m-tile lists meanwhile
         moe::plan::Params q{};
         q.st = plan_stats(s, w, demand, prob_sum, aux, z_loss, aux_kl, health, mean_weight);
         if (dplan != nullptr) q.dp = *dplan;
@@ -542,7 +542,7 @@ moe_status run_route(const moe_shape *s, DeviceState *dev, const uint16_t *x, co
         q.tile_hist = w.tile_hist;
         q.tile_prob = w.tile_prob;
         q.tile_w = w.tile_w;
-        moe::plan::plan_kernel<<<1, moe::plan::kThreads, 0, st>>>(q);
+        moe::plan::plan_kernel<<<dplan != nullptr ? 2 : 1, moe::plan::kThreads, 0, st>>>(q);
         count_launch();
         return launch_status();
     }

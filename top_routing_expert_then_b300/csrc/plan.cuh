@@ -14,9 +14,12 @@
 //              (the CSDN page's MoELayer KL balance loss; +inf for an idle expert),
 //     health = [std_e f_e, drop rate, mean routing entropy, max |logit|],
 //     mean_weight[e] = mean routing weight of the assignments to e.
-// plan_kernel does this in one block of 1024 threads for any number of
-// tiles; a single-tile batch (decode) does it inside the router kernel with
-// the block-level pieces below, which also place its assignments.
+// plan_kernel does this with blocks of 1024 threads for any number of tiles:
+// block 0 the dispatch plan and the m-tile lists, block 1 (or block 0 when
+// there is no plan to form) the statistics and losses, which no later kernel
+// waits for, at the same time; a single-tile batch (decode) does it inside
+// the router kernel with the block-level pieces below, which also place its
+// assignments.
 // Every sum runs in a fixed order, so results do not depend on scheduling:
 // integers for the counts and the fixed-point probability and weight sums;
 // fp32 for the few hundred loss terms, each a non-negative quantity added in a
@@ -194,10 +197,11 @@ __device__ __forceinline__ void assign_tokens(const int32_t *topk_idx, int T, in
     }
 }
 
-// One block of 1024 threads: per-expert totals over the tiles (G lanes, a
-// power of two <= 32, share an expert; lane j of the group takes a contiguous
-// run of tiles, so the tile order is kept by an exclusive scan across the
-// group), then the plan, the m-tile list and the statistics.
+// Blocks of 1024 threads: per-expert totals over the tiles (G lanes, a power
+// of two <= 32, share an expert; lane j of the group takes a contiguous run of
+// tiles, so the tile order is kept by an exclusive scan across the group);
+// then block 0 forms the plan and the m-tile lists, and the last block
+// (block 1 of two, or block 0 alone) the statistics and losses.
 __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
     __shared__ int s_dem[1024], s_off[1025], sc[1024];
     __shared__ float s_prob[1024], t_aux[1024], t_kl[1024], t_var[1024];
@@ -226,7 +230,9 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
         wr += __shfl_xor_sync(0xffffffffu, wr, o, G);
     }
     const int dem = __shfl_sync(0xffffffffu, incl, G - 1, G);
-    if (e < N && p.dp.base != nullptr) {
+    const bool plan_here = blockIdx.x == 0 && p.dp.base != nullptr;
+    const bool stats_here = blockIdx.x == gridDim.x - 1;
+    if (e < N && plan_here) {
         int run = incl - cnt;
         for (int c = c0; c < c1; ++c) {
             const size_t i = (size_t)c * N + e;
@@ -238,14 +244,16 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
         const float prob = __ull2float_rn(pr) * kFixUnit;  // the integer total rounded once, then scaled exactly
         s_dem[e] = dem;
         s_prob[e] = prob;
-        p.st.demand[e] = dem;
-        p.st.prob_sum[e] = prob;
-        if (p.st.mean_weight != nullptr)
-            p.st.mean_weight[e] = dem > 0 ? __ull2float_rn(wr) * kFixUnit / (float)dem : 0.f;
+        if (stats_here) {
+            p.st.demand[e] = dem;
+            p.st.prob_sum[e] = prob;
+            if (p.st.mean_weight != nullptr)
+                p.st.mean_weight[e] = dem > 0 ? __ull2float_rn(wr) * kFixUnit / (float)dem : 0.f;
+        }
     }
     __syncthreads();
     int kept_rows = -1;
-    if (p.dp.base != nullptr) {
+    if (plan_here) {
         expert_offsets(s_dem, N, p.dp.C, s_off, sc, p.dp.kept, p.dp.offsets);
         kept_rows = s_off[N];
         if (p.dp.mtiles != nullptr)
@@ -255,8 +263,15 @@ __global__ void __launch_bounds__(kThreads) plan_kernel(const Params p) {
         if (p.dp.mtiles2 != nullptr)
             gg::build_mtiles_block(s_off, N, p.st.T * p.st.K, p.dp.tile_rows2, p.dp.raster2, p.dp.max_tiles,
                                    p.dp.mtiles2, p.dp.num_mtiles2, sc);
+    } else if (p.dp.base != nullptr) {  // rows kept = sum of min(demand, C), an integer sum (any order)
+        int v = tid < N ? min(s_dem[tid], p.dp.C) : 0;
+        v = __reduce_add_sync(0xffffffffu, v);
+        if ((tid & 31) == 0) sc[tid >> 5] = v;
+        __syncthreads();
+        kept_rows = 0;
+        for (int w = 0; w < kThreads / 32; ++w) kept_rows += sc[w];
     }
-    losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, kept_rows);
+    if (stats_here) losses(p.st, s_dem, s_prob, t_aux, t_kl, t_var, kept_rows);
 }
 
 }  // namespace plan
