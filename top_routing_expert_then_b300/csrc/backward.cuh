@@ -1,7 +1,7 @@
 // backward.cuh -- the layer's backward pass: everything but the four big
 // contractions, which run on the grouped tcgen05 GEMM (grouped_gemm.cuh):
-//   dh  = dO W2            (grouped over experts, W2 transposed per expert)
-//   dx' = da W1            (grouped over experts, W1 transposed per expert)
+//   dh  = dO W2            (grouped over experts, W2 read as stored: N-major B)
+//   dx' = da W1            (grouped over experts, W1 read as stored: N-major B)
 //   dW2 = dO^T h, dW1 = da^T x    (per expert, the expert's tokens as the
 //                           reduction: transposed, 64-padded activation copies)
 // Definitions (the gradient of the forward with the routing held fixed; the
@@ -153,40 +153,6 @@ transpose_grouped_kernel(const uint16_t *__restrict__ in, int R, int C, const in
     for (int i = ty; i < 32; i += 8) {
         const int c = c0 + i;
         if (c < C) out[(size_t)c * ld + col] = tile[tx][i];
-    }
-}
-
-// out[g, b, a] = in[g, a, b] for G matrices [A, B] (bf16), A and B multiples
-// of 64. grid = (B / 64, A / 64, G), 256 threads, one 64 x 64 tile per block:
-// 16-byte loads along the input rows, the tile turned in shared memory (rows
-// 132 bytes apart: scattered 2-byte writes at most 2-way conflicted, 4-byte
-// reads conflict-free), 16-byte stores along the output rows.
-constexpr int kTT = 64;
-__global__ void __launch_bounds__(256)
-batched_transpose_kernel(const uint16_t *__restrict__ in, int A, int B, uint16_t *__restrict__ out) {
-    __shared__ __align__(16) uint16_t tile[kTT][kTT + 2];  // [b - b0][a - a0]
-    const size_t g = blockIdx.z;
-    const int b0 = blockIdx.x * kTT, a0 = blockIdx.y * kTT;
-    const uint16_t *src = in + g * (size_t)A * B;
-    uint16_t *dst = out + g * (size_t)A * B;
-    const int c = threadIdx.x & 7, r = threadIdx.x >> 3;  // 16-byte chunk, row 0..31
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int a = r + 32 * h;
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + (size_t)(a0 + a) * B + b0 + c * 8);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            tile[c * 8 + 2 * j][a] = (uint16_t)(w[j] & 0xFFFFu);
-            tile[c * 8 + 2 * j + 1][a] = (uint16_t)(w[j] >> 16);
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int bb = r + 32 * h;
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(&tile[bb][c * 8]);  // 4-byte aligned
-        *reinterpret_cast<uint4 *>(dst + (size_t)(b0 + bb) * A + a0 + c * 8) = make_uint4(row[0], row[1], row[2], row[3]);
     }
 }
 

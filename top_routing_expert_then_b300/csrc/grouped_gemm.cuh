@@ -124,6 +124,10 @@ struct Params {
     int a_rows_limit;         // rows of the gathered tensor (bounds check of a_rows)
     int q_rows;               // quantised channel-major kernel: the most rows any tile of the launch
                               // has (<= 32: half-size token stages, twice as many)
+    int b_mn;                 // grouped_gemm_kernel: B is given N-major, [num_groups * k_dim, n_out]
+                              // (each group's matrix as stored, reduction rows by output columns),
+                              // loaded as four 64-column boxes per stage and read by the MMA as
+                              // an MN-major operand, so no transposed copy is needed
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -234,6 +238,29 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle:
+// 64 consecutive N elements (128 bytes) per row, 8 reduction rows per
+// 1024-byte swizzle atom; the next 8 rows (SBO) 1024 bytes on, the next 64
+// columns (LBO) one 64-row box (8 KB) on.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((BK * 128) >> 4) << 16;  // LBO: the next 64-column box
+    d |= (uint64_t)(1024 >> 4) << 32;        // SBO: the next 8 reduction rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16_id(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
@@ -627,10 +654,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int brow = t.group * p.n_out + t.n0;
                 const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
                 const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
-                if (PF_DIST > 0)
+                if (PF_DIST > 0 && !p.b_mn)
                     for (int kb = kb0; kb < kb1 && kb < kb0 + PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
                 for (int kb = kb0; kb < kb1; kb += KPS) {
-                    if (PF_DIST > 0 && kb + PF_DIST < kb1) tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
+                    if (PF_DIST > 0 && !p.b_mn && kb + PF_DIST < kb1)
+                        tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
                     if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
                         stop = true;
                         break;
@@ -643,8 +671,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         uint8_t *a_s = smem + stage * G_STAGE_BYTES + part * STAGE_BYTES;
                         const int x = (kb + part) * BK;
                         if (!p.a_rows) load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, x, t.row0, t.rows, pol_a);
-                        if (pol_b) tma_load_2d_hint(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow, pol_b);
-                        else tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow);
+                        if (p.b_mn) {  // reduction rows x..x+63 of the group, four 64-column boxes
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(smem_u32(a_s + A_BYTES + j * (BK * 128)), &tmB, fb, t.n0 + 64 * j,
+                                            t.group * p.k_dim + x);
+                        } else if (pol_b) {
+                            tma_load_2d_hint(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow, pol_b);
+                        } else {
+                            tma_load_2d(smem_u32(a_s + A_BYTES), &tmB, fb, x, brow);
+                        }
                     }
                     issued_phase[stage] = (int)phase;
                     if (++stage == G_STAGES) {
@@ -686,10 +722,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int part = 0; part < nk; ++part) {
                         const uint32_t a_addr = smem_u32(smem + stage * G_STAGE_BYTES + part * STAGE_BYTES);
                         const uint32_t b_addr = a_addr + A_BYTES;
+                        if (p.b_mn) {  // B MN-major: 16 reduction rows = two 1024-byte atoms per MMA
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                            mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
-                                     (kb != kb0 || part != 0 || kk != 0) ? 1u : 0u);
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                                mma_bf16_id(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc_mn(b_addr + kk * 2048),
+                                            IDESC | (1u << 16), (kb != kb0 || part != 0 || kk != 0) ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                                mma_bf16(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc(b_addr + kk * UMMA_K * 2),
+                                         (kb != kb0 || part != 0 || kk != 0) ? 1u : 0u);
+                            }
                         }
                     }
                     mma_commit(smem_u32(&sh->empty[stage]));

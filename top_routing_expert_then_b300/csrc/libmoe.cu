@@ -228,19 +228,19 @@ ForwardWs carve_forward(Carve &c, const moe_shape *s) {
 }
 
 // Backward workspace: the forward's, plus the recomputed pre-activations, the
-// backward intermediates, transposed weights and the transposed, 64-padded
-// activation copies the per-expert weight-gradient GEMMs reduce over.
+// backward intermediates and the transposed, 64-padded activation copies the
+// per-expert weight-gradient GEMMs reduce over (the weights are read as stored).
 struct BackwardWs {
     ForwardWs fwd;
     int4 *mtiles;
     int *num_mtiles;
     float *A1, *DH, *DXP, *L, *DS, *dw;
-    uint16_t *DA, *dO, *W1t, *W2t, *dOT, *HT, *DAT, *XPT;
+    uint16_t *DA, *dO, *dOT, *HT, *DAT, *XPT;
     int32_t *poff;
     size_t ldp;  // columns of the padded transposed copies
     // shared expert
     float *As1, *DHs, *DXs;
-    uint16_t *DAs, *Ws1t, *Ws2t, *dyT, *HsT, *DAsT, *xT;
+    uint16_t *DAs, *dyT, *HsT, *DAsT, *xT;
     int32_t *soff, *spoff;
     size_t ldt;
 };
@@ -258,8 +258,6 @@ BackwardWs carve_backward(Carve &c, const moe_shape *s) {
     w.dw = c.take<float>(R);
     w.DA = c.take<uint16_t>(R * f);
     w.dO = c.take<uint16_t>(R * d);
-    w.W1t = c.take<uint16_t>(N * d * f);
-    w.W2t = c.take<uint16_t>(N * f * d);
     w.ldp = (R + 63) / 64 * 64 + 64 * N;  // >= sum of the 64-padded groups; rows 16-byte aligned
     w.dOT = c.take<uint16_t>(d * w.ldp);
     w.HT = c.take<uint16_t>(f * w.ldp);
@@ -272,8 +270,6 @@ BackwardWs carve_backward(Carve &c, const moe_shape *s) {
         w.DHs = c.take<float>(T * f);
         w.DXs = c.take<float>(T * d);
         w.DAs = c.take<uint16_t>(T * f);
-        w.Ws1t = c.take<uint16_t>(d * f);
-        w.Ws2t = c.take<uint16_t>(f * d);
         w.dyT = c.take<uint16_t>(d * w.ldt);
         w.HsT = c.take<uint16_t>(f * w.ldt);
         w.DAsT = c.take<uint16_t>(f * w.ldt);
@@ -451,7 +447,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
                        cudaStream_t st, float *out_f32 = nullptr, int k_splits = 1, const int *k_ranges = nullptr,
-                       const int32_t *a_rows = nullptr);
+                       const int32_t *a_rows = nullptr, bool b_mn = false);
 
 // The dispatch plan the fused router's plan kernel also forms (forward path):
 // per-chunk bases, kept counts, expert offsets and the grouped GEMMs' m-tile list.
@@ -669,12 +665,19 @@ bool use_pair_gemm2(int64_t expected_rows_per_group, int k_dim) {
 moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_rows_n, const void *B, uint64_t b_rows,
                        int k_dim, int n_out, int groups, const float *bias, uint16_t *out, int out_rows,
                        const int4 *mtiles, const int *num_mtiles, int max_tiles, int dense_rows, bool gelu,
-                       cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges, const int32_t *a_rows) {
+                       cudaStream_t st, float *out_f32, int k_splits, const int *k_ranges, const int32_t *a_rows,
+                       bool b_mn) {
     CUtensorMap ta, tb, tc, ta32;
     const uint32_t b_box = pair ? moe::gg::BN / 2 : moe::gg::BN;
-    if (out_f32 != nullptr || a_rows != nullptr) pair = false;  // fp32 mode and gathered A: single-SM kernel
+    // fp32 mode, gathered A and an N-major B: single-SM kernel
+    if (out_f32 != nullptr || a_rows != nullptr || b_mn) pair = false;
     if (!make_tmap(&ta, A, a_rows_n, (uint64_t)k_dim, 128)) return MOE_ERR_CUDA;
-    if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) return MOE_ERR_CUDA;
+    if (b_mn) {  // B as stored: [groups * k_dim, n_out], 64 x 64 boxes
+        (void)b_rows;
+        if (!make_tmap(&tb, B, (uint64_t)groups * (uint64_t)k_dim, (uint64_t)n_out, 64, 64)) return MOE_ERR_CUDA;
+    } else if (!make_tmap(&tb, B, b_rows, (uint64_t)k_dim, b_box)) {
+        return MOE_ERR_CUDA;
+    }
     if (out != nullptr) {
         if (!make_tmap(&tc, out, (uint64_t)out_rows, (uint64_t)n_out, 32, 32, false)) return MOE_ERR_CUDA;
     } else if (out_f32 != nullptr) {
@@ -702,6 +705,7 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     p.a_rows = a_rows;  // gathered A: the row-gather warp copies rows a_rows[r] of A
     p.a_ptr = static_cast<const uint16_t *>(A);
     p.a_rows_limit = (int)a_rows_n;
+    p.b_mn = b_mn ? 1 : 0;
     if (pair && (out_f32 != nullptr || k_splits != 1)) return MOE_ERR_UNSUPPORTED;
     const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
     p.raster = pair ? kRasterPair : kRasterSingle;
@@ -993,14 +997,6 @@ moe_status transpose_grouped(const uint16_t *in, int R, int C, const int32_t *of
     return launch_status();
 }
 
-moe_status batched_transpose(const uint16_t *in, int G, int A, int B, uint16_t *out, cudaStream_t st) {
-    if (A % moe::bwd::kTT != 0 || B % moe::bwd::kTT != 0) return MOE_ERR_UNSUPPORTED;  // d, d_ff: multiples of 64
-    dim3 grid(B / moe::bwd::kTT, A / moe::bwd::kTT, G);
-    moe::bwd::batched_transpose_kernel<<<grid, 256, 0, st>>>(in, A, B, out);
-    count_launch();
-    return launch_status();
-}
-
 moe_status simt_gemm(const float *a, size_t a_ks, size_t a_ms, const uint16_t *b, size_t ldb, int M, int Nn, int Kk,
                      float *c, size_t ldc, cudaStream_t st) {
     dim3 grid((Nn + moe::bwd::kSB - 1) / moe::bwd::kSB, (M + moe::bwd::kSB - 1) / moe::bwd::kSB);
@@ -1045,15 +1041,14 @@ moe_status run_backward(const moe_shape *s, DeviceState *dev, const moe_weights 
                                                                         dw, w.dO);
     count_launch();
     // ---- routed experts
-    if ((r = batched_transpose(wt->W2, N, d, f, w.W2t, st)) != MOE_OK) return r;  // W2t[e] = W2[e]^T: [f, d]
-    if ((r = batched_transpose(wt->W1, N, f, d, w.W1t, st)) != MOE_OK) return r;  // W1t[e] = W1[e]^T: [d, f]
-    if ((r = launch_gemm(dev, false, w.dO, rows, w.W2t, (uint64_t)N * f, d, f, N, wt->b1, nullptr, rows, w.mtiles,
-                         w.num_mtiles, mt, 0, false, st, w.DH)) != MOE_OK)
+    // dh = dO W2_e and dx' = da W1_e read the weights as stored (N-major B): no transposed copies
+    if ((r = launch_gemm(dev, false, w.dO, rows, wt->W2, (uint64_t)N * d, d, f, N, wt->b1, nullptr, rows, w.mtiles,
+                         w.num_mtiles, mt, 0, false, st, w.DH, 1, nullptr, nullptr, true)) != MOE_OK)
         return r;
     moe::bwd::gelu_backward_kernel<<<rows, moe::bwd::kThreads, 0, st>>>(w.DH, w.A1, wt->b1, fw.offsets, N, f, w.DA);
     count_launch();
-    if ((r = launch_gemm(dev, false, w.DA, rows, w.W1t, (uint64_t)N * d, f, d, N, wt->b2, nullptr, rows, w.mtiles,
-                         w.num_mtiles, mt, 0, false, st, w.DXP)) != MOE_OK)
+    if ((r = launch_gemm(dev, false, w.DA, rows, wt->W1, (uint64_t)N * f, f, d, N, wt->b2, nullptr, rows, w.mtiles,
+                         w.num_mtiles, mt, 0, false, st, w.DXP, 1, nullptr, nullptr, true)) != MOE_OK)
         return r;
     moe::bwd::expert_colsum_kernel<<<dim3((f + 255) / 256, N), moe::bwd::kThreads, 0, st>>>(w.DA, fw.offsets, f,
                                                                                            g->db1);
@@ -1082,15 +1077,13 @@ moe_status run_backward(const moe_shape *s, DeviceState *dev, const moe_weights 
         if ((r = launch_gemm(dev, false, x, T, wt->Ws1, f, d, f, 1, wt->bs1, nullptr, T, nullptr, nullptr, 0, T, false,
                              st, w.As1)) != MOE_OK)
             return r;
-        if ((r = batched_transpose(wt->Ws2, 1, d, f, w.Ws2t, st)) != MOE_OK) return r;
-        if ((r = batched_transpose(wt->Ws1, 1, f, d, w.Ws1t, st)) != MOE_OK) return r;
-        if ((r = launch_gemm(dev, false, dy, T, w.Ws2t, f, d, f, 1, wt->bs1, nullptr, T, nullptr, nullptr, 0, T, false,
-                             st, w.DHs)) != MOE_OK)
+        if ((r = launch_gemm(dev, false, dy, T, wt->Ws2, d, d, f, 1, wt->bs1, nullptr, T, nullptr, nullptr, 0, T, false,
+                             st, w.DHs, 1, nullptr, nullptr, true)) != MOE_OK)
             return r;
         moe::bwd::gelu_backward_kernel<<<T, moe::bwd::kThreads, 0, st>>>(w.DHs, w.As1, wt->bs1, w.soff, 1, f, w.DAs);
         count_launch();
-        if ((r = launch_gemm(dev, false, w.DAs, T, w.Ws1t, d, f, d, 1, wt->bs2, nullptr, T, nullptr, nullptr, 0, T,
-                             false, st, w.DXs)) != MOE_OK)
+        if ((r = launch_gemm(dev, false, w.DAs, T, wt->Ws1, f, f, d, 1, wt->bs2, nullptr, T, nullptr, nullptr, 0, T,
+                             false, st, w.DXs, 1, nullptr, nullptr, true)) != MOE_OK)
             return r;
         moe::bwd::expert_colsum_kernel<<<dim3((f + 255) / 256, 1), moe::bwd::kThreads, 0, st>>>(w.DAs, w.soff, f,
                                                                                                g->dbs1);
