@@ -124,10 +124,6 @@ struct Params {
     int a_rows_limit;         // rows of the gathered tensor (bounds check of a_rows)
     int q_rows;               // quantised channel-major kernel: the most rows any tile of the launch
                               // has (<= 32: half-size token stages, twice as many)
-    int b_mn;                 // grouped_gemm_kernel: B is given N-major, [num_groups * k_dim, n_out]
-                              // (each group's matrix as stored, reduction rows by output columns),
-                              // loaded as four 64-column boxes per stage and read by the MMA as
-                              // an MN-major operand, so no transposed copy is needed
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -461,6 +457,11 @@ __device__ __forceinline__ void load_a_tile(uint32_t dst, const CUtensorMap *tmA
     }
 }
 
+// BMN: B is given N-major, [num_groups * k_dim, n_out] (each group's matrix as
+// stored, reduction rows by output columns), loaded as four 64-column boxes
+// per stage and read by the MMA as an MN-major operand, so no transposed copy
+// is needed (a separate instance: the K-major code is left as it was).
+template <bool BMN>
 __global__ void __launch_bounds__(NUM_THREADS_G, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const Params p,
@@ -654,10 +655,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int brow = t.group * p.n_out + t.n0;
                 const int kb0 = p.k_ranges ? p.k_ranges[w % splits] / BK : (w % splits) * kb_per_split;
                 const int kb1 = p.k_ranges ? p.k_ranges[w % splits + 1] / BK : min(kblocks, kb0 + kb_per_split);
-                if (PF_DIST > 0 && !p.b_mn)
+                if (PF_DIST > 0 && !BMN)
                     for (int kb = kb0; kb < kb1 && kb < kb0 + PF_DIST; ++kb) tma_prefetch_2d(&tmB, kb * BK, brow);
                 for (int kb = kb0; kb < kb1; kb += KPS) {
-                    if (PF_DIST > 0 && !p.b_mn && kb + PF_DIST < kb1)
+                    if (PF_DIST > 0 && !BMN && kb + PF_DIST < kb1)
                         tma_prefetch_2d(&tmB, (kb + PF_DIST) * BK, brow);
                     if (!wait_bounded(sh, smem_u32(&sh->empty[stage]), phase ^ 1u, WAIT_LIMIT_NS, true)) {
                         stop = true;
@@ -671,7 +672,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         uint8_t *a_s = smem + stage * G_STAGE_BYTES + part * STAGE_BYTES;
                         const int x = (kb + part) * BK;
                         if (!p.a_rows) load_a_tile(smem_u32(a_s), &tmA, &tmA32, fb, x, t.row0, t.rows, pol_a);
-                        if (p.b_mn) {  // reduction rows x..x+63 of the group, four 64-column boxes
+                        if constexpr (BMN) {  // reduction rows x..x+63 of the group, four 64-column boxes
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
                                 tma_load_2d(smem_u32(a_s + A_BYTES + j * (BK * 128)), &tmB, fb, t.n0 + 64 * j,
@@ -722,7 +723,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int part = 0; part < nk; ++part) {
                         const uint32_t a_addr = smem_u32(smem + stage * G_STAGE_BYTES + part * STAGE_BYTES);
                         const uint32_t b_addr = a_addr + A_BYTES;
-                        if (p.b_mn) {  // B MN-major: 16 reduction rows = two 1024-byte atoms per MMA
+                        if constexpr (BMN) {  // B MN-major: 16 reduction rows = two 1024-byte atoms per MMA
 #pragma unroll
                             for (int kk = 0; kk < BK / UMMA_K; ++kk)
                                 mma_bf16_id(d_tmem, sdesc(a_addr + kk * UMMA_K * 2), sdesc_mn(b_addr + kk * 2048),

@@ -344,7 +344,10 @@ moe_status device_state(DeviceState **out) {
     std::call_once(st.once, [&st, dev]() {
         cudaError_t e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_kernel,
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe::gg::grouped_gemm_kernel<true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, moe::gg::SMEM_BYTES);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(moe::gg::grouped_gemm_pair_kernel,
@@ -705,7 +708,6 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
     p.a_rows = a_rows;  // gathered A: the row-gather warp copies rows a_rows[r] of A
     p.a_ptr = static_cast<const uint16_t *>(A);
     p.a_rows_limit = (int)a_rows_n;
-    p.b_mn = b_mn ? 1 : 0;
     if (pair && (out_f32 != nullptr || k_splits != 1)) return MOE_ERR_UNSUPPORTED;
     const int tile_m = pair ? moe::gg::PAIR_BM : moe::gg::BM;
     p.raster = pair ? kRasterPair : kRasterSingle;
@@ -723,7 +725,12 @@ moe_status launch_gemm(DeviceState *dev, bool pair, const void *A, uint64_t a_ro
         if (work < grid) grid = (int)work;
         if (grid < 1) grid = 1;
         if (!make_tmap(&ta32, A, a_rows_n, (uint64_t)k_dim, moe::gg::A_CHUNK_ROWS)) return MOE_ERR_CUDA;
-        moe::gg::grouped_gemm_kernel<<<grid, moe::gg::NUM_THREADS_G, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p, ta32);
+        if (b_mn)
+            moe::gg::grouped_gemm_kernel<true><<<grid, moe::gg::NUM_THREADS_G, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc, p,
+                                                                                                       ta32);
+        else
+            moe::gg::grouped_gemm_kernel<false><<<grid, moe::gg::NUM_THREADS_G, moe::gg::SMEM_BYTES, st>>>(ta, tb, tc,
+                                                                                                        p, ta32);
     }
     count_launch();
     return MOE_OK;
